@@ -1,0 +1,317 @@
+"""Pins for the CPU oracle: each check compares it with something other than itself.
+
+* Storage-layout equivalence: a token stream appended chunk by chunk to a plain contiguous
+  cache and scattered into a paged pool through the slot mapping must gather back to the
+  same bytes, and attention must be unchanged by a renaming of physical blocks
+  ("Optional paged KV cache (vLLM-style) — v1 design", Implementation order 1 and 3:
+  gathered fetch bit-equal to a plain cache every step, tolerance 0).
+* Brute force: an explicit scalar loop that reads keys straight out of the pool by
+  (block, offset) arithmetic, sums with math.fsum and never calls the oracle.
+* Closed forms: ctx = 1 returns v_0; identical keys return the mean of V; one dominant key
+  returns its value.
+* Library cross-check: torch scaled_dot_product_attention in fp64 (textbook MHA at g = 1,
+  and GQA with K/V repeated per group).
+* Integers printed on the P3 page (Review, pool guard; Memory accounting).
+* Mutants planted in the oracle (the P3 page's Evidence item 5 list): each must fail a pin.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle.paged_attention as pa
+from continuous_batching_gb300 import workloads as wl
+
+
+# ---------------------------------------------------------------------------- helpers
+
+def brute_force_rows(step: wl.Step, k_pool, v_pool):
+    """Scalar triple loop: for each row, head and key, fetch the key from the pool through
+    table[s][j // bs] and j % bs, and form the softmax-weighted sum in plain Python."""
+    bs = step.block_size
+    g = step.Hq // step.Hkv
+    scale = 1.0 / math.sqrt(step.D)
+    kp = pa.bf16_to_f64(k_pool)
+    vp = pa.bf16_to_f64(v_pool)
+    qf = pa.bf16_to_f64(step.q)
+    out = np.zeros((step.T, step.Hq, step.D))
+    for s in range(step.B):
+        n = int(step.cu_seqlens_q[s + 1] - step.cu_seqlens_q[s])
+        for i in range(n):
+            t = int(step.cu_seqlens_q[s]) + i
+            p = int(step.ctx_lens[s]) - n + i
+            for h in range(step.Hq):
+                kh = h // g
+                scores = []
+                for j in range(p + 1):
+                    blk = int(step.block_table[s][j // bs])
+                    key = kp[blk, j % bs, kh]
+                    scores.append(scale * math.fsum(float(a) * float(b) for a, b in zip(qf[t, h], key)))
+                m = max(scores)
+                w = [math.exp(x - m) for x in scores]
+                z = math.fsum(w)
+                for d in range(step.D):
+                    out[t, h, d] = math.fsum(
+                        w[j] * float(vp[int(step.block_table[s][j // bs]), j % bs, kh, d])
+                        for j in range(p + 1)) / z
+    return out
+
+
+def tiny_mixed(seed=5, D=8):
+    """Two decode rows and two prefill segments (one at offset 0, one at an offset)."""
+    return wl.make_step(Hq=4, Hkv=2, D=D, block_size=4, ctx_lens=[1, 13, 9, 22],
+                        n_q=[1, 1, 9, 6], seed=seed)
+
+
+def run_step(step):
+    return pa.step(step.q, step.k_new, step.v_new, step.k_pool, step.v_pool, step.block_table,
+                   step.cu_seqlens_q, step.ctx_lens, step.Hq, step.block_size)
+
+
+def check_brute_force(step):
+    slots, kp, vp, out = run_step(step)
+    ref = brute_force_rows(step, kp, vp)
+    err = np.abs(out - ref).max()
+    assert err <= 1e-12, f"oracle differs from the brute-force loop by {err}"
+
+
+def check_layout_equivalence(seed=11):
+    """Append a stream chunk by chunk to a contiguous cache and to the paged pool."""
+    rng = np.random.default_rng(seed)
+    Hq, Hkv, D, bs = 4, 2, 8, 4
+    lengths = [23, 9, 17]
+    nblk = [(L + bs - 1) // bs for L in lengths]
+    num_blocks = sum(nblk) + 5
+    perm = rng.permutation(num_blocks)
+    table = np.full((3, max(nblk)), -1, np.int32)
+    off = 0
+    for i, n in enumerate(nblk):
+        table[i, :n] = perm[off:off + n]
+        off += n
+    streams_k = [wl.random_bf16(rng, (L, Hkv, D)) for L in lengths]
+    streams_v = [wl.random_bf16(rng, (L, Hkv, D)) for L in lengths]
+    k_pool = wl.random_bf16(rng, (num_blocks, bs, Hkv, D))
+    v_pool = wl.random_bf16(rng, (num_blocks, bs, Hkv, D))
+    done = [0, 0, 0]
+    while done != lengths:
+        n_q = [min(int(rng.integers(1, 6)), L - d) for L, d in zip(lengths, done)]
+        ctx = [d + n for d, n in zip(done, n_q)]
+        cu = np.concatenate([[0], np.cumsum(n_q)]).astype(np.int32)
+        k_new = np.concatenate([streams_k[i][done[i]:ctx[i]] for i in range(3)])
+        v_new = np.concatenate([streams_v[i][done[i]:ctx[i]] for i in range(3)])
+        ctx_arr = np.asarray(ctx, np.int32)
+        slots = pa.slot_mapping(table, cu, ctx_arr, bs)
+        k_pool = pa.kv_write(k_pool, k_new, slots)
+        v_pool = pa.kv_write(v_pool, v_new, slots)
+        for i in range(3):
+            if ctx[i] == 0:
+                continue
+            got = pa.gather(k_pool, table[i], ctx[i])            # [Hkv, L, D]
+            want = streams_k[i][:ctx[i]].transpose(1, 0, 2)       # plain contiguous cache
+            assert np.array_equal(got, want), "gathered K differs from the contiguous cache"
+            gotv = pa.gather(v_pool, table[i], ctx[i])
+            assert np.array_equal(gotv, streams_v[i][:ctx[i]].transpose(1, 0, 2))
+        done = ctx
+
+
+# ---------------------------------------------------------------------------- pins
+
+def test_layout_equivalence_chunked_stream():
+    check_layout_equivalence()
+
+
+def test_block_renaming_invariance():
+    """Relocate every physical block (table entries renamed accordingly): output bits equal."""
+    st = wl.make_config("tiny")
+    slots, kp, vp, out = run_step(st)
+    rng = np.random.default_rng(99)
+    perm = rng.permutation(st.num_blocks)       # new position of old block b is perm[b]
+    kp2 = np.empty_like(kp)
+    vp2 = np.empty_like(vp)
+    kp2[perm] = kp
+    vp2[perm] = vp
+    table2 = np.where(st.block_table >= 0, perm[np.maximum(st.block_table, 0)], -1).astype(np.int32)
+    out2 = pa.attention(st.q, kp2, vp2, table2, st.cu_seqlens_q, st.ctx_lens, st.Hq)
+    assert np.array_equal(out, out2)
+
+
+@pytest.mark.parametrize("seed", [5, 6])
+def test_brute_force_tiny_mixed(seed):
+    check_brute_force(tiny_mixed(seed))
+
+
+def test_brute_force_tiny_config():
+    """The named tiny workload (D = 64, four decode rows) against the scalar loop."""
+    check_brute_force(wl.make_config("tiny"))
+
+
+def test_ctx_one_returns_v0():
+    st = wl.make_step(Hq=4, Hkv=2, D=16, block_size=4, ctx_lens=[1, 1], n_q=[1, 1], seed=3)
+    slots, kp, vp, out = run_step(st)
+    for s in range(2):
+        v0 = pa.bf16_to_f64(st.v_new[s])          # [Hkv, D]
+        for h in range(4):
+            assert np.array_equal(out[s, h], v0[h // 2])
+
+
+def test_identical_keys_give_mean_of_values():
+    st = wl.make_step(Hq=2, Hkv=1, D=8, block_size=4, ctx_lens=[11], n_q=[3], seed=4)
+    st.k_pool[:] = st.k_pool[0, 0]            # every key identical
+    st.k_new[:] = st.k_pool[0, 0]
+    slots, kp, vp, out = run_step(st)
+    V = pa.bf16_to_f64(pa.gather(vp, st.block_table[0], 11))[0]   # [L, D]
+    for i in range(3):
+        p = 11 - 3 + i
+        want = V[:p + 1].mean(axis=0)
+        assert np.abs(out[i, 0] - want).max() <= 1e-14
+
+
+def test_dominant_key_returns_its_value():
+    st = wl.make_step(Hq=1, Hkv=1, D=8, block_size=4, ctx_lens=[10], n_q=[1], seed=8)
+    slots, kp, vp, _ = run_step(st)
+    K = pa.bf16_to_f64(pa.gather(kp, st.block_table[0], 10))[0]
+    q = np.zeros((1, 1, 8))
+    j = 6
+    q[0, 0] = 400.0 * K[j] / np.linalg.norm(K[j]) ** 2 * math.sqrt(8)   # score gap >> 40
+    out = pa.attention(q, kp, vp, st.block_table, st.cu_seqlens_q, st.ctx_lens, 1)
+    v = pa.bf16_to_f64(pa.gather(vp, st.block_table[0], 10))[0, j]
+    assert np.abs(out[0, 0] - v).max() < 1e-9
+
+
+def _sdpa_reference(st, kp, vp):
+    """torch SDPA in fp64 per sequence, K/V repeated per group (blocked GQA map)."""
+    g = st.Hq // st.Hkv
+    out = np.zeros((st.T, st.Hq, st.D))
+    for s in range(st.B):
+        n = int(st.cu_seqlens_q[s + 1] - st.cu_seqlens_q[s])
+        ctx = int(st.ctx_lens[s])
+        K = torch.from_numpy(pa.bf16_to_f64(pa.gather(kp, st.block_table[s], ctx)))
+        V = torch.from_numpy(pa.bf16_to_f64(pa.gather(vp, st.block_table[s], ctx)))
+        K = K.repeat_interleave(g, dim=0)
+        V = V.repeat_interleave(g, dim=0)
+        q = torch.from_numpy(pa.bf16_to_f64(st.q[st.cu_seqlens_q[s]:st.cu_seqlens_q[s + 1]]))
+        q = q.permute(1, 0, 2)                                  # [Hq, n, D]
+        pos = ctx - n + torch.arange(n)
+        mask = torch.arange(ctx)[None, :] <= pos[:, None]       # [n, ctx]
+        o = torch.nn.functional.scaled_dot_product_attention(q, K, V, attn_mask=mask)
+        out[st.cu_seqlens_q[s]:st.cu_seqlens_q[s + 1]] = o.permute(1, 0, 2).numpy()
+    return out
+
+
+@pytest.mark.parametrize("Hq,Hkv", [(4, 4), (8, 2)])
+def test_matches_torch_sdpa_fp64(Hq, Hkv):
+    st = wl.make_step(Hq=Hq, Hkv=Hkv, D=16, block_size=8, ctx_lens=[5, 40, 33, 70],
+                      n_q=[1, 40, 1, 12], seed=12)
+    slots, kp, vp, out = run_step(st)
+    ref = _sdpa_reference(st, kp, vp)
+    assert np.abs(out - ref).max() <= 1e-12
+
+
+def test_tiny_config_matches_sdpa():
+    st = wl.make_config("tiny")
+    slots, kp, vp, out = run_step(st)
+    assert np.abs(out - _sdpa_reference(st, kp, vp)).max() <= 1e-12
+
+
+def test_slots_land_in_the_right_block_and_offset():
+    """Slot arithmetic on a hand-made table: block 7 then block 2, block size 4."""
+    table = np.array([[7, 2, -1]], np.int32)
+    cu = np.array([0, 3], np.int32)
+    ctx = np.array([6], np.int32)                # positions 3, 4, 5
+    assert pa.slot_mapping(table, cu, ctx, 4).tolist() == [7 * 4 + 3, 2 * 4 + 0, 2 * 4 + 1]
+
+
+def test_page_integer_examples():
+    """Integers printed on the P3 page, stored with their citation in tests/golden."""
+    import json
+    import os
+    g = json.load(open(os.path.join(os.path.dirname(__file__), "golden", "page_integers.json")))
+    pg = g["pool_guard"]
+    assert pa.cached_tokens(pg["prompt"], pg["max_new"]) == pg["cached_tokens"]
+    assert pa.blocks_needed(pg["cached_tokens"], pg["block_size"]) == pg["blocks"]
+    for row in g["kv_bytes_per_token"]:
+        assert pa.kv_bytes_per_token(row["layers"], row["kv_heads"], row["head_dim"],
+                                     row["dtype_bytes"], tp_degree=row["tp"]) == row["bytes"]
+
+
+def test_workload_shapes():
+    want_T = {"tiny": 4, "decode": 64, "mixed": 2096, "longtail": 128, "prefix": 128}
+    for name in wl.CONFIG_NAMES:
+        st = wl.make_config(name, with_pool=False)
+        assert st.T == want_T[name]
+        nb = (st.ctx_lens.astype(np.int64) + st.block_size - 1) // st.block_size
+        for s in range(st.B):
+            row = st.block_table[s]
+            assert np.all(row[:nb[s]] >= 0) and np.all(row[:nb[s]] < st.num_blocks)
+            assert np.all(row[nb[s]:] == -1)
+        used = np.concatenate([st.block_table[s, :nb[s]] for s in range(st.B)])
+        if name == "prefix":
+            assert len(np.unique(used)) == st.num_blocks
+            assert st.shared_blocks == 16 * 64
+        else:
+            assert len(np.unique(used)) == len(used)
+
+
+# ---------------------------------------------------------------------------- mutants
+
+def _gqa_flipped(q_rows, K, V, pos, Hq, scale):
+    Hkv, L, D = K.shape
+    out = np.empty((q_rows.shape[0], Hq, D))
+    for r in range(q_rows.shape[0]):
+        n = int(pos[r]) + 1
+        for h in range(Hq):
+            kh = h % Hkv                         # wrong map
+            s = K[kh, :n] @ q_rows[r, h] * scale
+            w = np.exp(s - s.max())
+            out[r, h] = (w / w.sum()) @ V[kh, :n]
+    return out
+
+
+def _causal_off_by_one(q_rows, K, V, pos, Hq, scale):
+    Hkv, L, D = K.shape
+    g = Hq // Hkv
+    out = np.empty((q_rows.shape[0], Hq, D))
+    for r in range(q_rows.shape[0]):
+        n = max(int(pos[r]), 1)                   # drops the diagonal key
+        for h in range(Hq):
+            s = K[h // g, :n] @ q_rows[r, h] * scale
+            w = np.exp(s - s.max())
+            out[r, h] = (w / w.sum()) @ V[h // g, :n]
+    return out
+
+
+def _gather_drops_last(pool, table_row, ctx):
+    full = _orig_gather(pool, table_row, ctx)
+    return full[:, :max(ctx - 1, 1)] if ctx > 1 else full * 0
+
+
+_orig_gather = pa.gather
+
+
+def _slots_ignore_offset(block_table, cu, ctx, bs):
+    s = _orig_slots(block_table, cu, ctx, bs)
+    return (s // bs) * bs
+
+
+_orig_slots = pa.slot_mapping
+
+
+@pytest.mark.parametrize("name,fn,check", [
+    ("gqa_flipped", "_attend_sequence", "brute"),
+    ("causal_off_by_one", "_attend_sequence", "brute"),
+    ("gather_drops_last_key", "gather", "brute"),
+    ("slot_ignores_offset", "slot_mapping", "layout"),
+])
+def test_planted_mutants_are_killed(monkeypatch, name, fn, check):
+    impl = {"gqa_flipped": _gqa_flipped, "causal_off_by_one": _causal_off_by_one,
+            "gather_drops_last_key": _gather_drops_last,
+            "slot_ignores_offset": _slots_ignore_offset}[name]
+    # control: the unmutated oracle passes
+    (check_brute_force(tiny_mixed(5)) if check == "brute" else check_layout_equivalence())
+    monkeypatch.setattr(pa, fn, impl)
+    with pytest.raises(AssertionError):
+        if check == "brute":
+            check_brute_force(tiny_mixed(5))
+        else:
+            check_layout_equivalence()
