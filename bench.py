@@ -1,0 +1,386 @@
+"""Benchmark of one flat ragged paged-attention step on GB300 (one JSON line on stdout).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+A step is the whole hot path over one batch of synthetic input: the KV-write scatter of the
+step's new K/V rows, then paged attention for every query row (plus the fixed-order split
+combine). The timed workload is the decode batch (Hq 32, Hkv 8, D 128, block 16, 64 decode
+rows, ctx ~ lognormal(median 2048, sigma 1) clipped to [16, 16384]); the metric is decode KV
+GB/s: algorithmic K/V bytes read per step (sum ctx * 2 * Hkv * D * 2 B) / step time. The
+mixed ragged step (48 decode rows + 4 x 512 prefill rows) is reported alongside as tokens/s.
+
+Inputs are resident in HBM before timing; the K/V pools (0.84 GB) exceed the 129 MB L2 and
+L2 is also flushed (a 256 MiB write) between timed steps. Timing: CUDA events on the
+launching stream around each step, W untimed warm-up steps, max over ranks.
+
+--impl reference times the CPU oracle (fp64 numpy) on a bounded sample of the same workload
+on the host cores, with the same metric and unit.
+
+Under torchrun (N > 1) every rank runs its own decode batch (seed + rank) with no data-path
+collective: the path shards by sequence, so scaling is weak.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from continuous_batching_gb300 import workloads as wl  # noqa: E402
+
+METRIC = "paged-attn decode KV GB/s (% of HBM peak) and ragged-step tokens/s, 1×GB300"
+UNIT = "GB/s"
+WORKLOAD = ("decode batch: Hq=32, Hkv=8, D=128, block_size=16, 64 decode rows, ctx lognormal "
+            "(median 2048, sigma 1.0) clipped to [16,16384], pool = sum(ceil(ctx/16)) blocks, "
+            "permuted tables, bf16 ~N(0,1), seed 1")
+MIXED = ("mixed ragged step: 48 decode rows (ctx lognormal median 3000, cap 16384) + 4 chunked-"
+         "prefill segments of 512 rows at prior offsets {0,512,4096,9000}, T=2096, seed 2")
+
+
+def kv_bytes(st: wl.Step) -> int:
+    return int(st.ctx_lens.astype(np.int64).sum()) * 2 * st.Hkv * st.D * 2
+
+
+def prefill_flops(st: wl.Step) -> float:
+    f = 0.0
+    for s in range(st.B):
+        n = int(st.n_q[s])
+        if n > 1:
+            o = int(st.ctx_lens[s]) - n
+            f += 4.0 * st.D * st.Hq * (n * o + n * (n + 1) / 2)
+    return f
+
+
+def load_peaks() -> dict:
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained"), "src": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+            "src": "fallback"}
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for f in ("attention.cu", "tmem_ldst.h", "common.h"):
+        h.update(open(os.path.join(ROOT, "continuous_batching_gb300", "csrc", f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def measured_traffic():
+    """DRAM bytes per attention launch from the committed ncu summary, if it was taken on the
+    current kernel source (else None)."""
+    p = os.path.join(ROOT, "profiles", "attention_decode_traffic.json")
+    if not os.path.exists(p):
+        return None
+    d = json.load(open(p))
+    if d.get("kernel_source_sha256_16") != kernel_source_hash():
+        return None
+    return d.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle samples taken while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self) -> dict:
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------------------------ GPU arm
+
+class GpuStep:
+    """Device-resident inputs for one workload plus the public-API runner."""
+
+    def __init__(self, st: wl.Step, torch, bd):
+        self.st, self.torch, self.bd = st, torch, bd
+        dev = lambda a: torch.from_numpy(a.view(np.int16)).cuda().view(torch.bfloat16)
+        self.shape = bd.Shape.make(st.Hq, st.Hkv, st.D, st.block_size, st.num_blocks)
+        self.kp, self.vp = dev(st.k_pool), dev(st.v_pool)
+        self.q, self.kn, self.vn = dev(st.q), dev(st.k_new), dev(st.v_new)
+        self.out = torch.empty((st.T, st.Hq, st.D), dtype=torch.bfloat16, device="cuda")
+        self.runner = bd.StepRunner(self.shape).prepare(st.cu_seqlens_q, st.ctx_lens,
+                                                        st.block_table)
+        # pinned host copies for the end-to-end measurement
+        pin = lambda a: torch.from_numpy(a.view(np.int16).copy()).pin_memory()
+        self.h_q, self.h_kn, self.h_vn = pin(st.q), pin(st.k_new), pin(st.v_new)
+        self.h_out = torch.empty((st.T, st.Hq, st.D), dtype=torch.int16).pin_memory()
+
+    def launches_per_step(self) -> int:
+        return 2 + (1 if int(self.st.ctx_lens.max()) > self.bd.PA_SPLIT_TOKENS else 0)
+
+    def step(self):
+        self.runner.run(self.q, self.kn, self.vn, self.kp, self.vp, self.out)
+
+    def step_e2e(self):
+        """Public API from host buffers: plan + slots on the host, H2D of inputs and metadata,
+        kernels, D2H of the output."""
+        torch, st = self.torch, self.st
+        self.runner.prepare(st.cu_seqlens_q, st.ctx_lens, st.block_table)
+        self.q.view(torch.int16).copy_(self.h_q, non_blocking=True)
+        self.kn.view(torch.int16).copy_(self.h_kn, non_blocking=True)
+        self.vn.view(torch.int16).copy_(self.h_vn, non_blocking=True)
+        self.step()
+        self.h_out.copy_(self.out.view(torch.int16), non_blocking=True)
+        torch.cuda.current_stream().synchronize()
+
+    def e2e_bytes(self):
+        st = self.st
+        meta = 4 * (st.B + 1 + st.B + st.block_table.size + st.T) + self.runner.h_items.nbytes
+        h2d = st.q.nbytes + st.k_new.nbytes + st.v_new.nbytes + meta
+        return h2d, st.T * st.Hq * st.D * 2
+
+
+def time_steps(g: GpuStep, torch, steps: int, warmup: int, flush, attn_only=False):
+    """Per-step CUDA events (L2 flushed before each step, outside the events).
+    Returns (per-step ms list, per-attention-call ms list)."""
+    s = torch.cuda.current_stream()
+    for _ in range(warmup):
+        g.step()
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+           torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    for i in range(steps):
+        flush.zero_()
+        a, b, c = ev[i]
+        a.record(s)
+        g.runner.write(g.kn, g.vn, g.kp, g.vp)
+        b.record(s)
+        g.runner.attend(g.q, g.kp, g.vp, g.out)
+        c.record(s)
+    torch.cuda.synchronize()
+    step_ms = [a.elapsed_time(c) for a, b, c in ev]
+    attn_ms = [b.elapsed_time(c) for a, b, c in ev]
+    return step_ms, attn_ms
+
+
+def run_ours(args) -> dict:
+    import torch
+
+    from continuous_batching_gb300 import binding as bd
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    bd.load()
+    peaks = load_peaks()
+
+    st = wl.make_config("decode", seed=1 + rank)
+    g = GpuStep(st, torch, bd)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    barrier()
+    t0 = time.perf_counter()
+    with ClockSampler(local) as clk:
+        step_ms, attn_ms = time_steps(g, torch, args.steps, args.warmup, flush)
+        barrier()
+    wall = time.perf_counter() - t0
+    total_ms = sum(step_ms)
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([total_ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / args.steps
+    bytes_step = kv_bytes(st)
+    value = bytes_step * world / (ms_per_step * 1e-3) / 1e9
+
+    # end to end through the public API with host buffers
+    for _ in range(2):
+        g.step_e2e()
+    t1 = time.perf_counter()
+    n_e2e = max(3, args.steps // 2)
+    for _ in range(n_e2e):
+        g.step_e2e()
+    e2e_s = (time.perf_counter() - t1) / n_e2e
+    h2d, d2h = g.e2e_bytes()
+
+    attn_avg = statistics.mean(attn_ms)
+    achieved = bytes_step / (attn_avg * 1e-3) / 1e9
+    roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
+            "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
+            "traffic": measured_traffic(),
+            "kernel": "paged_attention_step (tile routine + split combine)",
+            "peak_src": peaks["src"]}
+
+    # the mixed ragged step (tokens/s) alongside
+    mixed = None
+    if not args.no_mixed:
+        sm = wl.make_config("mixed", seed=2 + rank)
+        gm = GpuStep(sm, torch, bd)
+        m_step, m_attn = time_steps(gm, torch, args.steps, args.warmup, flush)
+        mm = statistics.mean(m_step)
+        pf = prefill_flops(sm)
+        mixed = {"workload": MIXED, "tokens_per_s": round(sm.T / (mm * 1e-3), 1),
+                 "ms_per_step": round(mm, 4),
+                 "prefill_algorithmic_tflop_per_s_over_whole_step": round(pf / (mm * 1e-3) / 1e12, 2),
+                 "tensor_peak_tflops": peaks["bf16_tflops"]}
+        del gm
+
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": WORKLOAD, "kv_bytes_per_step": bytes_step, "T": st.T,
+                   "l2": "inputs larger than L2 (0.84 GB K/V) and L2 flushed by a 256 MiB "
+                         "write between timed steps", "parallelism": f"replicas{world}"},
+        "e2e": {"value": round(bytes_step / e2e_s / 1e9, 2), "unit": UNIT,
+                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+                "ms_per_step": round(e2e_s * 1e3, 4)},
+        "roofline": roof,
+        "gpu_launches": g.launches_per_step() * args.steps,
+        "clocks": clk.summary(),
+        "wall_s_timed_region": round(wall, 3),
+    }
+    if mixed:
+        line["ragged_step"] = mixed
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(st, budget_s=args.cpu_budget)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return line if rank == 0 else None
+
+
+# ---------------------------------------------------------------------- CPU oracle arm
+
+def cpu_baseline(st: wl.Step, budget_s: float = 15.0, rows=None) -> dict:
+    """Times the oracle (fp64 numpy, as it stands) on whole sequences of the workload until
+    about budget_s of CPU work; reports KV GB/s of the sample."""
+    import oracle.paged_attention as pa
+    rng = np.random.default_rng(0)
+    order = rng.permutation(st.B)
+    done_bytes = 0
+    n_seq = 0
+    t0 = time.perf_counter()
+    for s in order:
+        r = np.arange(st.cu_seqlens_q[s], st.cu_seqlens_q[s + 1])
+        pa.attention_rows(st.q, st.k_pool, st.v_pool, st.block_table, st.cu_seqlens_q,
+                          st.ctx_lens, st.Hq, r)
+        done_bytes += int(st.ctx_lens[s]) * 2 * st.Hkv * st.D * 2
+        n_seq += 1
+        if time.perf_counter() - t0 > budget_s:
+            break
+    dt = time.perf_counter() - t0
+    return {"value": round(done_bytes / dt / 1e9, 4), "unit": UNIT, "cores": 1,
+            "kind": "oracle",
+            "sample": f"{n_seq} of {st.B} decode rows (whole sequences, all 32 heads), "
+                      f"{done_bytes / 1e9:.3f} GB of K/V in {dt:.1f} s; numpy fp64 einsum on "
+                      f"one thread (host has {os.cpu_count()} cores)"}
+
+
+def run_reference(args) -> dict:
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return None
+    st = wl.make_config("decode")
+    for _ in range(args.warmup):
+        cpu_baseline(st, budget_s=0.5)
+    vals = []
+    t0 = time.perf_counter()
+    per = max(1.0, min(20.0, 90.0 / max(args.steps, 1)))
+    for _ in range(args.steps):
+        vals.append(cpu_baseline(st, budget_s=per))
+    wall = time.perf_counter() - t0
+    v = statistics.mean(x["value"] for x in vals)
+    base = vals[0]
+    base["value"] = round(v, 4)
+    return {"impl": "reference", "metric": METRIC, "value": round(v, 4), "unit": UNIT,
+            "n_gpus": int(os.environ.get("WORLD_SIZE", "1")), "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(wall / args.steps * 1e3, 2),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": {"workload": WORKLOAD},
+            "cpu_baseline": base,
+            "e2e": {"value": round(v, 4), "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-mixed", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=15.0)
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    line = run_reference(args) if args.impl == "reference" else run_ours(args)
+    if line is not None:
+        print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,379 @@
+"""Thin ctypes binding of libpagedattn (the C ABI declared in include/pagedattn.h).
+
+Argument marshalling only: every step of the hot path runs in the library's kernels. Device
+buffers are torch CUDA tensors (PyTorch supplies device memory and streams); host buffers are
+numpy arrays. Statuses other than PA_OK raise ``PagedAttnError`` (or a subclass).
+
+The library is loaded on first use from this package's directory; a missing library raises
+``RuntimeError`` (there is no fallback path).
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+import threading
+from typing import Optional
+
+import numpy as np
+
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libpagedattn.so")
+
+PA_OK, PA_ERR_INVALID, PA_ERR_SHAPE, PA_ERR_BOUNDS, PA_ERR_OOM, PA_ERR_READONLY, \
+    PA_ERR_DOUBLE_FREE, PA_ERR_INCONSISTENT, PA_ERR_WORKSPACE, PA_ERR_CUDA, PA_ERR_STATE = range(11)
+PA_DEVERR_BLOCK, PA_DEVERR_SLOT, PA_DEVERR_TIMEOUT, PA_DEVERR_META = 1, 2, 4, 8
+PA_SPLIT_TOKENS = 1024
+PA_TILE_KEYS = 128
+
+
+class PagedAttnError(RuntimeError):
+    def __init__(self, status: int, where: str = ""):
+        self.status = status
+        super().__init__(f"{where}: {status_string(status)}" if where else status_string(status))
+
+
+class PoolExhausted(PagedAttnError):
+    """PA_ERR_OOM: not enough free blocks; nothing changed."""
+
+
+class DoubleFree(PagedAttnError):
+    """PA_ERR_DOUBLE_FREE."""
+
+
+class ReadOnlyBlock(PagedAttnError):
+    """PA_ERR_READONLY: a write would land in a shared block."""
+
+
+_ERRORS = {PA_ERR_OOM: PoolExhausted, PA_ERR_DOUBLE_FREE: DoubleFree,
+           PA_ERR_READONLY: ReadOnlyBlock}
+
+
+class Shape(C.Structure):
+    _fields_ = [("num_q_heads", C.c_int32), ("num_kv_heads", C.c_int32),
+                ("head_dim", C.c_int32), ("block_size", C.c_int32), ("num_blocks", C.c_int32)]
+
+    @classmethod
+    def make(cls, Hq, Hkv, D, block_size, num_blocks) -> "Shape":
+        return cls(int(Hq), int(Hkv), int(D), int(block_size), int(num_blocks))
+
+
+class WorkItem(C.Structure):
+    _fields_ = [("seq", C.c_int32), ("q_start", C.c_int32), ("n_q", C.c_int32),
+                ("kv_head", C.c_int32), ("split", C.c_int32), ("n_tiles", C.c_int32),
+                ("reserved0", C.c_int32), ("reserved1", C.c_int32)]
+
+
+WORK_ITEM_DTYPE = np.dtype([(n, np.int32) for n, _ in WorkItem._fields_])
+
+_lib = None
+_lock = threading.Lock()
+_i32p = C.POINTER(C.c_int32)
+_vp = C.c_void_p
+
+
+def _sig(lib, name, res, args):
+    f = getattr(lib, name)
+    f.restype = res
+    f.argtypes = args
+
+
+def load() -> C.CDLL:
+    """Loads libpagedattn.so (once); raises RuntimeError if it has not been built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing: run __graft_entry__.build() or "
+                               "python -m continuous_batching_gb300.build")
+        lib = C.CDLL(LIB_PATH)
+        sp = C.POINTER(Shape)
+        ap = C.c_void_p                  # pa_allocator*
+        _sig(lib, "pa_abi_version", C.c_int32, [])
+        _sig(lib, "pa_status_string", C.c_char_p, [C.c_int32])
+        _sig(lib, "pa_last_cuda_error", C.c_int32, [])
+        _sig(lib, "pa_device_sm_count", C.c_int32, [_i32p])
+        _sig(lib, "pa_alloc_create", C.c_int32, [C.c_int32, C.c_int32, C.POINTER(ap)])
+        _sig(lib, "pa_alloc_destroy", C.c_int32, [ap])
+        _sig(lib, "pa_alloc_block", C.c_int32, [ap, _i32p])
+        _sig(lib, "pa_alloc_incref", C.c_int32, [ap, C.c_int32])
+        _sig(lib, "pa_alloc_free_block", C.c_int32, [ap, C.c_int32])
+        _sig(lib, "pa_alloc_admit", C.c_int32, [ap, C.c_int32, C.c_int32, C.c_int32, C.c_int32])
+        _sig(lib, "pa_alloc_ensure_capacity", C.c_int32, [ap, C.c_int32, C.c_int32])
+        _sig(lib, "pa_alloc_free_seq", C.c_int32, [ap, C.c_int32])
+        _sig(lib, "pa_alloc_check_consistent", C.c_int32, [ap])
+        _sig(lib, "pa_alloc_num_free", C.c_int32, [ap])
+        _sig(lib, "pa_alloc_refcount", C.c_int32, [ap, C.c_int32])
+        _sig(lib, "pa_alloc_table", C.c_int32, [ap, C.c_int32, _i32p, C.c_int32, _i32p])
+        _sig(lib, "pa_alloc_slots", C.c_int32, [ap, C.c_int32, C.c_int32, C.c_int32, _i32p])
+        _sig(lib, "pa_alloc_build_step", C.c_int32,
+             [ap, _i32p, _i32p, _i32p, C.c_int32, _i32p, _i32p, _i32p, C.c_int32])
+        _sig(lib, "pa_compute_slots", C.c_int32,
+             [sp, _i32p, C.c_int32, C.c_int32, _i32p, _i32p, _i32p])
+        _sig(lib, "pa_plan_max_items", C.c_int64, [sp, C.c_int32, C.c_int32, C.c_int32])
+        _sig(lib, "pa_plan_step", C.c_int32,
+             [sp, C.c_int32, _i32p, _i32p, C.POINTER(WorkItem), C.c_int32, _i32p])
+        _sig(lib, "pa_workspace_bytes", C.c_size_t, [sp, C.c_int32, C.c_int32])
+        _sig(lib, "pa_upload_block_table", C.c_int32,
+             [sp, _i32p, _vp, C.c_int32, C.c_int32, _vp])
+        _sig(lib, "paged_kv_write", C.c_int32,
+             [_vp, _vp, _vp, C.c_int32, _vp, _vp, sp, _vp, _vp])
+        _sig(lib, "paged_attention_step", C.c_int32,
+             [_vp, _vp, _vp, _vp, C.c_int32, _vp, _vp, C.c_int32, C.c_int32, C.c_int32,
+              _vp, C.c_int32, _vp, C.c_size_t, _vp, sp, _vp, _vp])
+        _lib = lib
+        return lib
+
+
+def status_string(st: int) -> str:
+    try:
+        return load().pa_status_string(int(st)).decode()
+    except RuntimeError:
+        return f"status {st}"
+
+
+def _check(st: int, where: str) -> None:
+    if st != PA_OK:
+        if st == PA_ERR_CUDA:
+            raise PagedAttnError(st, f"{where} (cudaError {load().pa_last_cuda_error()})")
+        raise _ERRORS.get(st, PagedAttnError)(st, where)
+
+
+def _i32(a: np.ndarray) -> np.ndarray:
+    a = np.ascontiguousarray(a, dtype=np.int32)
+    return a
+
+
+def _p32(a: Optional[np.ndarray]):
+    return None if a is None else a.ctypes.data_as(_i32p)
+
+
+def _dev(t) -> Optional[int]:
+    """Device address of a torch tensor (or None)."""
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("expected a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError("expected a contiguous tensor")
+    return t.data_ptr()
+
+
+def _stream(stream) -> Optional[int]:
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    return getattr(stream, "cuda_stream", stream)
+
+
+# ------------------------------------------------------------------------ library info
+
+def pa_abi_version() -> int:
+    return int(load().pa_abi_version())
+
+
+def pa_device_sm_count() -> int:
+    n = C.c_int32()
+    _check(load().pa_device_sm_count(C.byref(n)), "pa_device_sm_count")
+    return int(n.value)
+
+
+# ---------------------------------------------------------------------- host allocator
+
+class Allocator:
+    """Owns a pa_allocator (LIFO blocks, refcounts, read-only shared prefix blocks)."""
+
+    def __init__(self, num_blocks: int, block_size: int):
+        self._lib = load()
+        h = C.c_void_p()
+        _check(self._lib.pa_alloc_create(int(num_blocks), int(block_size), C.byref(h)),
+               "pa_alloc_create")
+        self._h = h
+        self.num_blocks = int(num_blocks)
+        self.block_size = int(block_size)
+
+    def close(self):
+        if getattr(self, "_h", None):
+            self._lib.pa_alloc_destroy(self._h)
+            self._h = None
+
+    __del__ = close
+
+    def alloc(self) -> int:
+        b = C.c_int32()
+        _check(self._lib.pa_alloc_block(self._h, C.byref(b)), "pa_alloc_block")
+        return int(b.value)
+
+    def incref(self, b: int) -> None:
+        _check(self._lib.pa_alloc_incref(self._h, int(b)), "pa_alloc_incref")
+
+    def free(self, b: int) -> None:
+        _check(self._lib.pa_alloc_free_block(self._h, int(b)), "pa_alloc_free_block")
+
+    def admit(self, seq: int, n_tokens: int, share_src: Optional[int] = None,
+              n_shared: int = 0) -> None:
+        _check(self._lib.pa_alloc_admit(self._h, int(seq), int(n_tokens),
+                                        -1 if share_src is None else int(share_src),
+                                        int(n_shared)), "pa_alloc_admit")
+
+    def ensure_capacity(self, seq: int, n_tokens: int) -> None:
+        _check(self._lib.pa_alloc_ensure_capacity(self._h, int(seq), int(n_tokens)),
+               "pa_alloc_ensure_capacity")
+
+    def free_seq(self, seq: int) -> None:
+        _check(self._lib.pa_alloc_free_seq(self._h, int(seq)), "pa_alloc_free_seq")
+
+    def check_consistent(self) -> None:
+        _check(self._lib.pa_alloc_check_consistent(self._h), "pa_alloc_check_consistent")
+
+    @property
+    def num_free(self) -> int:
+        return int(self._lib.pa_alloc_num_free(self._h))
+
+    def refcount(self, b: int) -> int:
+        return int(self._lib.pa_alloc_refcount(self._h, int(b)))
+
+    def table(self, seq: int) -> list:
+        n = C.c_int32()
+        _check(self._lib.pa_alloc_table(self._h, int(seq), None, 0, C.byref(n)), "pa_alloc_table")
+        out = np.empty(max(n.value, 1), np.int32)
+        _check(self._lib.pa_alloc_table(self._h, int(seq), _p32(out), n.value, C.byref(n)),
+               "pa_alloc_table")
+        return out[:n.value].tolist()
+
+    def slots(self, seq: int, start: int, n: int) -> list:
+        out = np.empty(max(n, 1), np.int32)
+        _check(self._lib.pa_alloc_slots(self._h, int(seq), int(start), int(n), _p32(out)),
+               "pa_alloc_slots")
+        return out[:n].tolist()
+
+    def build_step(self, seqs, ctx_lens, n_new, max_blocks: int):
+        """Returns (cu_seqlens_q, slot_mapping, block_table) host arrays for one step."""
+        seqs, ctx_lens, n_new = _i32(seqs), _i32(ctx_lens), _i32(n_new)
+        B = len(seqs)
+        cu = np.zeros(B + 1, np.int32)
+        T = int(n_new.sum())
+        slots = np.empty(max(T, 1), np.int32)
+        table = np.empty((max(B, 1), max_blocks), np.int32)
+        _check(self._lib.pa_alloc_build_step(self._h, _p32(seqs), _p32(ctx_lens), _p32(n_new), B,
+                                             _p32(cu), _p32(slots), _p32(table), int(max_blocks)),
+               "pa_alloc_build_step")
+        return cu, slots[:T], table[:B]
+
+
+# ------------------------------------------------------------------ host step metadata
+
+def pa_compute_slots(shape: Shape, block_table: np.ndarray, cu_seqlens_q: np.ndarray,
+                     ctx_lens: np.ndarray) -> np.ndarray:
+    bt = _i32(block_table)
+    cu, ctx = _i32(cu_seqlens_q), _i32(ctx_lens)
+    B = len(ctx)
+    T = int(cu[-1]) if B else 0
+    out = np.empty(max(T, 1), np.int32)
+    mb = bt.shape[1] if bt.ndim == 2 else 0
+    _check(load().pa_compute_slots(C.byref(shape), _p32(bt), B, mb, _p32(cu), _p32(ctx),
+                                   _p32(out)), "pa_compute_slots")
+    return out[:T]
+
+
+def pa_plan_step(shape: Shape, cu_seqlens_q: np.ndarray, ctx_lens: np.ndarray) -> np.ndarray:
+    """Work items for one step as a numpy structured array (dtype WORK_ITEM_DTYPE)."""
+    lib = load()
+    cu, ctx = _i32(cu_seqlens_q), _i32(ctx_lens)
+    B = len(ctx)
+    T = int(cu[-1]) if B else 0
+    max_ctx = int(ctx.max()) if B else 0
+    cap = int(lib.pa_plan_max_items(C.byref(shape), B, T, max_ctx))
+    buf = (WorkItem * max(cap, 1))()
+    n = C.c_int32()
+    _check(lib.pa_plan_step(C.byref(shape), B, _p32(cu), _p32(ctx), buf, cap, C.byref(n)),
+           "pa_plan_step")
+    arr = np.frombuffer(buf, dtype=WORK_ITEM_DTYPE, count=max(cap, 1))[:n.value].copy()
+    return arr
+
+
+def pa_workspace_bytes(shape: Shape, T: int, max_ctx: int) -> int:
+    return int(load().pa_workspace_bytes(C.byref(shape), int(T), int(max_ctx)))
+
+
+def pa_upload_block_table(shape: Shape, host: np.ndarray, dev, stream=None) -> None:
+    h = _i32(host)
+    B, mb = (h.shape if h.ndim == 2 else (0, 0))
+    _check(load().pa_upload_block_table(C.byref(shape), _p32(h), _dev(dev), B, mb,
+                                        _stream(stream)), "pa_upload_block_table")
+
+
+# ------------------------------------------------------------------------- device step
+
+def paged_kv_write(k_new, v_new, slot_mapping, k_pool, v_pool, shape: Shape, err=None,
+                   stream=None) -> None:
+    T = int(slot_mapping.shape[0])
+    _check(load().paged_kv_write(_dev(k_new), _dev(v_new), _dev(slot_mapping), T, _dev(k_pool),
+                                 _dev(v_pool), C.byref(shape), _dev(err), _stream(stream)),
+           "paged_kv_write")
+
+
+def paged_attention_step(q, k_pool, v_pool, block_table, cu_seqlens_q, ctx_lens, max_ctx: int,
+                         items, workspace, out, shape: Shape, err=None, stream=None) -> None:
+    """items: a device int32 tensor holding the pa_work_item records from pa_plan_step."""
+    B = int(ctx_lens.shape[0])
+    T = int(q.shape[0])
+    n_items = int(items.numel() // 8)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(load().paged_attention_step(
+        _dev(q), _dev(k_pool), _dev(v_pool), _dev(block_table), int(block_table.shape[1]),
+        _dev(cu_seqlens_q), _dev(ctx_lens), B, T, int(max_ctx), _dev(items), n_items,
+        _dev(workspace), ws_bytes, _dev(out), C.byref(shape), _dev(err), _stream(stream)),
+        "paged_attention_step")
+
+
+class StepRunner:
+    """One layer's step on the device: holds the plan buffers and workspace, runs
+    paged_kv_write then paged_attention_step on the current stream.
+
+    prepare() takes host metadata (the plan is computed on the host); run() launches."""
+
+    def __init__(self, shape: Shape, device="cuda"):
+        import torch
+        self.torch = torch
+        self.shape = shape
+        self.device = torch.device(device)
+        self.ws = None
+        self.err = torch.zeros(1, dtype=torch.int32, device=self.device)
+
+    def prepare(self, cu_seqlens_q: np.ndarray, ctx_lens: np.ndarray, block_table: np.ndarray,
+                slot_mapping: Optional[np.ndarray] = None):
+        torch = self.torch
+        cu, ctx = _i32(cu_seqlens_q), _i32(ctx_lens)
+        items = pa_plan_step(self.shape, cu, ctx)
+        if slot_mapping is None:
+            slot_mapping = pa_compute_slots(self.shape, block_table, cu, ctx)
+        self.max_ctx = int(ctx.max()) if len(ctx) else 0
+        self.T = int(cu[-1]) if len(ctx) else 0
+        d = self.device
+        self.h_items = items
+        self.items = torch.from_numpy(items.view(np.int32).reshape(-1).copy()).to(d)
+        self.cu = torch.from_numpy(cu.copy()).to(d)
+        self.ctx = torch.from_numpy(ctx.copy()).to(d)
+        self.table = torch.from_numpy(_i32(block_table).copy()).to(d)
+        self.slots = torch.from_numpy(_i32(slot_mapping).copy()).to(d)
+        need = pa_workspace_bytes(self.shape, self.T, self.max_ctx)
+        if self.ws is None or self.ws.numel() * 4 < need:
+            self.ws = torch.empty((need + 3) // 4, dtype=torch.float32, device=d)
+        return self
+
+    def write(self, k_new, v_new, k_pool, v_pool, stream=None):
+        paged_kv_write(k_new, v_new, self.slots, k_pool, v_pool, self.shape, self.err, stream)
+
+    def attend(self, q, k_pool, v_pool, out, stream=None):
+        paged_attention_step(q, k_pool, v_pool, self.table, self.cu, self.ctx, self.max_ctx,
+                             self.items, self.ws, out, self.shape, self.err, stream)
+
+    def run(self, q, k_new, v_new, k_pool, v_pool, out, stream=None):
+        self.write(k_new, v_new, k_pool, v_pool, stream)
+        self.attend(q, k_pool, v_pool, out, stream)
+        return out
+
+    def device_error(self) -> int:
+        return int(self.err.item())

@@ -1,0 +1,418 @@
+// Host half of libpagedattn: block allocator, step metadata, work planning, utilities.
+//
+// Allocator semantics follow "P3: native paged-KV continuous-batching sampler",
+// Design / paged.py (LIFO free list + refcounts, double-free guard, all-or-nothing capacity,
+// read-only shared blocks, check_consistent) and Design / engine.py (prefix sharing of full
+// blocks). The typed exhaustion error follows "Optional paged KV cache (vLLM-style) - v1
+// design", Design.
+#include <algorithm>
+#include <cstdint>
+#include <cstring>
+#include <unordered_map>
+#include <vector>
+
+#include <cuda_runtime.h>
+
+#include "../../include/pagedattn.h"
+#include "common.h"
+
+namespace {
+
+thread_local int32_t g_last_cuda_error = 0;
+
+}  // namespace
+
+namespace pa_detail {
+
+int32_t note_cuda(cudaError_t e) {
+    if (e == cudaSuccess) return PA_OK;
+    g_last_cuda_error = static_cast<int32_t>(e);
+    return PA_ERR_CUDA;
+}
+
+int32_t check_shape(const pa_shape* s) {
+    if (!s) return PA_ERR_INVALID;
+    if (s->num_q_heads <= 0 || s->num_kv_heads <= 0 || s->head_dim <= 0 || s->block_size <= 0 ||
+        s->num_blocks < 0)
+        return PA_ERR_INVALID;
+    if (s->num_q_heads % s->num_kv_heads) return PA_ERR_SHAPE;
+    const int g = s->num_q_heads / s->num_kv_heads;
+    if (g != 1 && g != 2 && g != 4 && g != 8 && g != 16) return PA_ERR_SHAPE;
+    if (s->head_dim != 64 && s->head_dim != 128) return PA_ERR_SHAPE;
+    const int bs = s->block_size;
+    if (bs < 8 || bs > 128 || (bs & (bs - 1))) return PA_ERR_SHAPE;
+    return PA_OK;
+}
+
+int32_t check_step_meta(int32_t B, const int32_t* cu, const int32_t* ctx) {
+    if (B < 0) return PA_ERR_INVALID;
+    if (B > 0 && (!cu || !ctx)) return PA_ERR_INVALID;
+    if (B == 0) return (cu && cu[0] != 0) ? PA_ERR_INVALID : PA_OK;
+    if (cu[0] != 0) return PA_ERR_INVALID;
+    for (int32_t s = 0; s < B; ++s) {
+        const int64_t n = int64_t(cu[s + 1]) - cu[s];
+        if (n < 0) return PA_ERR_INVALID;
+        if (ctx[s] < 0 || n > ctx[s]) return PA_ERR_INVALID;
+    }
+    return PA_OK;
+}
+
+}  // namespace pa_detail
+
+using namespace pa_detail;
+
+// ------------------------------------------------------------------------- allocator
+
+struct pa_allocator {
+    int32_t num_blocks = 0;
+    int32_t block_size = 0;
+    std::vector<int32_t> free_stack;      // top = back()
+    std::vector<int32_t> ref;
+    std::unordered_map<int32_t, std::vector<int32_t>> tables;
+};
+
+extern "C" {
+
+int32_t pa_abi_version(void) { return 1; }
+
+const char* pa_status_string(int32_t st) {
+    switch (st) {
+        case PA_OK: return "PA_OK";
+        case PA_ERR_INVALID: return "PA_ERR_INVALID";
+        case PA_ERR_SHAPE: return "PA_ERR_SHAPE";
+        case PA_ERR_BOUNDS: return "PA_ERR_BOUNDS";
+        case PA_ERR_OOM: return "PA_ERR_OOM";
+        case PA_ERR_READONLY: return "PA_ERR_READONLY";
+        case PA_ERR_DOUBLE_FREE: return "PA_ERR_DOUBLE_FREE";
+        case PA_ERR_INCONSISTENT: return "PA_ERR_INCONSISTENT";
+        case PA_ERR_WORKSPACE: return "PA_ERR_WORKSPACE";
+        case PA_ERR_CUDA: return "PA_ERR_CUDA";
+        case PA_ERR_STATE: return "PA_ERR_STATE";
+        default: return "PA_ERR_UNKNOWN";
+    }
+}
+
+int32_t pa_last_cuda_error(void) { return g_last_cuda_error; }
+
+int32_t pa_device_sm_count(int32_t* n) {
+    if (!n) return PA_ERR_INVALID;
+    int dev = 0;
+    int32_t st = note_cuda(cudaGetDevice(&dev));
+    if (st) return st;
+    int v = 0;
+    st = note_cuda(cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev));
+    if (st) return st;
+    *n = v;
+    return PA_OK;
+}
+
+int32_t pa_alloc_create(int32_t num_blocks, int32_t block_size, pa_allocator** out) {
+    if (!out || num_blocks < 0 || block_size <= 0) return PA_ERR_INVALID;
+    auto* a = new pa_allocator;
+    a->num_blocks = num_blocks;
+    a->block_size = block_size;
+    a->ref.assign(num_blocks, 0);
+    a->free_stack.resize(num_blocks);
+    for (int32_t i = 0; i < num_blocks; ++i) a->free_stack[i] = num_blocks - 1 - i;
+    *out = a;
+    return PA_OK;
+}
+
+int32_t pa_alloc_destroy(pa_allocator* a) {
+    delete a;
+    return PA_OK;
+}
+
+int32_t pa_alloc_block(pa_allocator* a, int32_t* block) {
+    if (!a || !block) return PA_ERR_INVALID;
+    if (a->free_stack.empty()) return PA_ERR_OOM;
+    const int32_t b = a->free_stack.back();
+    a->free_stack.pop_back();
+    a->ref[b] = 1;
+    *block = b;
+    return PA_OK;
+}
+
+int32_t pa_alloc_incref(pa_allocator* a, int32_t b) {
+    if (!a) return PA_ERR_INVALID;
+    if (b < 0 || b >= a->num_blocks) return PA_ERR_BOUNDS;
+    if (a->ref[b] <= 0) return PA_ERR_STATE;
+    a->ref[b] += 1;
+    return PA_OK;
+}
+
+int32_t pa_alloc_free_block(pa_allocator* a, int32_t b) {
+    if (!a) return PA_ERR_INVALID;
+    if (b < 0 || b >= a->num_blocks) return PA_ERR_BOUNDS;
+    if (a->ref[b] == 0) return PA_ERR_DOUBLE_FREE;
+    if (--a->ref[b] == 0) a->free_stack.push_back(b);
+    return PA_OK;
+}
+
+static int64_t blocks_for(int64_t n_tokens, int32_t bs) { return (n_tokens + bs - 1) / bs; }
+
+int32_t pa_alloc_admit(pa_allocator* a, int32_t seq, int32_t n_tokens, int32_t share_src,
+                       int32_t n_shared) {
+    if (!a || seq < 0 || n_tokens < 0 || n_shared < 0) return PA_ERR_INVALID;
+    if (a->tables.count(seq)) return PA_ERR_STATE;
+    const std::vector<int32_t>* src = nullptr;
+    if (share_src >= 0 && n_shared > 0) {
+        auto it = a->tables.find(share_src);
+        if (it == a->tables.end()) return PA_ERR_STATE;
+        src = &it->second;
+        if (n_shared > int32_t(src->size()) || int64_t(n_shared) * a->block_size > n_tokens)
+            return PA_ERR_INVALID;
+    } else {
+        n_shared = 0;
+    }
+    const int64_t need = blocks_for(n_tokens, a->block_size) - n_shared;
+    if (need > int64_t(a->free_stack.size())) return PA_ERR_OOM;
+    std::vector<int32_t> t;
+    t.reserve(n_shared + std::max<int64_t>(need, 0));
+    for (int32_t i = 0; i < n_shared; ++i) {
+        const int32_t b = (*src)[i];
+        a->ref[b] += 1;
+        t.push_back(b);
+    }
+    for (int64_t i = 0; i < need; ++i) {
+        int32_t b;
+        pa_alloc_block(a, &b);
+        t.push_back(b);
+    }
+    a->tables.emplace(seq, std::move(t));
+    return PA_OK;
+}
+
+int32_t pa_alloc_ensure_capacity(pa_allocator* a, int32_t seq, int32_t n_tokens) {
+    if (!a || n_tokens < 0) return PA_ERR_INVALID;
+    auto it = a->tables.find(seq);
+    if (it == a->tables.end()) return PA_ERR_STATE;
+    const int64_t need = blocks_for(n_tokens, a->block_size) - int64_t(it->second.size());
+    if (need <= 0) return PA_OK;
+    if (need > int64_t(a->free_stack.size())) return PA_ERR_OOM;
+    for (int64_t i = 0; i < need; ++i) {
+        int32_t b;
+        pa_alloc_block(a, &b);
+        it->second.push_back(b);
+    }
+    return PA_OK;
+}
+
+int32_t pa_alloc_free_seq(pa_allocator* a, int32_t seq) {
+    if (!a) return PA_ERR_INVALID;
+    auto it = a->tables.find(seq);
+    if (it == a->tables.end()) return PA_ERR_STATE;
+    for (int32_t b : it->second) {
+        const int32_t st = pa_alloc_free_block(a, b);
+        if (st) return st;
+    }
+    a->tables.erase(it);
+    return PA_OK;
+}
+
+int32_t pa_alloc_check_consistent(const pa_allocator* a) {
+    if (!a) return PA_ERR_INVALID;
+    std::vector<uint8_t> on_free(a->num_blocks, 0);
+    for (int32_t b : a->free_stack) {
+        if (b < 0 || b >= a->num_blocks || on_free[b]) return PA_ERR_INCONSISTENT;
+        on_free[b] = 1;
+        if (a->ref[b] != 0) return PA_ERR_INCONSISTENT;
+    }
+    int64_t referenced = 0;
+    for (int32_t b = 0; b < a->num_blocks; ++b) referenced += a->ref[b] > 0;
+    if (referenced + int64_t(a->free_stack.size()) != a->num_blocks) return PA_ERR_INCONSISTENT;
+    std::vector<int32_t> want(a->num_blocks, 0);
+    for (const auto& kv : a->tables)
+        for (int32_t b : kv.second) {
+            if (b < 0 || b >= a->num_blocks) return PA_ERR_INCONSISTENT;
+            want[b] += 1;
+        }
+    for (int32_t b = 0; b < a->num_blocks; ++b)
+        if (want[b] != a->ref[b]) return PA_ERR_INCONSISTENT;
+    return PA_OK;
+}
+
+int32_t pa_alloc_num_free(const pa_allocator* a) {
+    return a ? int32_t(a->free_stack.size()) : -1;
+}
+
+int32_t pa_alloc_refcount(const pa_allocator* a, int32_t b) {
+    if (!a || b < 0 || b >= a->num_blocks) return -1;
+    return a->ref[b];
+}
+
+int32_t pa_alloc_table(const pa_allocator* a, int32_t seq, int32_t* out, int32_t cap,
+                       int32_t* n) {
+    if (!a || !n || cap < 0 || (cap > 0 && !out)) return PA_ERR_INVALID;
+    auto it = a->tables.find(seq);
+    if (it == a->tables.end()) return PA_ERR_STATE;
+    const int32_t len = int32_t(it->second.size());
+    *n = len;
+    std::memcpy(out, it->second.data(), sizeof(int32_t) * std::min(cap, len));
+    return PA_OK;
+}
+
+static int32_t slots_of(const pa_allocator* a, const std::vector<int32_t>& t, int32_t start,
+                        int32_t n, int32_t* out) {
+    const int32_t bs = a->block_size;
+    for (int32_t i = 0; i < n; ++i) {
+        const int64_t p = int64_t(start) + i;
+        const int64_t j = p / bs;
+        if (p < 0 || j >= int64_t(t.size())) return PA_ERR_BOUNDS;
+        if (a->ref[t[j]] > 1) return PA_ERR_READONLY;
+    }
+    for (int32_t i = 0; i < n; ++i) {
+        const int64_t p = int64_t(start) + i;
+        out[i] = int32_t(int64_t(t[p / bs]) * bs + p % bs);
+    }
+    return PA_OK;
+}
+
+int32_t pa_alloc_slots(const pa_allocator* a, int32_t seq, int32_t start, int32_t n,
+                       int32_t* out) {
+    if (!a || n < 0 || (n > 0 && !out)) return PA_ERR_INVALID;
+    auto it = a->tables.find(seq);
+    if (it == a->tables.end()) return PA_ERR_STATE;
+    return slots_of(a, it->second, start, n, out);
+}
+
+int32_t pa_alloc_build_step(const pa_allocator* a, const int32_t* seqs, const int32_t* ctx_lens,
+                            const int32_t* n_new, int32_t B, int32_t* cu_seqlens_q,
+                            int32_t* slot_mapping, int32_t* block_table, int32_t max_blocks) {
+    if (!a || B < 0 || max_blocks <= 0 || !cu_seqlens_q) return PA_ERR_INVALID;
+    if (B > 0 && (!seqs || !ctx_lens || !n_new || !block_table)) return PA_ERR_INVALID;
+    // validate everything before writing anything
+    int64_t T = 0;
+    std::vector<const std::vector<int32_t>*> rows(B);
+    for (int32_t i = 0; i < B; ++i) {
+        auto it = a->tables.find(seqs[i]);
+        if (it == a->tables.end()) return PA_ERR_STATE;
+        if (ctx_lens[i] < 0 || n_new[i] < 0 || n_new[i] > ctx_lens[i]) return PA_ERR_INVALID;
+        const int64_t nb = blocks_for(ctx_lens[i], a->block_size);
+        if (nb > int64_t(it->second.size())) return PA_ERR_BOUNDS;
+        if (nb > max_blocks) return PA_ERR_BOUNDS;
+        const int32_t start = ctx_lens[i] - n_new[i];
+        for (int32_t k = 0; k < n_new[i]; ++k) {
+            const int64_t j = (int64_t(start) + k) / a->block_size;
+            if (a->ref[it->second[j]] > 1) return PA_ERR_READONLY;
+        }
+        rows[i] = &it->second;
+        T += n_new[i];
+    }
+    if (T > INT32_MAX) return PA_ERR_INVALID;
+    if (T > 0 && !slot_mapping) return PA_ERR_INVALID;
+    cu_seqlens_q[0] = 0;
+    for (int32_t i = 0; i < B; ++i) {
+        cu_seqlens_q[i + 1] = cu_seqlens_q[i] + n_new[i];
+        int32_t* row = block_table + int64_t(i) * max_blocks;
+        const int64_t nb = blocks_for(ctx_lens[i], a->block_size);
+        for (int32_t j = 0; j < max_blocks; ++j) row[j] = j < nb ? (*rows[i])[j] : -1;
+        slots_of(a, *rows[i], ctx_lens[i] - n_new[i], n_new[i], slot_mapping + cu_seqlens_q[i]);
+    }
+    return PA_OK;
+}
+
+// --------------------------------------------------------------------- step metadata
+
+int32_t pa_compute_slots(const pa_shape* shape, const int32_t* block_table, int32_t B,
+                         int32_t max_blocks, const int32_t* cu, const int32_t* ctx,
+                         int32_t* slot_mapping) {
+    int32_t st = check_shape(shape);
+    if (st) return st;
+    st = check_step_meta(B, cu, ctx);
+    if (st) return st;
+    if (B > 0 && (!block_table || max_blocks <= 0)) return PA_ERR_INVALID;
+    const int32_t bs = shape->block_size;
+    for (int32_t s = 0; s < B; ++s) {
+        const int64_t nb = blocks_for(ctx[s], bs);
+        if (nb > max_blocks) return PA_ERR_BOUNDS;
+        for (int64_t j = 0; j < nb; ++j) {
+            const int32_t b = block_table[int64_t(s) * max_blocks + j];
+            if (b < 0 || b >= shape->num_blocks) return PA_ERR_BOUNDS;
+        }
+    }
+    const int32_t T = B > 0 ? cu[B] : 0;
+    if (T > 0 && !slot_mapping) return PA_ERR_INVALID;
+    for (int32_t s = 0; s < B; ++s) {
+        const int32_t n = cu[s + 1] - cu[s];
+        for (int32_t i = 0; i < n; ++i) {
+            const int64_t p = int64_t(ctx[s]) - n + i;
+            const int64_t b = block_table[int64_t(s) * max_blocks + p / bs];
+            slot_mapping[cu[s] + i] = int32_t(b * bs + p % bs);
+        }
+    }
+    return PA_OK;
+}
+
+int64_t pa_plan_max_items(const pa_shape* shape, int32_t B, int32_t T, int32_t max_ctx) {
+    if (check_shape(shape) || B < 0 || T < 0 || max_ctx < 0) return 0;
+    const int32_t g = shape->num_q_heads / shape->num_kv_heads;
+    const int64_t rows_per_tile = PA_ROWS / g;
+    const int64_t tiles = int64_t(B) + T / rows_per_tile + 1;   // each seq adds <= 1 ragged tile
+    const int64_t splits = (int64_t(max_ctx) + PA_SPLIT_TOKENS - 1) / PA_SPLIT_TOKENS;
+    return tiles * shape->num_kv_heads * std::max<int64_t>(splits, 1);
+}
+
+int32_t pa_plan_step(const pa_shape* shape, int32_t B, const int32_t* cu, const int32_t* ctx,
+                     pa_work_item* items, int32_t max_items, int32_t* n_items) {
+    int32_t st = check_shape(shape);
+    if (st) return st;
+    st = check_step_meta(B, cu, ctx);
+    if (st) return st;
+    if (!n_items || max_items < 0 || (max_items > 0 && !items)) return PA_ERR_INVALID;
+    const int32_t g = shape->num_q_heads / shape->num_kv_heads;
+    const int32_t rpt = PA_ROWS / g;
+    std::vector<pa_work_item> out;
+    for (int32_t s = 0; s < B; ++s) {
+        const int32_t n = cu[s + 1] - cu[s];
+        for (int32_t t0 = 0; t0 < n; t0 += rpt) {
+            const int32_t nt = std::min(rpt, n - t0);
+            const int64_t p_max = int64_t(ctx[s]) - n + t0 + nt - 1;
+            const int32_t nsplit = int32_t(p_max / PA_SPLIT_TOKENS + 1);
+            for (int32_t h = 0; h < shape->num_kv_heads; ++h)
+                for (int32_t sp = 0; sp < nsplit; ++sp) {
+                    const int64_t k0 = int64_t(sp) * PA_SPLIT_TOKENS;
+                    const int64_t k1 = std::min<int64_t>(k0 + PA_SPLIT_TOKENS, p_max + 1);
+                    pa_work_item it{};
+                    it.seq = s;
+                    it.q_start = cu[s] + t0;
+                    it.n_q = nt;
+                    it.kv_head = h;
+                    it.split = sp;
+                    it.n_tiles = int32_t((k1 - k0 + PA_TILE_KEYS - 1) / PA_TILE_KEYS);
+                    out.push_back(it);
+                }
+        }
+    }
+    if (int64_t(out.size()) > max_items) return PA_ERR_INVALID;
+    std::stable_sort(out.begin(), out.end(), [](const pa_work_item& x, const pa_work_item& y) {
+        return x.n_tiles > y.n_tiles;
+    });
+    if (!out.empty()) std::memcpy(items, out.data(), out.size() * sizeof(pa_work_item));
+    *n_items = int32_t(out.size());
+    return PA_OK;
+}
+
+size_t pa_workspace_bytes(const pa_shape* shape, int32_t T, int32_t max_ctx) {
+    if (check_shape(shape) || T < 0 || max_ctx < 0) return 0;
+    const size_t splits = (size_t(max_ctx) + PA_SPLIT_TOKENS - 1) / PA_SPLIT_TOKENS;
+    const size_t per = size_t(shape->num_q_heads) * (shape->head_dim + 2) * sizeof(float);
+    return std::max<size_t>(size_t(T) * std::max<size_t>(splits, 1) * per, 256);
+}
+
+int32_t pa_upload_block_table(const pa_shape* shape, const int32_t* host, int32_t* dev,
+                              int32_t B, int32_t max_blocks, pa_stream_t stream) {
+    int32_t st = check_shape(shape);
+    if (st) return st;
+    if (B < 0 || max_blocks < 0) return PA_ERR_INVALID;
+    const int64_t n = int64_t(B) * max_blocks;
+    if (n == 0) return PA_OK;
+    if (!host) return PA_ERR_INVALID;
+    for (int64_t i = 0; i < n; ++i)
+        if (host[i] < -1 || host[i] >= shape->num_blocks) return PA_ERR_BOUNDS;
+    if (!dev) return PA_ERR_INVALID;
+    return note_cuda(cudaMemcpyAsync(dev, host, size_t(n) * sizeof(int32_t),
+                                     cudaMemcpyHostToDevice, stream));
+}
+
+}  // extern "C"

@@ -1,0 +1,239 @@
+/*
+ * pagedattn.h - C ABI of libpagedattn: attention over a paged KV cache for one flat ragged
+ * continuous-batching step, on one NVIDIA GB300 (sm_103a).
+ *
+ * The operation follows "P3: native paged-KV continuous-batching sampler"
+ * (code/docs/P3_ENGINE.md), Design / paged.py and Design / engine.py:
+ *   - per-layer K and V pools shaped [num_blocks, block_size, Hkv, D];
+ *   - an int32 block table [B, max_blocks] per step ("the argument a kernel takes");
+ *   - a copy-free append: new K/V rows scatter into (block, offset) through a slot mapping;
+ *   - one flat ragged step mixes decode rows and chunked-prefill segments
+ *     (cu_seqlens_q, ctx_lens), with the GQA map kv_head = q_head / (Hq / Hkv);
+ *   - a kernel contract with a fixed KV split per context length and no atomics, so that a
+ *     sequence's output bits do not depend on what else is in the batch.
+ * and "Finish RL Training Faster: Bitwise-Consistent, High-Performance, Agent-Driven",
+ * section 2 (batch independence, phase consistency: a token gets the same bits in prefill
+ * and in decode) and 4.2 (decode goes through the prefill read path).
+ *
+ * Conventions for every function below:
+ *   - Every function returns a pa_status (PA_OK == 0) unless stated otherwise. Arguments are
+ *     validated on the host before anything is launched; a failed check launches nothing.
+ *   - "host" pointers are ordinary CPU memory; "device" pointers are CUDA global memory on
+ *     the current device. The caller owns all buffers; the library never frees them and the
+ *     step calls (paged_kv_write, paged_attention_step) allocate no memory.
+ *   - bf16 tensors are passed as void* holding IEEE bfloat16 values, row-major, dense.
+ *   - Kernels never trap. Device-side range checks (a block id outside the pool, a slot
+ *     outside the pool) skip the access and OR a PA_DEVERR_* bit into *err_flag when the
+ *     caller passes a device int32 (may be NULL). Every device wait is bounded; a wait that
+ *     runs out sets PA_DEVERR_TIMEOUT and the kernel returns.
+ *   - Streams: pa_stream_t is cudaStream_t (struct CUstream_st*); NULL is the legacy stream.
+ */
+#ifndef PAGEDATTN_H
+#define PAGEDATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* pa_stream_t;
+
+typedef enum pa_status {
+    PA_OK = 0,
+    PA_ERR_INVALID = 1,       /* null pointer, negative size, inconsistent metadata */
+    PA_ERR_SHAPE = 2,         /* head_dim / group / block_size this build does not support */
+    PA_ERR_BOUNDS = 3,        /* block id, slot or position outside the pool or the table */
+    PA_ERR_OOM = 4,           /* pool exhausted; the allocator changed nothing */
+    PA_ERR_READONLY = 5,      /* a write would land in a block with refcount > 1 */
+    PA_ERR_DOUBLE_FREE = 6,   /* free of a block whose refcount is already 0 */
+    PA_ERR_INCONSISTENT = 7,  /* allocator books do not balance */
+    PA_ERR_WORKSPACE = 8,     /* workspace smaller than pa_workspace_bytes() */
+    PA_ERR_CUDA = 9,          /* a CUDA runtime call failed: pa_last_cuda_error() */
+    PA_ERR_STATE = 10         /* unknown or duplicate sequence id */
+} pa_status;
+
+/* Bits OR-ed into the optional device error word by the kernels. */
+#define PA_DEVERR_BLOCK   1   /* a block-table entry outside [0, num_blocks) was read */
+#define PA_DEVERR_SLOT    2   /* a slot outside [0, num_blocks * block_size) was written */
+#define PA_DEVERR_TIMEOUT 4   /* a bounded device wait ran out */
+#define PA_DEVERR_META    8   /* a work item inconsistent with cu_seqlens_q / ctx_lens / limits */
+
+/* Fixed KV split: keys [s * PA_SPLIT_TOKENS, (s + 1) * PA_SPLIT_TOKENS) form split s of every
+ * sequence. It depends on nothing but the key position, which keeps the numerics of a row
+ * independent of the batch ("fixed KV split per context length", P3 page Design / paged.py). */
+#define PA_SPLIT_TOKENS 1024
+/* Keys per tile of the shared tile routine; tiles are aligned to multiples of this. */
+#define PA_TILE_KEYS 128
+
+/* Geometry of one layer's pool. Supported: head_dim in {64, 128}; group = Hq / Hkv in
+ * {1, 2, 4, 8, 16}; block_size a power of two in [8, 128]. */
+typedef struct pa_shape {
+    int32_t num_q_heads;    /* Hq */
+    int32_t num_kv_heads;   /* Hkv; divides Hq */
+    int32_t head_dim;       /* D */
+    int32_t block_size;     /* tokens per block */
+    int32_t num_blocks;     /* blocks in each of the K and V pools */
+} pa_shape;
+
+/* One unit of attention work: query rows [q_start, q_start + n_q) of sequence `seq`, one KV
+ * head, one KV split. Produced by pa_plan_step on the host; copied to the device by the
+ * caller and passed to paged_attention_step. */
+typedef struct pa_work_item {
+    int32_t seq;        /* index into cu_seqlens_q / ctx_lens / block_table rows */
+    int32_t q_start;    /* first query row (token index into q and out) */
+    int32_t n_q;        /* query rows, 1 .. 128 / group */
+    int32_t kv_head;    /* KV head */
+    int32_t split;      /* KV split index */
+    int32_t n_tiles;    /* key tiles of PA_TILE_KEYS the item reads (a cost estimate) */
+    int32_t reserved0;
+    int32_t reserved1;
+} pa_work_item;
+
+/* ---------------------------------------------------------------- library ---------- */
+
+/* ABI version of this header (returns the integer, not a status). */
+int32_t pa_abi_version(void);
+
+/* Human-readable name of a pa_status (static string; never NULL). */
+const char* pa_status_string(int32_t status);
+
+/* The cudaError_t of the most recent failed CUDA call on this host thread (0 if none). */
+int32_t pa_last_cuda_error(void);
+
+/* Streaming multiprocessors of the current device, in *n (host). */
+int32_t pa_device_sm_count(int32_t* n);
+
+/* ------------------------------------------------- host block allocator ------------ */
+/* "P3: native paged-KV continuous-batching sampler", Design / paged.py: BlockAllocator is a
+ * LIFO free list with refcounts; free on refcount 0 raises; check_consistent proves
+ * free + referenced == total with no duplicates. PagedKVCache: ensure_capacity is
+ * all-or-nothing; a block with refcount > 1 is read-only for everyone, owner included.
+ * Design / engine.py: prefix sharing adopts the leading FULL blocks of a running sequence.
+ * Exhaustion is a typed error, never truncation ("Optional paged KV cache (vLLM-style) - v1
+ * design", Design: alloc throws PagedPoolExhausted).
+ * The free stack starts so that the first allocation returns block 0; a freed block is the
+ * next one handed out. Sequence ids are any non-negative int32. Not thread-safe. */
+typedef struct pa_allocator pa_allocator;
+
+/* Creates an allocator over num_blocks blocks of block_size tokens; *out owns it. */
+int32_t pa_alloc_create(int32_t num_blocks, int32_t block_size, pa_allocator** out);
+/* Destroys it (NULL is ignored). Returns PA_OK. */
+int32_t pa_alloc_destroy(pa_allocator* a);
+/* Pops one block (refcount 1) into *block; PA_ERR_OOM when none is free. */
+int32_t pa_alloc_block(pa_allocator* a, int32_t* block);
+/* Adds a reference to a live block; PA_ERR_STATE if it is free, PA_ERR_BOUNDS if out of range. */
+int32_t pa_alloc_incref(pa_allocator* a, int32_t block);
+/* Drops a reference; the block returns to the free list at 0. PA_ERR_DOUBLE_FREE at 0. */
+int32_t pa_alloc_free_block(pa_allocator* a, int32_t block);
+/* Creates the table of `seq` covering n_tokens tokens. With share_src >= 0, its first
+ * n_shared blocks are the leading blocks of share_src's table (they must be full blocks of
+ * the source, n_shared * block_size <= n_tokens), each gaining a reference. All or nothing:
+ * PA_ERR_OOM / PA_ERR_STATE / PA_ERR_INVALID leave every table and refcount unchanged. */
+int32_t pa_alloc_admit(pa_allocator* a, int32_t seq, int32_t n_tokens, int32_t share_src,
+                       int32_t n_shared);
+/* Grows seq's table to cover n_tokens; all or nothing (PA_ERR_OOM changes nothing). */
+int32_t pa_alloc_ensure_capacity(pa_allocator* a, int32_t seq, int32_t n_tokens);
+/* Releases every block of seq's table and forgets seq. */
+int32_t pa_alloc_free_seq(pa_allocator* a, int32_t seq);
+/* PA_OK if free + referenced == total, the free list has no duplicates and every refcount
+ * equals the references held by live tables; PA_ERR_INCONSISTENT otherwise. */
+int32_t pa_alloc_check_consistent(const pa_allocator* a);
+/* Free blocks (returns the count, not a status; -1 on NULL). */
+int32_t pa_alloc_num_free(const pa_allocator* a);
+/* Refcount of a block (returns the count; -1 when out of range). */
+int32_t pa_alloc_refcount(const pa_allocator* a, int32_t block);
+/* Copies seq's table into out[0 .. cap) (host), the table length into *n. */
+int32_t pa_alloc_table(const pa_allocator* a, int32_t seq, int32_t* out, int32_t cap, int32_t* n);
+/* Slots of positions start .. start+n-1 of seq (host out[n]); PA_ERR_READONLY if any lands in
+ * a block with refcount > 1, PA_ERR_BOUNDS beyond the table. Writes nothing on error. */
+int32_t pa_alloc_slots(const pa_allocator* a, int32_t seq, int32_t start, int32_t n,
+                       int32_t* out);
+/* Builds one step's host metadata from the allocator: sequence i of the step is seqs[i] with
+ * ctx_lens[i] tokens after the step, n_new[i] of them new (written this step). Outputs
+ * (host, caller-owned): cu_seqlens_q[B+1], slot_mapping[sum n_new], block_table[B*max_blocks]
+ * (row-major, -1 padded). Capacity must already cover ctx_lens (PA_ERR_BOUNDS otherwise);
+ * PA_ERR_READONLY if a new token would land in a shared block. Writes nothing on error. */
+int32_t pa_alloc_build_step(const pa_allocator* a, const int32_t* seqs, const int32_t* ctx_lens,
+                            const int32_t* n_new, int32_t B, int32_t* cu_seqlens_q,
+                            int32_t* slot_mapping, int32_t* block_table, int32_t max_blocks);
+
+/* ------------------------------------------------------- host step metadata -------- */
+
+/* Slot mapping from explicit host tables (P3 page, Design / paged.py: copy-free append).
+ * Token i of sequence s sits at position p = ctx_lens[s] - n_q(s) + i, where
+ * n_q(s) = cu_seqlens_q[s+1] - cu_seqlens_q[s]; its slot is
+ * block_table[s*max_blocks + p/block_size] * block_size + p % block_size.
+ * Validates: cu_seqlens_q[0] == 0 and non-decreasing; 0 <= n_q(s) <= ctx_lens[s];
+ * ceil(ctx/block_size) <= max_blocks; table entries covering ctx in [0, num_blocks).
+ * Output slot_mapping[T] (host), T = cu_seqlens_q[B]. Writes nothing on error. */
+int32_t pa_compute_slots(const pa_shape* shape, const int32_t* block_table, int32_t B,
+                         int32_t max_blocks, const int32_t* cu_seqlens_q,
+                         const int32_t* ctx_lens, int32_t* slot_mapping);
+
+/* Upper bound on the work items pa_plan_step produces for B sequences, T query rows and no
+ * context longer than max_ctx. Returns the count (0 on bad arguments). */
+int64_t pa_plan_max_items(const pa_shape* shape, int32_t B, int32_t T, int32_t max_ctx);
+
+/* Splits the step into work items (host in, host out). Query rows of a sequence are cut
+ * into tiles of 128 / group rows; every (tile, KV head, KV split the tile's last row reaches)
+ * is one item. Items are ordered by decreasing n_tiles (ties keep the generation order), so
+ * the order is a pure function of the metadata. Validates the metadata like
+ * pa_compute_slots (minus the table). PA_ERR_INVALID if max_items is too small. */
+int32_t pa_plan_step(const pa_shape* shape, int32_t B, const int32_t* cu_seqlens_q,
+                     const int32_t* ctx_lens, pa_work_item* items, int32_t max_items,
+                     int32_t* n_items);
+
+/* Bytes of fp32 workspace paged_attention_step needs for T query rows and contexts up to
+ * max_ctx: split partials (acc[D], m, l) for every (row, split, q head). Sized by limits, not
+ * by the load, so one buffer serves every step under the same limits. */
+size_t pa_workspace_bytes(const pa_shape* shape, int32_t T, int32_t max_ctx);
+
+/* Copies a validated host block table [B * max_blocks] to device memory `dev` on `stream`
+ * (an ordinary async copy; pinned host memory makes it asynchronous). Entries must be -1 or
+ * in [0, num_blocks): PA_ERR_BOUNDS otherwise, and nothing is copied. */
+int32_t pa_upload_block_table(const pa_shape* shape, const int32_t* host, int32_t* dev,
+                              int32_t B, int32_t max_blocks, pa_stream_t stream);
+
+/* ------------------------------------------------------------- device step --------- */
+
+/* KV-write scatter (P3 page, Design / paged.py: "write scatters into (block, offset) in
+ * place"). For t in [0, T): if slot_mapping[t] >= 0, copies k_new[t] (Hkv*D bf16) to
+ * k_pool[slot] and v_new[t] to v_pool[slot], where the pools are viewed as
+ * [num_blocks*block_size, Hkv, D]. Bytes are copied unchanged (16-byte vector stores).
+ * Device: k_new, v_new [T, Hkv, D] bf16; slot_mapping [T] int32; k_pool, v_pool
+ * [num_blocks, block_size, Hkv, D] bf16; err_flag optional. A slot >= num_blocks*block_size
+ * is skipped and sets PA_DEVERR_SLOT. T == 0 launches nothing. */
+int32_t paged_kv_write(const void* k_new, const void* v_new, const int32_t* slot_mapping,
+                       int32_t T, void* k_pool, void* v_pool, const pa_shape* shape,
+                       int32_t* err_flag, pa_stream_t stream);
+
+/* Attention for one flat ragged step over an already-written pool (call paged_kv_write
+ * first: ctx_lens count this step's tokens, P3 page "write new K/V, return [T, H, D]").
+ * For every query row t of sequence s at position p = ctx_lens[s] - n_q(s) + (t - cu[s]) and
+ * every q head h: out[t, h] = sum_{j <= p} softmax_j(q[t,h] . K_s[j, h/g] / sqrt(D)) V_s[j, h/g],
+ * where K_s, V_s are s's keys in table order. Arithmetic: bf16 tensor-core products with fp32
+ * accumulation, fp32 online softmax per fixed KV split, splits combined in ascending order,
+ * result rounded to bf16 (nearest even). Every row, decode or prefill, runs the same tile
+ * routine, so its bits depend only on its own query, keys and position.
+ * Device inputs: q [T, Hq, D] bf16; k_pool, v_pool [num_blocks, block_size, Hkv, D] bf16;
+ * block_table [B, max_blocks] int32; cu_seqlens_q [B+1], ctx_lens [B] int32 (the same values
+ * given to pa_plan_step); items [n_items] from pa_plan_step; workspace of ws_bytes >=
+ * pa_workspace_bytes(shape, T, max_ctx) with max_ctx >= every ctx_lens[s].
+ * Device output: out [T, Hq, D] bf16 (rows not covered by items are not written).
+ * Host checks: pointers, shape support, workspace size; T == 0 or n_items == 0 launches
+ * nothing. */
+int32_t paged_attention_step(const void* q, const void* k_pool, const void* v_pool,
+                             const int32_t* block_table, int32_t max_blocks,
+                             const int32_t* cu_seqlens_q, const int32_t* ctx_lens,
+                             int32_t B, int32_t T, int32_t max_ctx,
+                             const pa_work_item* items, int32_t n_items,
+                             void* workspace, size_t ws_bytes, void* out,
+                             const pa_shape* shape, int32_t* err_flag, pa_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PAGEDATTN_H */

@@ -1,0 +1,114 @@
+"""The C-ABI library on the CPU: it loads, exports every symbol include/pagedattn.h declares,
+and its host-side step metadata is bit-exact against the oracle (no GPU needed)."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+import oracle.paged_attention as pa
+from continuous_batching_gb300 import binding as bd
+from continuous_batching_gb300 import workloads as wl
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "pagedattn.h")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built_library():
+    if not os.path.exists(bd.LIB_PATH):
+        from continuous_batching_gb300 import build
+        build.build()
+    return bd.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return re.findall(r"^\s*(?:const\s+)?(?:int32_t|int64_t|size_t|char\s*\*|void)\s*\**\s*(\w+)\s*\(",
+                      text, flags=re.M)
+
+
+def test_every_declared_symbol_is_exported(built_library):
+    names = declared_functions()
+    assert len(names) >= 20
+    lib = ctypes.CDLL(bd.LIB_PATH)
+    missing = [n for n in names if not hasattr(lib, n)]
+    assert not missing, missing
+
+
+def test_abi_version_and_status_strings():
+    assert bd.pa_abi_version() == 1
+    assert bd.status_string(bd.PA_ERR_OOM) == "PA_ERR_OOM"
+    assert bd.status_string(999) == "PA_ERR_UNKNOWN"
+
+
+@pytest.mark.parametrize("name", wl.CONFIG_NAMES)
+def test_slot_mapping_matches_oracle(name):
+    st = wl.make_config(name, with_pool=False)
+    shape = bd.Shape.make(st.Hq, st.Hkv, st.D, st.block_size, st.num_blocks)
+    got = bd.pa_compute_slots(shape, st.block_table, st.cu_seqlens_q, st.ctx_lens)
+    want = pa.slot_mapping(st.block_table, st.cu_seqlens_q, st.ctx_lens, st.block_size)
+    assert got.dtype == np.int32 and np.array_equal(got.astype(np.int64), want)
+
+
+def test_slot_mapping_rejects_bad_metadata():
+    st = wl.make_config("tiny", with_pool=False)
+    shape = bd.Shape.make(st.Hq, st.Hkv, st.D, st.block_size, st.num_blocks)
+    bad = st.block_table.copy()
+    bad[0, 0] = st.num_blocks                    # outside the pool
+    with pytest.raises(bd.PagedAttnError):
+        bd.pa_compute_slots(shape, bad, st.cu_seqlens_q, st.ctx_lens)
+    cu = st.cu_seqlens_q.copy()
+    cu[2] = cu[1] - 1                            # decreasing
+    with pytest.raises(bd.PagedAttnError):
+        bd.pa_compute_slots(shape, st.block_table, cu, st.ctx_lens)
+    ctx = st.ctx_lens.copy()
+    ctx[0] = 0                                   # fewer keys than query rows
+    with pytest.raises(bd.PagedAttnError):
+        bd.pa_compute_slots(shape, st.block_table, st.cu_seqlens_q, ctx)
+    with pytest.raises(bd.PagedAttnError):       # unsupported head_dim
+        bd.pa_compute_slots(bd.Shape.make(4, 2, 96, 16, 32), st.block_table, st.cu_seqlens_q,
+                            st.ctx_lens)
+
+
+@pytest.mark.parametrize("name", wl.CONFIG_NAMES)
+def test_plan_covers_every_row_head_split_once(name):
+    """Each (query row, KV head, split s <= pos // 1024) appears in exactly one item."""
+    st = wl.make_config(name, with_pool=False)
+    shape = bd.Shape.make(st.Hq, st.Hkv, st.D, st.block_size, st.num_blocks)
+    items = bd.pa_plan_step(shape, st.cu_seqlens_q, st.ctx_lens)
+    g = st.Hq // st.Hkv
+    seq_of, pos_of = pa.row_positions(st.cu_seqlens_q, st.ctx_lens)
+    nsplit = pos_of // bd.PA_SPLIT_TOKENS + 1
+    count = {}
+    for it in items:
+        assert 1 <= it["n_q"] <= 128 // g
+        assert st.cu_seqlens_q[it["seq"]] <= it["q_start"]
+        assert it["q_start"] + it["n_q"] <= st.cu_seqlens_q[it["seq"] + 1]
+        for t in range(it["q_start"], it["q_start"] + it["n_q"]):
+            if it["split"] < nsplit[t]:
+                key = (t, it["kv_head"], it["split"])
+                count[key] = count.get(key, 0) + 1
+    want = {(t, h, s) for t in range(st.T) for h in range(st.Hkv) for s in range(nsplit[t])}
+    assert set(count) == want and all(v == 1 for v in count.values())
+    # longest items first, deterministic
+    assert np.all(np.diff(items["n_tiles"]) <= 0)
+    again = bd.pa_plan_step(shape, st.cu_seqlens_q, st.ctx_lens)
+    assert np.array_equal(items, again)
+
+
+def test_workspace_bytes_cover_partials():
+    shape = bd.Shape.make(32, 8, 128, 16, 100)
+    assert bd.pa_workspace_bytes(shape, 10, 3000) == 10 * 3 * 32 * 130 * 4
+    assert bd.pa_workspace_bytes(shape, 0, 0) == 256
+
+
+def test_upload_rejects_out_of_range_table_without_gpu():
+    """Validation happens on the host before any copy, so it needs no device."""
+    shape = bd.Shape.make(4, 2, 64, 16, 8)
+    bad = np.array([[0, 9]], np.int32)
+    st = bd.load().pa_upload_block_table(ctypes.byref(shape), bad.ctypes.data_as(bd._i32p),
+                                         None, 1, 2, None)
+    assert st == bd.PA_ERR_BOUNDS

@@ -1,0 +1,178 @@
+"""GPU parity of the hot path through the C ABI: KV write bit-exact against the oracle, bf16
+attention within max|diff| <= 1.5e-2 and mean|diff| <= 2e-3 of the fp64 oracle, on small
+cases in full and on the five named workloads at full size (sampled rows)."""
+import numpy as np
+import pytest
+
+import oracle.paged_attention as pa
+from continuous_batching_gb300 import binding as bd
+from continuous_batching_gb300 import workloads as wl
+from tests.gpu_util import assert_close, pool_np, run_step, shape_of
+
+pytestmark = pytest.mark.gpu
+torch = pytest.importorskip("torch")
+if not torch.cuda.is_available():
+    pytest.skip("no CUDA device", allow_module_level=True)
+
+
+@pytest.fixture(scope="module", autouse=True)
+def lib():
+    from continuous_batching_gb300 import build
+    build.build()
+    return bd.load()
+
+
+def oracle_full(st):
+    return pa.step(st.q, st.k_new, st.v_new, st.k_pool, st.v_pool, st.block_table,
+                   st.cu_seqlens_q, st.ctx_lens, st.Hq, st.block_size)
+
+
+def test_tiny_config_all_rows():
+    st = wl.make_config("tiny")
+    out, kp, vp, err = run_step(st, torch)
+    slots, kp_ref, vp_ref, ref = oracle_full(st)
+    assert err == 0
+    assert np.array_equal(pool_np(kp, torch), kp_ref)
+    assert np.array_equal(pool_np(vp, torch), vp_ref)
+    assert_close(out, ref, "tiny")
+
+
+# ragged mix: decode rows at tile and split boundaries plus prefill segments that start at 0,
+# straddle the first split boundary, end on a tile boundary and have ragged tails
+MID_CTX = [1, 17, 127, 128, 129, 1023, 1024, 1025, 2049, 3000, 200, 1100, 2100, 5, 384]
+MID_NQ = [1, 1, 1, 1, 1, 1, 1, 1, 1, 1, 200, 77, 33, 5, 129]
+
+
+@pytest.mark.parametrize("Hq,Hkv,D,bs", [(32, 8, 128, 16), (8, 8, 128, 32), (16, 2, 64, 8),
+                                         (64, 8, 128, 64), (16, 1, 128, 128), (4, 2, 64, 16)])
+def test_mixed_step_all_rows(Hq, Hkv, D, bs):
+    st = wl.make_step(Hq, Hkv, D, bs, MID_CTX, MID_NQ, seed=Hq * 7 + D + bs)
+    out, kp, vp, err = run_step(st, torch)
+    slots, kp_ref, vp_ref, ref = oracle_full(st)
+    assert err == 0
+    assert np.array_equal(pool_np(kp, torch), kp_ref)
+    assert np.array_equal(pool_np(vp, torch), vp_ref)
+    assert_close(out, ref, f"mixed Hq{Hq} Hkv{Hkv} D{D} bs{bs}")
+
+
+def _sample_rows(st, rng, n=24):
+    rows = set()
+    for s in range(st.B):
+        a, b = int(st.cu_seqlens_q[s]), int(st.cu_seqlens_q[s + 1])
+        if b - a > 1:
+            rows.update([a, b - 1, a + (b - a) // 2])
+    rows.update(rng.choice(st.T, size=min(n, st.T), replace=False).tolist())
+    long_s = int(np.argmax(st.ctx_lens))
+    rows.add(int(st.cu_seqlens_q[long_s + 1]) - 1)
+    return np.array(sorted(rows))
+
+
+@pytest.mark.parametrize("name", ["decode", "mixed", "longtail", "prefix"])
+def test_full_size_workloads_sampled(name):
+    st = wl.make_config(name)
+    out, kp, vp, err = run_step(st, torch)
+    assert err == 0
+    slots = pa.slot_mapping(st.block_table, st.cu_seqlens_q, st.ctx_lens, st.block_size)
+    kp_np, vp_np = pool_np(kp, torch), pool_np(vp, torch)
+    # the written slots carry the new rows bit-exactly; a sample of other blocks is untouched
+    flat_k = kp_np.reshape(-1, st.Hkv, st.D)
+    flat_v = vp_np.reshape(-1, st.Hkv, st.D)
+    assert np.array_equal(flat_k[slots], st.k_new) and np.array_equal(flat_v[slots], st.v_new)
+    rng = np.random.default_rng(1234)
+    untouched = np.setdiff1d(np.arange(flat_k.shape[0]), slots)
+    pick = rng.choice(untouched, size=min(4096, len(untouched)), replace=False)
+    assert np.array_equal(flat_k[pick], st.k_pool.reshape(-1, st.Hkv, st.D)[pick])
+    rows = _sample_rows(st, rng)
+    ref = pa.attention_rows(st.q, kp_np, vp_np, st.block_table, st.cu_seqlens_q, st.ctx_lens,
+                            st.Hq, rows)
+    assert_close(out[rows], ref, name)
+    assert np.all(np.isfinite(pa.bf16_to_f64(out)))
+
+
+def test_longest_context_and_late_prefill_chunk():
+    """ctx 40960 decode row and a 512-row chunk at prior offset 40448 (40 splits)."""
+    st = wl.make_step(64, 8, 128, 32, [40960, 40960], [1, 512], seed=77)
+    out, kp, vp, err = run_step(st, torch)
+    assert err == 0
+    rows = np.array([0, 1, 2, 100, 256, 511, 512])
+    ref = pa.attention_rows(st.q, pool_np(kp, torch), pool_np(vp, torch), st.block_table,
+                            st.cu_seqlens_q, st.ctx_lens, st.Hq, rows)
+    assert_close(out[rows], ref, "ctx 40960")
+
+
+def test_empty_step_and_zero_row_sequences():
+    st = wl.make_step(8, 2, 128, 16, [40, 10, 300], [0, 0, 0], seed=3)
+    out, kp, vp, err = run_step(st, torch)
+    assert out.shape[0] == 0 and err == 0
+    st = wl.make_step(8, 2, 128, 16, [40, 10, 300, 7], [0, 3, 0, 1], seed=4)
+    out, kp, vp, err = run_step(st, torch)
+    slots, kp_ref, vp_ref, ref = oracle_full(st)
+    assert_close(out, ref, "zero-row sequences")
+
+
+def test_stale_nan_in_pool_is_never_read():
+    """Slots past each sequence's context hold NaN bit patterns: outputs stay finite and
+    bit-identical to a pool holding ordinary stale values."""
+    st = wl.make_step(32, 8, 128, 16, [5, 130, 1030, 17], [1, 1, 3, 17], seed=9)
+    clean, _, _, _ = run_step(st, torch)
+    kp = st.k_pool.copy()
+    vp = st.v_pool.copy()
+    flat_k = kp.reshape(-1, st.Hkv, st.D)
+    flat_v = vp.reshape(-1, st.Hkv, st.D)
+    live = set()
+    for s in range(st.B):
+        for p in range(int(st.ctx_lens[s])):
+            live.add(int(st.block_table[s, p // st.block_size]) * st.block_size + p % st.block_size)
+    dead = np.array(sorted(set(range(flat_k.shape[0])) - live))
+    flat_k[dead] = 0x7FC1
+    flat_v[dead] = 0xFFC3
+    dirty, _, _, err = run_step(st, torch, k_pool=kp, v_pool=vp)
+    assert err == 0
+    assert np.array_equal(clean, dirty)
+
+
+def test_device_error_word_for_bad_slot_and_block():
+    st = wl.make_config("tiny")
+    shape = shape_of(st)
+    import tests.gpu_util as gu
+    kp = gu.bf16_dev(st.k_pool, torch)
+    vp = gu.bf16_dev(st.v_pool, torch)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    slots = torch.tensor([0, st.num_blocks * st.block_size + 5, -1, 3], dtype=torch.int32,
+                         device="cuda")
+    bd.paged_kv_write(gu.bf16_dev(st.k_new, torch), gu.bf16_dev(st.v_new, torch), slots, kp, vp,
+                      shape, err)
+    torch.cuda.synchronize()
+    assert int(err.item()) & bd.PA_DEVERR_SLOT
+    # a corrupt table entry (outside the pool) reads zeros and raises the block bit
+    table = st.block_table.copy()
+    table[3, 1] = st.num_blocks + 100
+    runner = bd.StepRunner(shape)
+    runner.prepare(st.cu_seqlens_q, st.ctx_lens, st.block_table)
+    runner.table = torch.from_numpy(table).cuda()
+    out = torch.zeros((st.T, st.Hq, st.D), dtype=torch.bfloat16, device="cuda")
+    runner.attend(gu.bf16_dev(st.q, torch), kp, vp, out)
+    torch.cuda.synchronize()
+    assert runner.device_error() & bd.PA_DEVERR_BLOCK
+    # the other sequences are unaffected
+    ref = pa.attention(st.q, pool_np(kp, torch), pool_np(vp, torch), st.block_table,
+                       st.cu_seqlens_q, st.ctx_lens, st.Hq)
+    o = out.view(torch.int16).cpu().numpy().view(np.uint16)
+    assert_close(o[:3], ref[:3], "unaffected rows")
+
+
+def test_host_rejects_bad_arguments_before_launch():
+    st = wl.make_config("tiny")
+    shape = shape_of(st)
+    runner = bd.StepRunner(shape).prepare(st.cu_seqlens_q, st.ctx_lens, st.block_table)
+    import tests.gpu_util as gu
+    q = gu.bf16_dev(st.q, torch)
+    kp = gu.bf16_dev(st.k_pool, torch)
+    out = torch.zeros((st.T, st.Hq, st.D), dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(bd.PagedAttnError):
+        bd.paged_attention_step(q, kp, kp, runner.table, runner.cu, runner.ctx, 5000,
+                                runner.items, None, out, shape)     # needs a workspace
+    bad = bd.Shape.make(st.Hq, st.Hkv, 96, st.block_size, st.num_blocks)
+    with pytest.raises(bd.PagedAttnError):
+        bd.paged_attention_step(q, kp, kp, runner.table, runner.cu, runner.ctx, 100,
+                                runner.items, runner.ws, out, bad)
