@@ -214,6 +214,14 @@ def time_steps(g: GpuStep, torch, steps: int, warmup: int, flush, attn_only=Fals
     return step_ms, attn_ms
 
 
+def load_for(g: GpuStep, torch, seconds: float) -> None:
+    t = time.perf_counter()
+    while time.perf_counter() - t < seconds:
+        for _ in range(20):
+            g.step()
+        torch.cuda.synchronize()
+
+
 def run_ours(args) -> dict:
     import torch
 
@@ -239,11 +247,18 @@ def run_ours(args) -> dict:
         torch.cuda.synchronize()
 
     barrier()
-    t0 = time.perf_counter()
     with ClockSampler(local) as clk:
+        # keep the GPU under the same load for about a second on both sides of the timed
+        # region so that the 200 ms clock samples cover it
+        if not args.no_clocks:
+            load_for(g, torch, 1.0)
+        barrier()
+        t0 = time.perf_counter()
         step_ms, attn_ms = time_steps(g, torch, args.steps, args.warmup, flush)
         barrier()
-    wall = time.perf_counter() - t0
+        wall = time.perf_counter() - t0
+        if not args.no_clocks:
+            load_for(g, torch, 1.0)
     total_ms = sum(step_ms)
     if world > 1:
         import torch.distributed as dist
@@ -292,8 +307,9 @@ def run_ours(args) -> dict:
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic",
         "config": {"workload": WORKLOAD, "kv_bytes_per_step": bytes_step, "T": st.T,
-                   "l2": "inputs larger than L2 (0.84 GB K/V) and L2 flushed by a 256 MiB "
-                         "write between timed steps", "parallelism": f"replicas{world}"},
+                   "l2": f"inputs larger than L2 ({bytes_step / 1e9:.2f} GB K/V) and L2 flushed "
+                         "by a 256 MiB write between timed steps",
+                   "parallelism": f"replicas{world}"},
         "e2e": {"value": round(bytes_step / e2e_s / 1e9, 2), "unit": UNIT,
                 "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                 "ms_per_step": round(e2e_s * 1e3, 4)},
@@ -374,6 +390,9 @@ def main(argv=None):
     ap.add_argument("--no-mixed", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
+    ap.add_argument("--no-clocks", action="store_true",
+                    help="skip the loaded windows around the timed region that the clock "
+                         "samples need (for profiler runs)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
