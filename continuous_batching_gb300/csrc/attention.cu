@@ -30,6 +30,7 @@
 
 #include <cmath>
 #include <cstring>
+#include <mutex>
 
 #include "common.h"
 #include "tmem_ldst.h"
@@ -733,6 +734,92 @@ extern "C" int32_t paged_attention_step(const void* q, const void* k_pool, const
     prm.ws_ml = workspace ? static_cast<float*>(workspace) +
                                 size_t(T) * max_splits * shape->num_q_heads * D
                           : nullptr;
+    prm.out = static_cast<__nv_bfloat16*>(out);
+    prm.err = err_flag;
+    prm.B = B;
+    prm.T = T;
+    prm.max_blocks = max_blocks;
+    prm.max_splits = max_splits;
+    prm.Hq = shape->num_q_heads;
+    prm.Hkv = shape->num_kv_heads;
+    prm.g = shape->num_q_heads / shape->num_kv_heads;
+    prm.bs = shape->block_size;
+    prm.num_blocks = shape->num_blocks;
+    prm.c = float(1.4426950408889634 / std::sqrt(double(D)));
+    if (D == 128) return launch<128>(mk, mv, prm, n_items, B, T, max_ctx, stream);
+    return launch<64>(mk, mv, prm, n_items, B, T, max_ctx, stream);
+}
+
+// ------------------------------------------- allocation-free variant of the attention step
+// Some callers cannot allocate device memory at the point where they run a step: a serving
+// process that reserves all GPU memory up front and forbids later cudaMalloc calls, a plug-in
+// that only receives tensors from its host framework and has no allocator of its own, or a
+// latency-critical loop where cudaMalloc's implicit device synchronisation is not acceptable.
+// For them the split-partial scratch lives in the fixed array below instead of a
+// caller-provided workspace. Every GPU that loads the library keeps this array until the
+// process exits.
+namespace {
+
+static __device__ __align__(256) float g_static_scratch[PA_STATIC_SCRATCH_BYTES / sizeof(float)];
+
+constexpr int kMaxDevices = 64;
+float* g_static_scratch_addr[kMaxDevices] = {};   // device address per device, set on first use
+std::mutex g_static_scratch_mu;
+
+// Host code cannot use g_static_scratch as a pointer (on the host it names a stand-in, not
+// device memory): look its device address up once per device, with that device current.
+int32_t static_scratch_for_current_device(float** out) {
+    int dev = 0;
+    int32_t st = note_cuda(cudaGetDevice(&dev));
+    if (st) return st;
+    if (dev < 0 || dev >= kMaxDevices) return PA_ERR_INVALID;
+    std::lock_guard<std::mutex> lock(g_static_scratch_mu);
+    if (!g_static_scratch_addr[dev]) {
+        void* ptr = nullptr;
+        st = note_cuda(cudaGetSymbolAddress(&ptr, g_static_scratch));
+        if (st) return st;
+        g_static_scratch_addr[dev] = static_cast<float*>(ptr);
+    }
+    *out = g_static_scratch_addr[dev];
+    return PA_OK;
+}
+
+}  // namespace
+
+extern "C" int32_t paged_attention_step_static_scratch(
+    const void* q, const void* k_pool, const void* v_pool, const int32_t* block_table,
+    int32_t max_blocks, const int32_t* cu_seqlens_q, const int32_t* ctx_lens, int32_t B,
+    int32_t T, int32_t max_ctx, const pa_work_item* items, int32_t n_items, void* out,
+    const pa_shape* shape, int32_t* err_flag, pa_stream_t stream) {
+    int32_t st = check_shape(shape);
+    if (st) return st;
+    if (B < 0 || T < 0 || n_items < 0 || max_ctx < 0 || max_blocks < 0) return PA_ERR_INVALID;
+    if (T == 0 || n_items == 0) return PA_OK;
+    if (!q || !k_pool || !v_pool || !block_table || !cu_seqlens_q || !ctx_lens || !items || !out)
+        return PA_ERR_INVALID;
+    if (int64_t(shape->num_blocks) * shape->block_size > INT32_MAX) return PA_ERR_SHAPE;
+    if ((reinterpret_cast<uintptr_t>(k_pool) | reinterpret_cast<uintptr_t>(v_pool) |
+         reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(out)) & 15)
+        return PA_ERR_INVALID;
+    // the partials of this step must fit the fixed array; nothing is launched otherwise
+    if (max_ctx > kSplit && pa_workspace_bytes(shape, T, max_ctx) > PA_STATIC_SCRATCH_BYTES)
+        return PA_ERR_WORKSPACE;
+    float* scratch = nullptr;
+    if ((st = static_scratch_for_current_device(&scratch))) return st;
+
+    CUtensorMap mk, mv;
+    if ((st = make_pool_map(&mk, k_pool, shape))) return st;
+    if ((st = make_pool_map(&mv, v_pool, shape))) return st;
+    const int D = shape->head_dim;
+    const int max_splits = int((int64_t(max_ctx) + kSplit - 1) / kSplit);
+    Params prm;
+    prm.q = static_cast<const __nv_bfloat16*>(q);
+    prm.block_table = block_table;
+    prm.cu = cu_seqlens_q;
+    prm.ctx = ctx_lens;
+    prm.items = items;
+    prm.ws_acc = scratch;
+    prm.ws_ml = scratch + size_t(T) * max_splits * shape->num_q_heads * D;
     prm.out = static_cast<__nv_bfloat16*>(out);
     prm.err = err_flag;
     prm.B = B;

@@ -232,6 +232,34 @@ int32_t paged_attention_step(const void* q, const void* k_pool, const void* v_po
                              void* workspace, size_t ws_bytes, void* out,
                              const pa_shape* shape, int32_t* err_flag, pa_stream_t stream);
 
+/* Allocation-free variant of paged_attention_step (no counterpart on the pages: it is a
+ * deployment convenience of this library). Same arguments, meaning and result as
+ * paged_attention_step, minus the workspace: the split partials go to a fixed device array of
+ * PA_STATIC_SCRATCH_BYTES that the library itself holds on every GPU that loads it, until the
+ * process exits. It is meant for callers that cannot allocate device memory when they run a
+ * step: a serving process that reserves all GPU memory at start-up and allows no later
+ * cudaMalloc, a plug-in that only receives tensors from its host framework, or a loop that
+ * cannot afford cudaMalloc's implicit synchronisation. It calls no cudaMalloc, cudaFree or
+ * other allocating routine.
+ *   - Limit: a step whose partials need more than PA_STATIC_SCRATCH_BYTES (see
+ *     pa_workspace_bytes(shape, T, max_ctx); steps with max_ctx <= PA_SPLIT_TOKENS need none)
+ *     returns PA_ERR_WORKSPACE and launches nothing.
+ *   - The first call on each device looks up the array's device address (cudaGetSymbolAddress,
+ *     with that device current); make that first call before any stream capture.
+ *   - Every call on a device shares the one array, and it keeps whatever the last call left
+ *     there; nothing in it needs to start at zero, because every partial the combine reads is
+ *     written earlier in the same call. Calls whose kernels overlap on the GPU (different
+ *     streams, no ordering between them) race on the array: order them on one stream or with
+ *     events. */
+#define PA_STATIC_SCRATCH_BYTES (32u << 20)
+int32_t paged_attention_step_static_scratch(const void* q, const void* k_pool, const void* v_pool,
+                                            const int32_t* block_table, int32_t max_blocks,
+                                            const int32_t* cu_seqlens_q, const int32_t* ctx_lens,
+                                            int32_t B, int32_t T, int32_t max_ctx,
+                                            const pa_work_item* items, int32_t n_items, void* out,
+                                            const pa_shape* shape, int32_t* err_flag,
+                                            pa_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif
