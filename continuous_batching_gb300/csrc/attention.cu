@@ -20,14 +20,19 @@
 // bits do not depend on the other rows of the tile; the fixed splits
 // [s*1024, (s+1)*1024) and the ascending-order combine make them independent of the batch.
 //
-// Warp roles (192 threads): warps 0-3 softmax / rescale / epilogue, warp 4 TMA producer,
-// warp 5 MMA issuer and TMEM owner. K/V blocks arrive by TMA (one box per block and 64-column
-// half, 128-byte swizzle) into a 2-stage ring; every wait on an mbarrier is bounded.
+// Persistent schedule: one CTA per SM walks the items blockIdx.x, blockIdx.x + gridDim.x, ...
+// (the host orders items longest first). Warp roles (192 threads): warps 0-3 softmax /
+// rescale / epilogue, warp 4 TMA producer, warp 5 MMA issuer and TMEM owner. The producer
+// streams K/V tiles through a ring of shared-memory stages across item boundaries and loads
+// each item's Q tile by TMA into one of two Q buffers. TMEM holds two S buffers (S of the
+// next tile is computed while the softmax works on the current one) and two O accumulators
+// (an item's epilogue overlaps the next item's MMAs). Every wait on an mbarrier is bounded.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cmath>
 #include <cstring>
 #include <mutex>
@@ -42,9 +47,9 @@ namespace {
 constexpr int kRows = PA_ROWS;
 constexpr int kTileKeys = PA_TILE_KEYS;
 constexpr int kSplit = PA_SPLIT_TOKENS;
-constexpr int kStages = 2;
 constexpr int kThreads = 192;
-constexpr uint32_t kTmemCols = 256;                 // S: columns [0,128), O: [128, 128 + D)
+constexpr uint32_t kTmemCols = 512;     // S0 [0,128) S1 [128,256) O0 [256,384) O1 [384,512)
+constexpr uint32_t kTmemO = 256;
 constexpr unsigned long long kWaitLimitNs = 1000000000ull;   // one second per wait
 
 static_assert(kSplit % kTileKeys == 0, "splits are whole tiles");
@@ -52,26 +57,42 @@ static_assert(kSplit % kTileKeys == 0, "splits are whole tiles");
 template <int D>
 struct Layout {
     static constexpr int kChunks = D / 64;                  // 128-byte column chunks of a row
-    static constexpr int kQHalf = kRows * 128;              // bytes of one chunk column of Q
+    static constexpr int kStages = D == 128 ? 2 : 4;        // K/V ring depth
+    static constexpr int kQHalf = kRows * 128;              // one 64-column chunk of a Q tile
+    static constexpr int kQBuf = kChunks * kQHalf;
     static constexpr int kKVHalf = kTileKeys * 128;
-    static constexpr int kQ = 0;
-    static constexpr int kP = kQ + kChunks * kQHalf;        // P: 128 keys = 2 chunks
+    static constexpr int kKVTile = kChunks * kKVHalf;       // K (or V) of one key tile
+    static constexpr int kQ = 0;                            // two Q buffers
+    static constexpr int kP = kQ + 2 * kQBuf;               // P: 128 rows x 128 keys, 2 chunks
     static constexpr int kK = kP + 2 * kRows * 128;
-    static constexpr int kKVStage = kChunks * kKVHalf;
-    static constexpr int kV = kK + kStages * kKVStage;
-    static constexpr int kBar = kV + kStages * kKVStage;
-    static constexpr int kBytes = kBar + 256;
+    static constexpr int kV = kK + kStages * kKVTile;
+    static constexpr int kBar = kV + kStages * kKVTile;     // barriers, item ring, table
+    static constexpr int kBytes = kBar + 1024;
     static constexpr int kAlloc = kBytes + 1024;            // room to align the base to 1024
 };
 
 // mbarrier slots (8 bytes each) at Layout::kBar
-enum Bar { kKVFull0 = 0, kKVFull1, kKVEmpty0, kKVEmpty1, kSFull, kPFull, kOFull, kQFull, kDrain,
-           kNumBars };
+enum Bar {
+    kKVFull = 0,     // + stage (up to 4): TMA -> MMA
+    kKVEmpty = 4,    // + stage: MMA (after PV) -> TMA
+    kQFull = 8,      // + buffer: TMA -> MMA
+    kQEmpty = 10,    // + buffer: MMA (after the item's last S) -> TMA
+    kSFull = 12,     // + buffer: MMA -> softmax
+    kPFull = 14,     // softmax (128 arrivals) -> MMA: P stored, O rescaled, V tail zeroed
+    kPVDone = 15,    // MMA -> softmax: the previous PV has finished
+    kOFree = 16,     // + buffer: epilogue (128 arrivals) -> MMA
+    kDrain = 18,
+    kItemFull = 19,  // + slot (4): producer -> everyone: the slot holds the next item
+    kItemEmpty = 23, // + slot: consumers (MMA 2 + softmax 128 arrivals) -> producer
+    kNumBars = 27
+};
 constexpr int kHolderOff = 8 * kNumBars;          // TMEM address written by tcgen05.alloc
 constexpr int kAbortOff = kHolderOff + 4;
+constexpr int kRingOff = 256;                     // 4 item slots of 64 bytes
+constexpr int kTableOff = 512;                    // block-table entries of the current item
+constexpr int kMaxTableEntries = 128;             // 1024 keys / 8-token blocks
 
 struct Params {
-    const __nv_bfloat16* q;
     const int32_t* block_table;
     const int32_t* cu;
     const int32_t* ctx;
@@ -80,7 +101,7 @@ struct Params {
     float* ws_ml;       // [T][max_splits][Hq][2]
     __nv_bfloat16* out;
     int32_t* err;
-    int32_t B, T, max_blocks, max_splits, Hq, Hkv, g, bs, num_blocks;
+    int32_t n_items, B, T, max_blocks, max_splits, Hq, Hkv, g, bs, num_blocks;
     float c;            // log2(e) / sqrt(D): softmax works in base 2 on raw scores
 };
 
@@ -110,6 +131,17 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     uint32_t ok;
     asm volatile(
         "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tmbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
         "selp.u32 %0, 1, 0, p;\n\t}"
         : "=r"(ok)
         : "r"(bar), "r"(parity)
@@ -221,25 +253,41 @@ __device__ __forceinline__ uint32_t swz(int row, int chunk) {
     return uint32_t(row * 128 + ((chunk ^ (row & 7)) << 4));
 }
 
-// --------------------------------------------------------------- the tile routine
 
-template <int D>
-__global__ void __launch_bounds__(kThreads, 1)
-    paged_attn_kernel(const __grid_constant__ CUtensorMap tm_k,
-                      const __grid_constant__ CUtensorMap tm_v, const Params p) {
-    using L = Layout<D>;
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                               ~uintptr_t(1023));
-    const uint32_t sb = smem_u32(smem);
-    const uint32_t bars = sb + L::kBar;
-    volatile int* abort_word = reinterpret_cast<volatile int*>(smem + L::kBar + kAbortOff);
-    const int warp = threadIdx.x >> 5;
-    const int lane = threadIdx.x & 31;
+// One work item, checked against the metadata it points at (device data). A bad item does
+// no work in any role and raises PA_DEVERR_META (reported by the softmax warps).
+struct Item {
+    bool good;
+    int seq, ctx, q_start, n_q, kvh, split, pos0, k_begin, n_tiles, rows_valid;
+};
 
-    pa_work_item it = p.items[blockIdx.x];
-    // The item and the metadata it points at are device data: check them before use. A bad
-    // item does no work (n_tiles = 0) and raises PA_DEVERR_META.
+// What the producer publishes in an item slot (64 bytes); `last` marks the end of the CTA's
+// item list.
+struct ItemSlot {
+    int seq, ctx, q_start, n_q, kvh, split, pos0, k_begin, n_tiles, rows_valid, last, pad[5];
+};
+static_assert(sizeof(ItemSlot) == 64, "item slot size");
+
+__device__ __forceinline__ Item slot_item(const volatile ItemSlot* sl, bool* last) {
+    Item I;
+    I.good = true;
+    I.seq = sl->seq;
+    I.ctx = sl->ctx;
+    I.q_start = sl->q_start;
+    I.n_q = sl->n_q;
+    I.kvh = sl->kvh;
+    I.split = sl->split;
+    I.pos0 = sl->pos0;
+    I.k_begin = sl->k_begin;
+    I.n_tiles = sl->n_tiles;
+    I.rows_valid = sl->rows_valid;
+    *last = sl->last != 0;
+    return I;
+}
+
+__device__ __forceinline__ Item load_item(const Params& p, int idx) {
+    const pa_work_item it = p.items[idx];
+    Item I;
     bool good = it.seq >= 0 && it.seq < p.B && it.kv_head >= 0 && it.kv_head < p.Hkv &&
                 it.n_q >= 1 && it.n_q * p.g <= kRows && it.split >= 0 && it.q_start >= 0 &&
                 it.q_start + it.n_q <= p.T;
@@ -254,13 +302,43 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int k_begin = it.split * kSplit;
     good = good && k_begin <= p_max && (p_max < kSplit || p_max / kSplit < p.max_splits);
     const int k_end = min(k_begin + kSplit, p_max + 1);
-    const int n_tiles = good ? (k_end - k_begin + kTileKeys - 1) / kTileKeys : 0;
-    const int rows_valid = good ? it.n_q * p.g : 0;
-    if (!good && threadIdx.x == 0 && p.err) atomicOr(p.err, PA_DEVERR_META);
+    I.good = good;
+    I.seq = seq;
+    I.ctx = ctx_s;
+    I.q_start = it.q_start;
+    I.n_q = it.n_q;
+    I.kvh = it.kv_head;
+    I.split = it.split;
+    I.pos0 = pos0;
+    I.k_begin = k_begin;
+    I.n_tiles = good ? (k_end - k_begin + kTileKeys - 1) / kTileKeys : 0;
+    I.rows_valid = good ? it.n_q * p.g : 0;
+    return I;
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    paged_attn_kernel(const __grid_constant__ CUtensorMap tm_k,
+                      const __grid_constant__ CUtensorMap tm_v,
+                      const __grid_constant__ CUtensorMap tm_q1,
+                      const __grid_constant__ CUtensorMap tm_qn, const Params p) {
+    using L = Layout<D>;
+    constexpr int S = L::kStages;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                               ~uintptr_t(1023));
+    const uint32_t sb = smem_u32(smem);
+    const uint32_t bars = sb + L::kBar;
+    volatile int* abort_word = reinterpret_cast<volatile int*>(smem + L::kBar + kAbortOff);
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const auto bar = [&](int b) { return bars + 8 * b; };
 
     if (threadIdx.x == 0) {
         for (int b = 0; b < kNumBars; ++b)
-            mbar_init(bars + 8 * b, (b == kPFull || b == kQFull) ? 128 : 1);
+            mbar_init(bars + 8 * b, (b == kPFull || b == kOFree || b == kOFree + 1) ? 128
+                                    : (b >= kItemEmpty && b < kItemEmpty + 4) ? 130
+                                                                              : 1);
         *abort_word = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -275,254 +353,358 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + L::kBar + kHolderOff);
-    const uint32_t tm_s = tmem;
-    const uint32_t tm_o = tmem + 128;
 
     if (warp == 4) {
         // ------------------------------------------------------------ TMA producer
-        if (lane == 0 && n_tiles > 0) {
+        // The only role that reads work items and metadata from global memory: it publishes
+        // each item in a slot of the item ring, stages the item's block-table entries in
+        // shared memory (all 32 lanes load them at once), then lane 0 issues the TMA loads.
+        volatile ItemSlot* ring = reinterpret_cast<volatile ItemSlot*>(smem + L::kBar + kRingOff);
+        int32_t* tbl = reinterpret_cast<int32_t*>(smem + L::kBar + kTableOff);
+        if (lane == 0) {
             asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_k)) : "memory");
             asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_v)) : "memory");
-            const int32_t* trow = p.block_table + int64_t(seq) * p.max_blocks;
-            const int kvh = it.kv_head;
-            int issued = 0;
-            for (int jt = 0; jt < n_tiles; ++jt) {
-                const int st = jt & 1;
-                if (jt >= 2 && !wait_bounded(bars + 8 * (kKVEmpty0 + st), ((jt >> 1) - 1) & 1,
-                                             abort_word))
-                    break;
-                const int kb = k_begin + jt * kTileKeys;
-                const int key_hi = min(kb + kTileKeys, ctx_s);       // real keys end at ctx
-                const int nblk = (key_hi - kb + p.bs - 1) / p.bs;
-                const uint32_t bar = bars + 8 * (kKVFull0 + st);
-                mbar_expect_tx(bar, uint32_t(nblk) * p.bs * 128 * L::kChunks * 2);
-                const uint32_t dk = sb + L::kK + st * L::kKVStage;
-                const uint32_t dv = sb + L::kV + st * L::kKVStage;
-                for (int b = 0; b < nblk; ++b) {
-                    int phys = trow[kb / p.bs + b];
-                    if (phys < 0 || phys >= p.num_blocks) {
-                        // out of range: the box lands outside the tensor and reads as zeros
-                        if (p.err) atomicOr(p.err, PA_DEVERR_BLOCK);
-                        phys = -1;
-                    }
-                    const int z = phys * p.bs;
-                    for (int h = 0; h < L::kChunks; ++h) {
-                        const uint32_t off = h * L::kKVHalf + b * p.bs * 128;
-                        tma_load_3d(dk + off, &tm_k, bar, 64 * h, kvh, z);
-                        tma_load_3d(dv + off, &tm_v, bar, 64 * h, kvh, z);
+            asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_q1)) : "memory");
+            asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_qn)) : "memory");
+        }
+        int tc = 0, ic = 0;
+        int ok = 1;
+        int idx = blockIdx.x;
+        for (;;) {
+            Item I;
+            I.good = false;
+            for (; idx < p.n_items; idx += gridDim.x) {
+                I = load_item(p, idx);
+                if (I.good) break;
+                if (lane == 0 && p.err) atomicOr(p.err, PA_DEVERR_META);
+            }
+            const bool have = idx < p.n_items;
+            const int slot = ic & 3;
+            if (lane == 0) {
+                if (ic >= 4)
+                    ok = wait_bounded(bar(kItemEmpty + slot), ((ic >> 2) - 1) & 1, abort_word);
+                if (ok) {
+                    volatile ItemSlot* sl = ring + slot;
+                    sl->seq = I.seq;
+                    sl->ctx = I.ctx;
+                    sl->q_start = I.q_start;
+                    sl->n_q = I.n_q;
+                    sl->kvh = I.kvh;
+                    sl->split = I.split;
+                    sl->pos0 = I.pos0;
+                    sl->k_begin = I.k_begin;
+                    sl->n_tiles = I.n_tiles;
+                    sl->rows_valid = I.rows_valid;
+                    sl->last = have ? 0 : 1;
+                    mbar_arrive(bar(kItemFull + slot));
+                }
+            }
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (!ok || !have) break;
+            // the item's block-table entries, loaded by the whole warp
+            const int key_end = min(I.k_begin + I.n_tiles * kTileKeys, I.ctx);
+            const int first = I.k_begin / p.bs;
+            const int n_ent = min((key_end - I.k_begin + p.bs - 1) / p.bs, kMaxTableEntries);
+            const int32_t* trow = p.block_table + int64_t(I.seq) * p.max_blocks + first;
+            __syncwarp();
+            for (int e = lane; e < n_ent; e += 32) tbl[e] = __ldg(trow + e);
+            __syncwarp();
+            if (lane == 0) {
+                const int qb = ic & 1;
+                if (ic >= 2)
+                    ok = wait_bounded(bar(kQEmpty + qb), ((ic >> 1) - 1) & 1, abort_word);
+                if (ok) {   // Q: rows (token, head-in-group), one box per 64-column chunk
+                    const bool dec = I.n_q == 1;
+                    const CUtensorMap* tq = dec ? &tm_q1 : &tm_qn;
+                    const uint32_t rows = dec ? uint32_t(p.g) : uint32_t(kRows);
+                    mbar_expect_tx(bar(kQFull + qb), rows * 128 * L::kChunks);
+                    for (int h = 0; h < L::kChunks; ++h)
+                        tma_load_3d(sb + L::kQ + qb * L::kQBuf + h * L::kQHalf, tq,
+                                    bar(kQFull + qb), 64 * h, I.kvh * p.g, I.q_start);
+                }
+                for (int jt = 0; ok && jt < I.n_tiles; ++jt, ++tc) {
+                    const int st = tc % S;
+                    if (tc >= S &&
+                        !(ok = wait_bounded(bar(kKVEmpty + st), ((tc / S) - 1) & 1, abort_word)))
+                        break;
+                    const int kb = I.k_begin + jt * kTileKeys;
+                    const int key_hi = min(kb + kTileKeys, I.ctx);   // real keys end at ctx
+                    const int nblk = (key_hi - kb + p.bs - 1) / p.bs;
+                    mbar_expect_tx(bar(kKVFull + st), uint32_t(nblk) * p.bs * 128 * L::kChunks * 2);
+                    const uint32_t dk = sb + L::kK + st * L::kKVTile;
+                    const uint32_t dv = sb + L::kV + st * L::kKVTile;
+                    const int e0 = (kb - I.k_begin) / p.bs;
+                    for (int b = 0; b < nblk; ++b) {
+                        int phys = tbl[e0 + b];
+                        if (phys < 0 || phys >= p.num_blocks) {
+                            // out of range: the box lands outside the tensor and reads zeros
+                            if (p.err) atomicOr(p.err, PA_DEVERR_BLOCK);
+                            phys = -1;
+                        }
+                        const int z = phys * p.bs;
+                        for (int h = 0; h < L::kChunks; ++h) {
+                            const uint32_t off = h * L::kKVHalf + b * p.bs * 128;
+                            tma_load_3d(dk + off, &tm_k, bar(kKVFull + st), 64 * h, I.kvh, z);
+                            tma_load_3d(dv + off, &tm_v, bar(kKVFull + st), 64 * h, I.kvh, z);
+                        }
                     }
                 }
-                ++issued;
             }
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (!ok) break;
+            idx += gridDim.x;
+            ++ic;
+        }
+        if (lane == 0) {
             // never leave with copies in flight into this CTA's shared memory
-            for (int jt = max(0, issued - 2); jt < issued; ++jt)
-                wait_bounded(bars + 8 * (kKVFull0 + (jt & 1)), (jt >> 1) & 1, abort_word);
+            for (int t = max(0, tc - S); t < tc; ++t)
+                wait_bounded(bar(kKVFull + t % S), (t / S) & 1, abort_word);
+            for (int i = max(0, ic - 2); i < ic; ++i)
+                wait_bounded(bar(kQFull + (i & 1)), (i >> 1) & 1, abort_word);
         }
     } else if (warp == 5) {
         // ------------------------------------------------------------ MMA issuer
-        if (lane == 0 && n_tiles > 0) {
+        if (lane == 0) {
             constexpr uint32_t idesc_s = make_idesc(kRows, kTileKeys, false);
             constexpr uint32_t idesc_o = make_idesc(kRows, D, true);
-            const auto issue_s = [&](int jt) {
-                const uint32_t kbase = sb + L::kK + (jt & 1) * L::kKVStage;
+            const auto issue_s = [&](int qb, int st, uint32_t d) {
+                const uint32_t qbase = sb + L::kQ + qb * L::kQBuf;
+                const uint32_t kbase = sb + L::kK + st * L::kKVTile;
 #pragma unroll
                 for (int k = 0; k < D / 16; ++k) {
-                    const uint32_t qa = sb + L::kQ + (k >> 2) * L::kQHalf + (k & 3) * 32;
+                    const uint32_t qa = qbase + (k >> 2) * L::kQHalf + (k & 3) * 32;
                     const uint32_t ka = kbase + (k >> 2) * L::kKVHalf + (k & 3) * 32;
-                    umma_bf16(tm_s, make_sdesc(qa, 16, 1024), make_sdesc(ka, 16, 1024), idesc_s,
+                    umma_bf16(d, make_sdesc(qa, 16, 1024), make_sdesc(ka, 16, 1024), idesc_s,
                               k > 0);
                 }
             };
-            const auto issue_pv = [&](int jt) {
-                const uint32_t vbase = sb + L::kV + (jt & 1) * L::kKVStage;
+            const auto issue_pv = [&](int st, uint32_t d, bool acc) {
+                const uint32_t vbase = sb + L::kV + st * L::kKVTile;
 #pragma unroll
                 for (int k = 0; k < kTileKeys / 16; ++k) {
                     const uint32_t pa = sb + L::kP + (k >> 2) * (kRows * 128) + (k & 3) * 32;
                     const uint32_t va = vbase + k * 16 * 128;
-                    umma_bf16(tm_o, make_sdesc(pa, 16, 1024), make_sdesc(va, L::kKVHalf, 1024),
-                              idesc_o, (jt > 0 || k > 0) ? 1u : 0u);
+                    umma_bf16(d, make_sdesc(pa, 16, 1024), make_sdesc(va, L::kKVHalf, 1024),
+                              idesc_o, (acc || k > 0) ? 1u : 0u);
                 }
             };
-            bool ok = wait_bounded(bars + 8 * kQFull, 0, abort_word);
-            tc_fence_after();
-            for (int jt = 0; ok && jt < n_tiles; ++jt) {
-                if (jt > 0) {
-                    if (!(ok = wait_bounded(bars + 8 * kPFull, (jt - 1) & 1, abort_word))) break;
-                    tc_fence_after();
-                    issue_pv(jt - 1);
-                    tc_commit(bars + 8 * (kKVEmpty0 + ((jt - 1) & 1)));
+            // Two cursors walk the same item sequence: one issues S = Q K^T for the next tile
+            // as soon as its K has landed (and its S buffer is free), the other issues O += P V
+            // as soon as the softmax has produced P. Neither waits for the other, so the
+            // stage of a finished tile is released without waiting for the next tile's data.
+            struct Cursor {
+                int ic, jt, tc;
+                bool have, done;
+                Item I;
+            };
+            const volatile ItemSlot* ring =
+                reinterpret_cast<const volatile ItemSlot*>(smem + L::kBar + kRingOff);
+            // takes the cursor's next item from the ring once the producer has published it
+            const auto fetch = [&](Cursor& c) {
+                if (c.have || c.done) return;
+                const int slot = c.ic & 3;
+                if (!mbar_test_wait(bar(kItemFull + slot), (c.ic >> 2) & 1)) return;
+                bool last;
+                c.I = slot_item(ring + slot, &last);
+                mbar_arrive(bar(kItemEmpty + slot));
+                c.have = !last;
+                c.done = last;
+            };
+            const auto advance = [&](Cursor& c) {
+                ++c.tc;
+                if (++c.jt == c.I.n_tiles) {
+                    c.jt = 0;
+                    ++c.ic;
+                    c.have = false;
                 }
-                if (!(ok = wait_bounded(bars + 8 * (kKVFull0 + (jt & 1)), (jt >> 1) & 1,
-                                        abort_word)))
-                    break;
-                tc_fence_after();
-                issue_s(jt);
-                tc_commit(bars + 8 * kSFull);
-            }
-            if (ok && wait_bounded(bars + 8 * kPFull, (n_tiles - 1) & 1, abort_word)) {
-                tc_fence_after();
-                issue_pv(n_tiles - 1);
-                tc_commit(bars + 8 * (kKVEmpty0 + ((n_tiles - 1) & 1)));
-                tc_commit(bars + 8 * kOFull);
+            };
+            Cursor cs{0, 0, 0, false, false, Item{}}, cv{0, 0, 0, false, false, Item{}};
+            unsigned long long idle_since = 0;
+            while (!(cs.done && cv.done)) {
+                bool progress = false;
+                fetch(cv);
+                fetch(cs);
+                // O += P V for the oldest tile whose P is ready
+                if (cv.have && cv.tc < cs.tc && mbar_test_wait(bar(kPFull), cv.tc & 1) &&
+                    (cv.jt > 0 || cv.ic < 2 ||
+                     mbar_test_wait(bar(kOFree + (cv.ic & 1)), ((cv.ic >> 1) - 1) & 1))) {
+                    tc_fence_after();
+                    const int st = cv.tc % S;
+                    issue_pv(st, tmem + kTmemO + (cv.ic & 1) * 128, cv.jt > 0);
+                    tc_commit(bar(kKVEmpty + st));
+                    tc_commit(bar(kPVDone));
+                    advance(cv);
+                    progress = true;
+                }
+                // S = Q K^T for the next tile: its S buffer was last read by the softmax of
+                // tile cs.tc - 2, whose P the PV cursor has already consumed
+                if (cs.have && cs.tc <= cv.tc + 1 &&
+                    (cs.jt > 0 || mbar_test_wait(bar(kQFull + (cs.ic & 1)), (cs.ic >> 1) & 1)) &&
+                    mbar_test_wait(bar(kKVFull + cs.tc % S), (cs.tc / S) & 1)) {
+                    tc_fence_after();
+                    issue_s(cs.ic & 1, cs.tc % S, tmem + (cs.tc & 1) * 128);
+                    tc_commit(bar(kSFull + (cs.tc & 1)));
+                    if (cs.jt == cs.I.n_tiles - 1) tc_commit(bar(kQEmpty + (cs.ic & 1)));
+                    advance(cs);
+                    progress = true;
+                }
+                if (progress) {
+                    idle_since = 0;
+                } else {
+                    const unsigned long long now = global_ns();
+                    if (!idle_since) idle_since = now;
+                    if (*abort_word) break;
+                    if (now - idle_since > kWaitLimitNs) {
+                        *abort_word = 1;
+                        break;
+                    }
+                }
             }
             // drain: every MMA this thread issued has finished before TMEM is released
-            tc_commit(bars + 8 * kDrain);
-            wait_bounded(bars + 8 * kDrain, 0, abort_word);
+            tc_commit(bar(kDrain));
+            wait_bounded(bar(kDrain), 0, abort_word);
         }
     } else {
         // ------------------------------------------------------------ softmax warps 0-3
         const int tid = threadIdx.x;              // 0..127
-        // zero P, then stage Q rows (token-major, head-in-group minor) in the swizzled layout
         for (int i = tid; i < 2 * kRows * 8; i += 128) st_shared_zero16(sb + L::kP + i * 16);
-        constexpr int kRowChunks = D / 8;          // 16-byte chunks per row
-        for (int i = tid; i < kRows * kRowChunks; i += 128) {
-            const int r = i / kRowChunks;
-            const int ch = i % kRowChunks;
-            const uint32_t dst = sb + L::kQ + (ch >> 3) * L::kQHalf + swz(r, ch & 7);
-            uint4 v = make_uint4(0, 0, 0, 0);
-            if (r < rows_valid) {
-                const int tok = it.q_start + r / p.g;
-                const int head = it.kv_head * p.g + r % p.g;
-                v = __ldg(reinterpret_cast<const uint4*>(p.q + (int64_t(tok) * p.Hq + head) * D) + ch);
-            }
-            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(v.x), "r"(v.y),
-                         "r"(v.z), "r"(v.w)
-                         : "memory");
-        }
         fence_proxy_async();
-        mbar_arrive(bars + 8 * kQFull);            // all 128 softmax threads arrive
-
         const int q4 = lane & 3;
         const int rs = lane >> 2;
-        bool half_on[2];
-        int pos[2][2];
-        float m_run[2][2], l_run[2][2], alpha[2][2];
-#pragma unroll
-        for (int hb = 0; hb < 2; ++hb) {
-            half_on[hb] = (32 * warp + 16 * hb) < rows_valid;
-#pragma unroll
-            for (int sr = 0; sr < 2; ++sr) {
-                const int row = 32 * warp + 16 * hb + rs + 8 * sr;
-                pos[hb][sr] = row < rows_valid ? pos0 + row / p.g : -1;
-                m_run[hb][sr] = -INFINITY;
-                l_run[hb][sr] = 0.f;
-                alpha[hb][sr] = 1.f;
-            }
-        }
         const float c = p.c;
+        const volatile ItemSlot* ring =
+            reinterpret_cast<const volatile ItemSlot*>(smem + L::kBar + kRingOff);
+        int tc = 0, ic = 0;
         bool ok = true;
-        for (int jt = 0; jt < n_tiles; ++jt) {
-            if (!(ok = wait_bounded(bars + 8 * kSFull, jt & 1, abort_word))) break;
-            tc_fence_after();
-            const int kb = k_begin + jt * kTileKeys;
+        for (;;) {
+            if (!(ok = wait_bounded(bar(kItemFull + (ic & 3)), (ic >> 2) & 1, abort_word))) break;
+            bool last;
+            const Item I = slot_item(ring + (ic & 3), &last);
+            mbar_arrive(bar(kItemEmpty + (ic & 3)));
+            if (last) break;
+            const int ob = ic & 1;
+            const uint32_t tm_o = tmem + kTmemO + ob * 128;
+            bool half_on[2];
+            int pos[2][2];
+            float m_run[2][2], l_run[2][2];
 #pragma unroll
             for (int hb = 0; hb < 2; ++hb) {
-                if (!half_on[hb]) continue;
-                uint32_t r[64];
-                tmem_ld_16x256b_x16(tm_s + (uint32_t(32 * warp + 16 * hb) << 16), r);
-                tmem_wait_ld();
+                half_on[hb] = (32 * warp + 16 * hb) < I.rows_valid;
 #pragma unroll
                 for (int sr = 0; sr < 2; ++sr) {
                     const int row = 32 * warp + 16 * hb + rs + 8 * sr;
-                    const int pr = pos[hb][sr];
-                    float sv[32];
-                    float mx = -INFINITY;
-#pragma unroll
-                    for (int cc = 0; cc < 16; ++cc)
-#pragma unroll
-                        for (int e = 0; e < 2; ++e) {
-                            const int key = kb + 8 * cc + 2 * q4 + e;
-                            const float s = key <= pr ? __uint_as_float(r[4 * cc + 2 * sr + e])
-                                                      : -INFINITY;
-                            sv[2 * cc + e] = s;
-                            mx = fmaxf(mx, s);
-                        }
-                    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-                    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-                    const float m_new = fmaxf(m_run[hb][sr], mx);
-                    const float m_use = m_new == -INFINITY ? 0.f : m_new;
-                    const float a = m_run[hb][sr] == m_use
-                                        ? 1.f
-                                        : ex2(__fmul_rn(__fsub_rn(m_run[hb][sr], m_use), c));
-                    const float nmc = __fmul_rn(-m_use, c);
-                    float sum = 0.f;
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) {
-                        sv[i] = ex2(__fmaf_rn(sv[i], c, nmc));
-                        sum = __fadd_rn(sum, sv[i]);
-                    }
-                    sum = __fadd_rn(sum, __shfl_xor_sync(0xffffffffu, sum, 1));
-                    sum = __fadd_rn(sum, __shfl_xor_sync(0xffffffffu, sum, 2));
-                    l_run[hb][sr] = __fadd_rn(__fmul_rn(l_run[hb][sr], a), sum);
-                    m_run[hb][sr] = m_new;
-                    alpha[hb][sr] = a;
-#pragma unroll
-                    for (int cc = 0; cc < 16; ++cc) {
-                        const uint32_t addr = sb + L::kP + (cc >> 3) * (kRows * 128) +
-                                              swz(row, cc & 7) + 4 * q4;
-                        st_shared_u32(addr, pack_bf16(sv[2 * cc], sv[2 * cc + 1]));
-                    }
+                    pos[hb][sr] = row < I.rows_valid ? I.pos0 + row / p.g : -1;
+                    m_run[hb][sr] = -INFINITY;
+                    l_run[hb][sr] = 0.f;
                 }
             }
-            // keys at or beyond ctx are stale or never loaded: give them zero values so that
-            // their (zero) probabilities contribute exact zeros
-            if (kb + kTileKeys > ctx_s) {
-                const int r0 = max(ctx_s - kb, 0);
-                const int nrow = kTileKeys - r0;
-                const uint32_t vb = sb + L::kV + (jt & 1) * L::kKVStage;
-                for (int i = tid; i < nrow * 8 * L::kChunks; i += 128) {
-                    const int h = i / (nrow * 8);
-                    const int rem = i % (nrow * 8);
-                    st_shared_zero16(vb + h * L::kKVHalf + (r0 + rem / 8) * 128 + (rem % 8) * 16);
-                }
-            }
-            if (jt > 0) {
+            for (int jt = 0; jt < I.n_tiles; ++jt, ++tc) {
+                if (!(ok = wait_bounded(bar(kSFull + (tc & 1)), (tc >> 1) & 1, abort_word)))
+                    break;
+                tc_fence_after();
+                const int kb = I.k_begin + jt * kTileKeys;
+                float alpha[2][2];
+                uint32_t pk[2][2][16];               // P rounded to bf16, packed in pairs
 #pragma unroll
                 for (int hb = 0; hb < 2; ++hb) {
                     if (!half_on[hb]) continue;
-                    const bool need = alpha[hb][0] != 1.f || alpha[hb][1] != 1.f;
-                    if (!__any_sync(0xffffffffu, need)) continue;
-                    const uint32_t ta = tm_o + (uint32_t(32 * warp + 16 * hb) << 16);
-                    if constexpr (D == 128) {
-                        uint32_t o[64];
-                        tmem_ld_16x256b_x16(ta, o);
-                        tmem_wait_ld();
+                    uint32_t r[64];
+                    tmem_ld_16x256b_x16(tmem + (tc & 1) * 128 + (uint32_t(32 * warp + 16 * hb) << 16), r);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int sr = 0; sr < 2; ++sr) {
+                        const int pr = pos[hb][sr];
+                        float sv[32];
+                        float mx = -INFINITY;
 #pragma unroll
                         for (int cc = 0; cc < 16; ++cc)
 #pragma unroll
-                            for (int sr = 0; sr < 2; ++sr)
+                            for (int e = 0; e < 2; ++e) {
+                                const int key = kb + 8 * cc + 2 * q4 + e;
+                                const float s = key <= pr ? __uint_as_float(r[4 * cc + 2 * sr + e])
+                                                          : -INFINITY;
+                                sv[2 * cc + e] = s;
+                                mx = fmaxf(mx, s);
+                            }
+                        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+                        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+                        const float m_new = fmaxf(m_run[hb][sr], mx);
+                        const float m_use = m_new == -INFINITY ? 0.f : m_new;
+                        const float a = m_run[hb][sr] == m_use
+                                            ? 1.f
+                                            : ex2(__fmul_rn(__fsub_rn(m_run[hb][sr], m_use), c));
+                        const float nmc = __fmul_rn(-m_use, c);
+                        float sum = 0.f;
 #pragma unroll
-                                for (int e = 0; e < 2; ++e) {
-                                    const int k = 4 * cc + 2 * sr + e;
-                                    o[k] = __float_as_uint(
-                                        __fmul_rn(__uint_as_float(o[k]), alpha[hb][sr]));
-                                }
-                        tmem_st_16x256b_x16(ta, o);
-                    } else {
-                        uint32_t o[32];
-                        tmem_ld_16x256b_x8(ta, o);
-                        tmem_wait_ld();
+                        for (int i = 0; i < 32; ++i) {
+                            sv[i] = ex2(__fmaf_rn(sv[i], c, nmc));
+                            sum = __fadd_rn(sum, sv[i]);
+                        }
+                        sum = __fadd_rn(sum, __shfl_xor_sync(0xffffffffu, sum, 1));
+                        sum = __fadd_rn(sum, __shfl_xor_sync(0xffffffffu, sum, 2));
+                        l_run[hb][sr] = __fadd_rn(__fmul_rn(l_run[hb][sr], a), sum);
+                        m_run[hb][sr] = m_new;
+                        alpha[hb][sr] = a;
 #pragma unroll
-                        for (int cc = 0; cc < 8; ++cc)
-#pragma unroll
-                            for (int sr = 0; sr < 2; ++sr)
-#pragma unroll
-                                for (int e = 0; e < 2; ++e) {
-                                    const int k = 4 * cc + 2 * sr + e;
-                                    o[k] = __float_as_uint(
-                                        __fmul_rn(__uint_as_float(o[k]), alpha[hb][sr]));
-                                }
-                        tmem_st_16x256b_x8(ta, o);
+                        for (int cc = 0; cc < 16; ++cc)
+                            pk[hb][sr][cc] = pack_bf16(sv[2 * cc], sv[2 * cc + 1]);
                     }
                 }
+                // P and O belong to the previous tile's PV until it has finished
+                if (tc > 0 && !(ok = wait_bounded(bar(kPVDone), (tc - 1) & 1, abort_word))) break;
+                tc_fence_after();
+#pragma unroll
+                for (int hb = 0; hb < 2; ++hb) {
+                    if (!half_on[hb]) continue;
+#pragma unroll
+                    for (int sr = 0; sr < 2; ++sr) {
+                        const int row = 32 * warp + 16 * hb + rs + 8 * sr;
+#pragma unroll
+                        for (int cc = 0; cc < 16; ++cc)
+                            st_shared_u32(sb + L::kP + (cc >> 3) * (kRows * 128) +
+                                              swz(row, cc & 7) + 4 * q4,
+                                          pk[hb][sr][cc]);
+                    }
+                    if (jt == 0) continue;
+                    const bool need = alpha[hb][0] != 1.f || alpha[hb][1] != 1.f;
+                    if (!__any_sync(0xffffffffu, need)) continue;
+                    const uint32_t ta = tm_o + (uint32_t(32 * warp + 16 * hb) << 16);
+                    uint32_t o[D / 2];
+                    if constexpr (D == 128) tmem_ld_16x256b_x16(ta, o);
+                    else tmem_ld_16x256b_x8(ta, o);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int cc = 0; cc < D / 8; ++cc)
+#pragma unroll
+                        for (int sr = 0; sr < 2; ++sr)
+#pragma unroll
+                            for (int e = 0; e < 2; ++e) {
+                                const int k = 4 * cc + 2 * sr + e;
+                                o[k] = __float_as_uint(__fmul_rn(__uint_as_float(o[k]), alpha[hb][sr]));
+                            }
+                    if constexpr (D == 128) tmem_st_16x256b_x16(ta, o);
+                    else tmem_st_16x256b_x8(ta, o);
+                }
                 tmem_wait_st();
+                // keys at or beyond ctx are stale or were never loaded: give them zero values
+                // so that their (zero) probabilities contribute exact zeros
+                if (kb + kTileKeys > I.ctx) {
+                    const int r0 = max(I.ctx - kb, 0);
+                    const int nrow = kTileKeys - r0;
+                    const uint32_t vb = sb + L::kV + (tc % S) * L::kKVTile;
+                    for (int i = tid; i < nrow * 8 * L::kChunks; i += 128) {
+                        const int h = i / (nrow * 8);
+                        const int rem = i % (nrow * 8);
+                        st_shared_zero16(vb + h * L::kKVHalf + (r0 + rem / 8) * 128 + (rem % 8) * 16);
+                    }
+                }
+                fence_proxy_async();
+                tc_fence_before();
+                mbar_arrive(bar(kPFull));            // all 128 softmax threads arrive
             }
-            fence_proxy_async();
-            tc_fence_before();
-            mbar_arrive(bars + 8 * kPFull);        // all 128 softmax threads arrive
-        }
-        // ---------------------------------------------------------------- epilogue
-        if (ok && n_tiles > 0 && wait_bounded(bars + 8 * kOFull, 0, abort_word)) {
+            if (!ok) break;
+            // ---------------------------------------------------------------- epilogue
+            if (!(ok = wait_bounded(bar(kPVDone), (tc - 1) & 1, abort_word))) break;
             tc_fence_after();
 #pragma unroll
             for (int hb = 0; hb < 2; ++hb) {
@@ -535,12 +717,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int sr = 0; sr < 2; ++sr) {
                     const int row = 32 * warp + 16 * hb + rs + 8 * sr;
-                    if (row >= rows_valid) continue;
+                    if (row >= I.rows_valid) continue;
                     const int pr = pos[hb][sr];
                     const int nsp = pr / kSplit + 1;
-                    if (it.split >= nsp) continue;      // the row has no keys in this split
-                    const int tok = it.q_start + row / p.g;
-                    const int head = it.kv_head * p.g + row % p.g;
+                    if (I.split >= nsp) continue;        // the row has no keys in this split
+                    const int tok = I.q_start + row / p.g;
+                    const int head = I.kvh * p.g + row % p.g;
                     if (nsp == 1) {
                         const float lsum = l_run[hb][sr];
                         __nv_bfloat16* dst = p.out + (int64_t(tok) * p.Hq + head) * D;
@@ -551,7 +733,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             *reinterpret_cast<uint32_t*>(dst + 8 * cc + 2 * q4) = pack_bf16(x0, x1);
                         }
                     } else {
-                        const int64_t slot = (int64_t(tok) * p.max_splits + it.split) * p.Hq + head;
+                        const int64_t slot = (int64_t(tok) * p.max_splits + I.split) * p.Hq + head;
                         float* acc = p.ws_acc + slot * D;
 #pragma unroll
                         for (int cc = 0; cc < D / 8; ++cc)
@@ -564,6 +746,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
             }
+            tc_fence_before();
+            mbar_arrive(bar(kOFree + ob));           // all 128 softmax threads arrive
+            ++ic;
         }
     }
     if (*abort_word && threadIdx.x == 0 && p.err) atomicOr(p.err, PA_DEVERR_TIMEOUT);
@@ -652,47 +837,128 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
-// Pool viewed as a 3-D tensor {D, Hkv, num_blocks * block_size}; one box is one block of one
-// KV head and one 64-element column chunk, 128-byte swizzled in shared memory.
-int32_t make_pool_map(CUtensorMap* m, const void* pool, const pa_shape* s) {
+// A bf16 3-D tensor {D, heads, rows} with 128-byte swizzled boxes {64, box_heads, box_rows}.
+int32_t make_map(CUtensorMap* m, const void* base, int D, int heads, int64_t rows,
+                 int box_heads, int box_rows) {
     auto fn = encode_fn();
     if (!fn) return PA_ERR_CUDA;
-    const cuuint64_t dims[3] = {cuuint64_t(s->head_dim), cuuint64_t(s->num_kv_heads),
-                                cuuint64_t(s->num_blocks) * s->block_size};
-    const cuuint64_t strides[2] = {cuuint64_t(s->head_dim) * 2,
-                                   cuuint64_t(s->num_kv_heads) * s->head_dim * 2};
-    const cuuint32_t box[3] = {64, 1, cuuint32_t(s->block_size)};
+    const cuuint64_t dims[3] = {cuuint64_t(D), cuuint64_t(heads), cuuint64_t(rows)};
+    const cuuint64_t strides[2] = {cuuint64_t(D) * 2, cuuint64_t(heads) * D * 2};
+    const cuuint32_t box[3] = {64, cuuint32_t(box_heads), cuuint32_t(box_rows)};
     const cuuint32_t estr[3] = {1, 1, 1};
-    const CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(pool), dims,
+    const CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims,
                           strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                           CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? PA_OK : PA_ERR_CUDA;
 }
 
+struct Maps {
+    CUtensorMap k, v, q1, qn;
+};
+
+// K/V pools as {D, Hkv, num_blocks * block_size}: one box is one block of one KV head and one
+// 64-column chunk. q as {D, Hq, T}: a decode item's box is its g heads of one token, a prefill
+// item's box is g heads of 128/g tokens (rows past the item are not used; past T they read 0).
+int32_t make_maps(Maps* m, const void* q, const void* k_pool, const void* v_pool, int32_t T,
+                  const pa_shape* s) {
+    const int D = s->head_dim;
+    const int g = s->num_q_heads / s->num_kv_heads;
+    const int64_t rows = int64_t(s->num_blocks) * s->block_size;
+    int32_t st;
+    if ((st = make_map(&m->k, k_pool, D, s->num_kv_heads, rows, 1, s->block_size))) return st;
+    if ((st = make_map(&m->v, v_pool, D, s->num_kv_heads, rows, 1, s->block_size))) return st;
+    if ((st = make_map(&m->q1, q, D, s->num_q_heads, T, g, 1))) return st;
+    return make_map(&m->qn, q, D, s->num_q_heads, T, g, kRows / g);
+}
+
+int32_t sm_count_for_current_device(int* n) {
+    static int cached[64] = {};
+    int dev = 0;
+    int32_t st = note_cuda(cudaGetDevice(&dev));
+    if (st) return st;
+    if (dev >= 0 && dev < 64 && cached[dev]) {
+        *n = cached[dev];
+        return PA_OK;
+    }
+    int v = 0;
+    st = note_cuda(cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev));
+    if (st) return st;
+    if (dev >= 0 && dev < 64) cached[dev] = v;
+    *n = v;
+    return PA_OK;
+}
+
 template <int D>
-int32_t launch(const CUtensorMap& mk, const CUtensorMap& mv, const Params& prm, int32_t n_items,
-               int32_t B, int32_t T, int32_t max_ctx, cudaStream_t stream) {
+int32_t launch(const Maps& maps, const Params& prm, int32_t max_ctx, cudaStream_t stream) {
     static int attr_device = -1;          // device the shared-memory limit was raised on
     int dev = 0;
-    int32_t st0 = note_cuda(cudaGetDevice(&dev));
-    if (st0) return st0;
+    int32_t st = note_cuda(cudaGetDevice(&dev));
+    if (st) return st;
     if (attr_device != dev) {
-        st0 = note_cuda(cudaFuncSetAttribute(
+        st = note_cuda(cudaFuncSetAttribute(
             paged_attn_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, Layout<D>::kAlloc));
-        if (st0) return st0;
+        if (st) return st;
         attr_device = dev;
     }
-    paged_attn_kernel<D><<<n_items, kThreads, Layout<D>::kAlloc, stream>>>(mk, mv, prm);
-    int32_t st = note_cuda(cudaGetLastError());
-    if (st) return st;
+    int sms = 0;
+    if ((st = sm_count_for_current_device(&sms))) return st;
+    const int grid = std::min(prm.n_items, sms);
+    paged_attn_kernel<D><<<grid, kThreads, Layout<D>::kAlloc, stream>>>(maps.k, maps.v, maps.q1,
+                                                                       maps.qn, prm);
+    if ((st = note_cuda(cudaGetLastError()))) return st;
     if (max_ctx > kSplit) {
-        const int64_t warps = int64_t(T) * prm.Hq;
+        const int64_t warps = int64_t(prm.T) * prm.Hq;
         combine_kernel<D><<<unsigned((warps + 3) / 4), 128, 0, stream>>>(
-            prm.ws_acc, prm.ws_ml, prm.cu, prm.ctx, B, T, prm.Hq, prm.max_splits, prm.c, prm.out);
+            prm.ws_acc, prm.ws_ml, prm.cu, prm.ctx, prm.B, prm.T, prm.Hq, prm.max_splits, prm.c,
+            prm.out);
         st = note_cuda(cudaGetLastError());
     }
     return st;
+}
+
+// Host checks and parameter set-up shared by both step entry points.
+int32_t prepare_step(const void* q, const void* k_pool, const void* v_pool,
+                     const int32_t* block_table, int32_t max_blocks, const int32_t* cu_seqlens_q,
+                     const int32_t* ctx_lens, int32_t B, int32_t T, int32_t max_ctx,
+                     const pa_work_item* items, int32_t n_items, void* out,
+                     const pa_shape* shape, int32_t* err_flag, Maps* maps, Params* prm) {
+    int32_t st = check_shape(shape);
+    if (st) return st;
+    if (B < 0 || T < 0 || n_items < 0 || max_ctx < 0 || max_blocks < 0) return PA_ERR_INVALID;
+    if (!q || !k_pool || !v_pool || !block_table || !cu_seqlens_q || !ctx_lens || !items || !out)
+        return PA_ERR_INVALID;
+    if (int64_t(shape->num_blocks) * shape->block_size > INT32_MAX) return PA_ERR_SHAPE;
+    if ((reinterpret_cast<uintptr_t>(k_pool) | reinterpret_cast<uintptr_t>(v_pool) |
+         reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(out)) & 15)
+        return PA_ERR_INVALID;
+    if ((st = make_maps(maps, q, k_pool, v_pool, T, shape))) return st;
+    const int D = shape->head_dim;
+    prm->block_table = block_table;
+    prm->cu = cu_seqlens_q;
+    prm->ctx = ctx_lens;
+    prm->items = items;
+    prm->ws_acc = nullptr;
+    prm->ws_ml = nullptr;
+    prm->out = static_cast<__nv_bfloat16*>(out);
+    prm->err = err_flag;
+    prm->n_items = n_items;
+    prm->B = B;
+    prm->T = T;
+    prm->max_blocks = max_blocks;
+    prm->max_splits = int((int64_t(max_ctx) + kSplit - 1) / kSplit);
+    prm->Hq = shape->num_q_heads;
+    prm->Hkv = shape->num_kv_heads;
+    prm->g = shape->num_q_heads / shape->num_kv_heads;
+    prm->bs = shape->block_size;
+    prm->num_blocks = shape->num_blocks;
+    prm->c = float(1.4426950408889634 / std::sqrt(double(D)));
+    return PA_OK;
+}
+
+void point_workspace(Params* prm, float* ws, int32_t T, int32_t Hq, int D) {
+    prm->ws_acc = ws;
+    prm->ws_ml = ws ? ws + size_t(T) * prm->max_splits * Hq * D : nullptr;
 }
 
 }  // namespace
@@ -709,45 +975,16 @@ extern "C" int32_t paged_attention_step(const void* q, const void* k_pool, const
     if (st) return st;
     if (B < 0 || T < 0 || n_items < 0 || max_ctx < 0 || max_blocks < 0) return PA_ERR_INVALID;
     if (T == 0 || n_items == 0) return PA_OK;
-    if (!q || !k_pool || !v_pool || !block_table || !cu_seqlens_q || !ctx_lens || !items || !out)
-        return PA_ERR_INVALID;
-    if (int64_t(shape->num_blocks) * shape->block_size > INT32_MAX) return PA_ERR_SHAPE;
-    const size_t need = pa_workspace_bytes(shape, T, max_ctx);
-    if (max_ctx > kSplit && (!workspace || ws_bytes < need)) return PA_ERR_WORKSPACE;
-    if ((reinterpret_cast<uintptr_t>(k_pool) | reinterpret_cast<uintptr_t>(v_pool) |
-         reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(out)) & 15)
-        return PA_ERR_INVALID;
-
-    CUtensorMap mk, mv;
-    if ((st = make_pool_map(&mk, k_pool, shape))) return st;
-    if ((st = make_pool_map(&mv, v_pool, shape))) return st;
-
-    const int D = shape->head_dim;
-    const int max_splits = int((int64_t(max_ctx) + kSplit - 1) / kSplit);
+    if (max_ctx > kSplit && (!workspace || ws_bytes < pa_workspace_bytes(shape, T, max_ctx)))
+        return PA_ERR_WORKSPACE;
+    Maps maps;
     Params prm;
-    prm.q = static_cast<const __nv_bfloat16*>(q);
-    prm.block_table = block_table;
-    prm.cu = cu_seqlens_q;
-    prm.ctx = ctx_lens;
-    prm.items = items;
-    prm.ws_acc = static_cast<float*>(workspace);
-    prm.ws_ml = workspace ? static_cast<float*>(workspace) +
-                                size_t(T) * max_splits * shape->num_q_heads * D
-                          : nullptr;
-    prm.out = static_cast<__nv_bfloat16*>(out);
-    prm.err = err_flag;
-    prm.B = B;
-    prm.T = T;
-    prm.max_blocks = max_blocks;
-    prm.max_splits = max_splits;
-    prm.Hq = shape->num_q_heads;
-    prm.Hkv = shape->num_kv_heads;
-    prm.g = shape->num_q_heads / shape->num_kv_heads;
-    prm.bs = shape->block_size;
-    prm.num_blocks = shape->num_blocks;
-    prm.c = float(1.4426950408889634 / std::sqrt(double(D)));
-    if (D == 128) return launch<128>(mk, mv, prm, n_items, B, T, max_ctx, stream);
-    return launch<64>(mk, mv, prm, n_items, B, T, max_ctx, stream);
+    if ((st = prepare_step(q, k_pool, v_pool, block_table, max_blocks, cu_seqlens_q, ctx_lens, B,
+                           T, max_ctx, items, n_items, out, shape, err_flag, &maps, &prm)))
+        return st;
+    point_workspace(&prm, static_cast<float*>(workspace), T, shape->num_q_heads, shape->head_dim);
+    if (shape->head_dim == 128) return launch<128>(maps, prm, max_ctx, stream);
+    return launch<64>(maps, prm, max_ctx, stream);
 }
 
 // ------------------------------------------- allocation-free variant of the attention step
@@ -795,43 +1032,17 @@ extern "C" int32_t paged_attention_step_static_scratch(
     if (st) return st;
     if (B < 0 || T < 0 || n_items < 0 || max_ctx < 0 || max_blocks < 0) return PA_ERR_INVALID;
     if (T == 0 || n_items == 0) return PA_OK;
-    if (!q || !k_pool || !v_pool || !block_table || !cu_seqlens_q || !ctx_lens || !items || !out)
-        return PA_ERR_INVALID;
-    if (int64_t(shape->num_blocks) * shape->block_size > INT32_MAX) return PA_ERR_SHAPE;
-    if ((reinterpret_cast<uintptr_t>(k_pool) | reinterpret_cast<uintptr_t>(v_pool) |
-         reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(out)) & 15)
-        return PA_ERR_INVALID;
     // the partials of this step must fit the fixed array; nothing is launched otherwise
     if (max_ctx > kSplit && pa_workspace_bytes(shape, T, max_ctx) > PA_STATIC_SCRATCH_BYTES)
         return PA_ERR_WORKSPACE;
+    Maps maps;
+    Params prm;
+    if ((st = prepare_step(q, k_pool, v_pool, block_table, max_blocks, cu_seqlens_q, ctx_lens, B,
+                           T, max_ctx, items, n_items, out, shape, err_flag, &maps, &prm)))
+        return st;
     float* scratch = nullptr;
     if ((st = static_scratch_for_current_device(&scratch))) return st;
-
-    CUtensorMap mk, mv;
-    if ((st = make_pool_map(&mk, k_pool, shape))) return st;
-    if ((st = make_pool_map(&mv, v_pool, shape))) return st;
-    const int D = shape->head_dim;
-    const int max_splits = int((int64_t(max_ctx) + kSplit - 1) / kSplit);
-    Params prm;
-    prm.q = static_cast<const __nv_bfloat16*>(q);
-    prm.block_table = block_table;
-    prm.cu = cu_seqlens_q;
-    prm.ctx = ctx_lens;
-    prm.items = items;
-    prm.ws_acc = scratch;
-    prm.ws_ml = scratch + size_t(T) * max_splits * shape->num_q_heads * D;
-    prm.out = static_cast<__nv_bfloat16*>(out);
-    prm.err = err_flag;
-    prm.B = B;
-    prm.T = T;
-    prm.max_blocks = max_blocks;
-    prm.max_splits = max_splits;
-    prm.Hq = shape->num_q_heads;
-    prm.Hkv = shape->num_kv_heads;
-    prm.g = shape->num_q_heads / shape->num_kv_heads;
-    prm.bs = shape->block_size;
-    prm.num_blocks = shape->num_blocks;
-    prm.c = float(1.4426950408889634 / std::sqrt(double(D)));
-    if (D == 128) return launch<128>(mk, mv, prm, n_items, B, T, max_ctx, stream);
-    return launch<64>(mk, mv, prm, n_items, B, T, max_ctx, stream);
+    point_workspace(&prm, scratch, T, shape->num_q_heads, shape->head_dim);
+    if (shape->head_dim == 128) return launch<128>(maps, prm, max_ctx, stream);
+    return launch<64>(maps, prm, max_ctx, stream);
 }
