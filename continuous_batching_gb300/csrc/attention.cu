@@ -21,10 +21,13 @@
 // [s*1024, (s+1)*1024) and the ascending-order combine make them independent of the batch.
 //
 // Persistent schedule: one CTA per SM walks the items blockIdx.x, blockIdx.x + gridDim.x, ...
-// (the host orders items longest first). Warp roles (192 threads): warps 0-3 softmax /
-// rescale / epilogue, warp 4 TMA producer, warp 5 MMA issuer and TMEM owner. The producer
-// streams K/V tiles through a ring of shared-memory stages across item boundaries and loads
-// each item's Q tile by TMA into one of two Q buffers. TMEM holds two S buffers (S of the
+// (the host orders items longest first). Warp roles (256 threads): warps 0-3 softmax /
+// rescale / epilogue, warp 4 producer (reads the work items, publishes them in a ring, loads
+// each item's Q tile by TMA into one of two Q buffers), warp 5 MMA issuer and TMEM owner,
+// warp 6 K loader, warp 7 V loader. The loaders stream tiles by TMA through rings of
+// shared-memory slots across item boundaries; a K slot is free again as soon as S has read
+// it, a V slot once PV has. A paged tile is one box per block (K: one per 64-column half,
+// V: both halves in one box), issued from all 32 lanes of the loader warp. TMEM holds two S buffers (S of the
 // next tile is computed while the softmax works on the current one) and two O accumulators
 // (an item's epilogue overlaps the next item's MMAs). Every wait on an mbarrier is bounded.
 #include <cuda.h>
@@ -47,7 +50,7 @@ namespace {
 constexpr int kRows = PA_ROWS;
 constexpr int kTileKeys = PA_TILE_KEYS;
 constexpr int kSplit = PA_SPLIT_TOKENS;
-constexpr int kThreads = 192;
+constexpr int kThreads = 256;
 constexpr uint32_t kTmemCols = 512;     // S0 [0,128) S1 [128,256) O0 [256,384) O1 [384,512)
 constexpr uint32_t kTmemO = 256;
 constexpr unsigned long long kWaitLimitNs = 1000000000ull;   // one second per wait
@@ -66,33 +69,38 @@ struct Layout {
     static constexpr int kP = kQ + 2 * kQBuf;               // P: 128 rows x 128 keys, 2 chunks
     static constexpr int kK = kP + 2 * kRows * 128;
     static constexpr int kV = kK + kStages * kKVTile;
-    static constexpr int kBar = kV + kStages * kKVTile;     // barriers, item ring, table
-    static constexpr int kBytes = kBar + 1024;
+    static constexpr int kBar = kV + kStages * kKVTile;     // barriers, item ring, tables
+    static constexpr int kBytes = kBar + 1792;
     static constexpr int kAlloc = kBytes + 1024;            // room to align the base to 1024
 };
 
 // mbarrier slots (8 bytes each) at Layout::kBar
 enum Bar {
-    kKVFull = 0,     // + stage (up to 4): TMA -> MMA
-    kKVEmpty = 4,    // + stage: MMA (after PV) -> TMA
-    kQFull = 8,      // + buffer: TMA -> MMA
-    kQEmpty = 10,    // + buffer: MMA (after the item's last S) -> TMA
-    kSFull = 12,     // + buffer: MMA -> softmax
-    kPFull = 14,     // softmax (128 arrivals) -> MMA: P stored, O rescaled, V tail zeroed
-    kPVDone = 15,    // MMA -> softmax: the previous PV has finished
-    kOFree = 16,     // + buffer: epilogue (128 arrivals) -> MMA
-    kDrain = 18,
-    kItemFull = 19,  // + slot (4): producer -> everyone: the slot holds the next item
-    kItemEmpty = 23, // + slot: consumers (MMA 2 + softmax 128 arrivals) -> producer
-    kNumBars = 27
+    kKFull = 0,      // + stage (up to 4): TMA -> MMA (K of the tile landed)
+    kKEmpty = 4,     // + stage: MMA (after S) -> K loader
+    kVFull = 8,      // + stage: TMA -> MMA, softmax (V of the tile landed)
+    kVEmpty = 12,    // + stage: MMA (after PV) -> V loader
+    kQFull = 16,     // + buffer: TMA -> MMA
+    kQEmpty = 18,    // + buffer: MMA (after the item's last S) -> producer
+    kSFull = 20,     // + buffer: MMA -> softmax
+    kPFull = 22,     // softmax (128 arrivals) -> MMA: P stored, O rescaled, V tail zeroed
+    kPVDone = 23,    // MMA -> softmax: the previous PV has finished
+    kOFree = 24,     // + buffer: epilogue (128 arrivals) -> MMA
+    kDrain = 26,
+    kItemFull = 27,  // + slot (4): producer -> everyone: the slot holds the next item
+    kItemEmpty = 31, // + slot: consumers (MMA 2, softmax 128, loaders 64 arrivals) -> producer
+    kNumBars = 35
 };
 constexpr int kHolderOff = 8 * kNumBars;          // TMEM address written by tcgen05.alloc
 constexpr int kAbortOff = kHolderOff + 4;
-constexpr int kRingOff = 256;                     // 4 item slots of 64 bytes
-constexpr int kTableOff = 512;                    // block-table entries of the current item
+constexpr int kRingOff = 512;                     // 4 item slots of 64 bytes
+constexpr int kTableOff = 768;                    // per loader warp: the item's table entries
 constexpr int kMaxTableEntries = 128;             // 1024 keys / 8-token blocks
+static_assert(kAbortOff + 4 <= kRingOff, "control area");
 
 struct Params {
+    const __nv_bfloat16* k_pool;
+    const __nv_bfloat16* v_pool;
     const int32_t* block_table;
     const int32_t* cu;
     const int32_t* ctx;
@@ -181,6 +189,15 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map
         "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
         " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(dst),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y), "r"(z)
+        : "memory");
+}
+
+__device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
+                                            int32_t x, int32_t y, int32_t z, int32_t w) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4, %5, %6}], [%2];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y), "r"(z), "r"(w)
         : "memory");
 }
 
@@ -336,9 +353,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (threadIdx.x == 0) {
         for (int b = 0; b < kNumBars; ++b)
-            mbar_init(bars + 8 * b, (b == kPFull || b == kOFree || b == kOFree + 1) ? 128
-                                    : (b >= kItemEmpty && b < kItemEmpty + 4) ? 130
-                                                                              : 1);
+            mbar_init(bars + 8 * b,
+                      (b == kPFull || b == kOFree || b == kOFree + 1) ? 128
+                      : (b >= kItemEmpty && b < kItemEmpty + 4)       ? 2 + 128 + 64
+                                                                      : 1);
         *abort_word = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -355,19 +373,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + L::kBar + kHolderOff);
 
     if (warp == 4) {
-        // ------------------------------------------------------------ TMA producer
-        // The only role that reads work items and metadata from global memory: it publishes
-        // each item in a slot of the item ring, stages the item's block-table entries in
-        // shared memory (all 32 lanes load them at once), then lane 0 issues the TMA loads.
+        // ------------------------------------------------------------ producer
+        // Reads the work items from global memory, publishes each one in a slot of the item
+        // ring for the other roles, and loads its Q tile by TMA.
         volatile ItemSlot* ring = reinterpret_cast<volatile ItemSlot*>(smem + L::kBar + kRingOff);
-        int32_t* tbl = reinterpret_cast<int32_t*>(smem + L::kBar + kTableOff);
         if (lane == 0) {
-            asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_k)) : "memory");
-            asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_v)) : "memory");
             asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_q1)) : "memory");
             asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_qn)) : "memory");
         }
-        int tc = 0, ic = 0;
+        int ic = 0;
         int ok = 1;
         int idx = blockIdx.x;
         for (;;) {
@@ -401,54 +415,20 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             ok = __shfl_sync(0xffffffffu, ok, 0);
             if (!ok || !have) break;
-            // the item's block-table entries, loaded by the whole warp
-            const int key_end = min(I.k_begin + I.n_tiles * kTileKeys, I.ctx);
-            const int first = I.k_begin / p.bs;
-            const int n_ent = min((key_end - I.k_begin + p.bs - 1) / p.bs, kMaxTableEntries);
-            const int32_t* trow = p.block_table + int64_t(I.seq) * p.max_blocks + first;
-            __syncwarp();
-            for (int e = lane; e < n_ent; e += 32) tbl[e] = __ldg(trow + e);
-            __syncwarp();
+            // Q: rows (token, head-in-group), one box per 64-column chunk
+            const int qb = ic & 1;
+            if (lane == 0 && ic >= 2)
+                ok = wait_bounded(bar(kQEmpty + qb), ((ic >> 1) - 1) & 1, abort_word);
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (!ok) break;
             if (lane == 0) {
-                const int qb = ic & 1;
-                if (ic >= 2)
-                    ok = wait_bounded(bar(kQEmpty + qb), ((ic >> 1) - 1) & 1, abort_word);
-                if (ok) {   // Q: rows (token, head-in-group), one box per 64-column chunk
-                    const bool dec = I.n_q == 1;
-                    const CUtensorMap* tq = dec ? &tm_q1 : &tm_qn;
-                    const uint32_t rows = dec ? uint32_t(p.g) : uint32_t(kRows);
-                    mbar_expect_tx(bar(kQFull + qb), rows * 128 * L::kChunks);
-                    for (int h = 0; h < L::kChunks; ++h)
-                        tma_load_3d(sb + L::kQ + qb * L::kQBuf + h * L::kQHalf, tq,
-                                    bar(kQFull + qb), 64 * h, I.kvh * p.g, I.q_start);
-                }
-                for (int jt = 0; ok && jt < I.n_tiles; ++jt, ++tc) {
-                    const int st = tc % S;
-                    if (tc >= S &&
-                        !(ok = wait_bounded(bar(kKVEmpty + st), ((tc / S) - 1) & 1, abort_word)))
-                        break;
-                    const int kb = I.k_begin + jt * kTileKeys;
-                    const int key_hi = min(kb + kTileKeys, I.ctx);   // real keys end at ctx
-                    const int nblk = (key_hi - kb + p.bs - 1) / p.bs;
-                    mbar_expect_tx(bar(kKVFull + st), uint32_t(nblk) * p.bs * 128 * L::kChunks * 2);
-                    const uint32_t dk = sb + L::kK + st * L::kKVTile;
-                    const uint32_t dv = sb + L::kV + st * L::kKVTile;
-                    const int e0 = (kb - I.k_begin) / p.bs;
-                    for (int b = 0; b < nblk; ++b) {
-                        int phys = tbl[e0 + b];
-                        if (phys < 0 || phys >= p.num_blocks) {
-                            // out of range: the box lands outside the tensor and reads zeros
-                            if (p.err) atomicOr(p.err, PA_DEVERR_BLOCK);
-                            phys = -1;
-                        }
-                        const int z = phys * p.bs;
-                        for (int h = 0; h < L::kChunks; ++h) {
-                            const uint32_t off = h * L::kKVHalf + b * p.bs * 128;
-                            tma_load_3d(dk + off, &tm_k, bar(kKVFull + st), 64 * h, I.kvh, z);
-                            tma_load_3d(dv + off, &tm_v, bar(kKVFull + st), 64 * h, I.kvh, z);
-                        }
-                    }
-                }
+                const bool dec = I.n_q == 1;
+                const CUtensorMap* tq = dec ? &tm_q1 : &tm_qn;
+                const uint32_t rows = dec ? uint32_t(p.g) : uint32_t(kRows);
+                mbar_expect_tx(bar(kQFull + qb), rows * 128 * L::kChunks);
+                for (int h = 0; h < L::kChunks; ++h)
+                    tma_load_3d(sb + L::kQ + qb * L::kQBuf + h * L::kQHalf, tq, bar(kQFull + qb),
+                                64 * h, I.kvh * p.g, I.q_start);
             }
             ok = __shfl_sync(0xffffffffu, ok, 0);
             if (!ok) break;
@@ -457,8 +437,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (lane == 0) {
             // never leave with copies in flight into this CTA's shared memory
-            for (int t = max(0, tc - S); t < tc; ++t)
-                wait_bounded(bar(kKVFull + t % S), (t / S) & 1, abort_word);
             for (int i = max(0, ic - 2); i < ic; ++i)
                 wait_bounded(bar(kQFull + (i & 1)), (i >> 1) & 1, abort_word);
         }
@@ -478,13 +456,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                               k > 0);
                 }
             };
+            // V tile: block b of the tile at b * bs * 128 * chunks bytes, its 64-column halves
+            // bs * 128 bytes apart (MN-major B operand: LBO = half stride, SBO = 8-key stride)
+            const uint32_t v_lbo = uint32_t(p.bs) * 128;
+            const uint32_t v_sbo = p.bs >= 16 ? 1024u : uint32_t(p.bs) * 128 * L::kChunks;
             const auto issue_pv = [&](int st, uint32_t d, bool acc) {
                 const uint32_t vbase = sb + L::kV + st * L::kKVTile;
 #pragma unroll
                 for (int k = 0; k < kTileKeys / 16; ++k) {
                     const uint32_t pa = sb + L::kP + (k >> 2) * (kRows * 128) + (k & 3) * 32;
-                    const uint32_t va = vbase + k * 16 * 128;
-                    umma_bf16(d, make_sdesc(pa, 16, 1024), make_sdesc(va, L::kKVHalf, 1024),
+                    const int key = 16 * k;                  // first key of this 16-key step
+                    const uint32_t va = vbase + (key / p.bs) * (p.bs * 128 * L::kChunks) +
+                                        (key % p.bs) * 128;
+                    umma_bf16(d, make_sdesc(pa, 16, 1024), make_sdesc(va, v_lbo, v_sbo),
                               idesc_o, (acc || k > 0) ? 1u : 0u);
                 }
             };
@@ -526,12 +510,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 fetch(cs);
                 // O += P V for the oldest tile whose P is ready
                 if (cv.have && cv.tc < cs.tc && mbar_test_wait(bar(kPFull), cv.tc & 1) &&
+                    mbar_test_wait(bar(kVFull + cv.tc % S), (cv.tc / S) & 1) &&
                     (cv.jt > 0 || cv.ic < 2 ||
                      mbar_test_wait(bar(kOFree + (cv.ic & 1)), ((cv.ic >> 1) - 1) & 1))) {
                     tc_fence_after();
                     const int st = cv.tc % S;
                     issue_pv(st, tmem + kTmemO + (cv.ic & 1) * 128, cv.jt > 0);
-                    tc_commit(bar(kKVEmpty + st));
+                    tc_commit(bar(kVEmpty + st));
                     tc_commit(bar(kPVDone));
                     advance(cv);
                     progress = true;
@@ -540,9 +525,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // tile cs.tc - 2, whose P the PV cursor has already consumed
                 if (cs.have && cs.tc <= cv.tc + 1 &&
                     (cs.jt > 0 || mbar_test_wait(bar(kQFull + (cs.ic & 1)), (cs.ic >> 1) & 1)) &&
-                    mbar_test_wait(bar(kKVFull + cs.tc % S), (cs.tc / S) & 1)) {
+                    mbar_test_wait(bar(kKFull + cs.tc % S), (cs.tc / S) & 1)) {
                     tc_fence_after();
                     issue_s(cs.ic & 1, cs.tc % S, tmem + (cs.tc & 1) * 128);
+                    tc_commit(bar(kKEmpty + cs.tc % S));
                     tc_commit(bar(kSFull + (cs.tc & 1)));
                     if (cs.jt == cs.I.n_tiles - 1) tc_commit(bar(kQEmpty + (cs.ic & 1)));
                     advance(cs);
@@ -563,6 +549,87 @@ __global__ void __launch_bounds__(kThreads, 1)
             // drain: every MMA this thread issued has finished before TMEM is released
             tc_commit(bar(kDrain));
             wait_bounded(bar(kDrain), 0, abort_word);
+        }
+    } else if (warp >= 6) {
+        // ------------------------------------------------------------ K (warp 6) / V (warp 7)
+        const bool is_v = warp == 7;
+        int32_t* tbl = reinterpret_cast<int32_t*>(smem + L::kBar + kTableOff) +
+                       (warp - 6) * kMaxTableEntries;
+        const volatile ItemSlot* ring =
+            reinterpret_cast<const volatile ItemSlot*>(smem + L::kBar + kRingOff);
+        const CUtensorMap* tmap = is_v ? &tm_v : &tm_k;
+        if (lane == 0)
+            asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tmap)) : "memory");
+        const int log2bs = __ffs(p.bs) - 1;
+        // boxes per block: K one per 64-column half; V one (both halves) when D = 128
+        const int boxes_per_block = is_v ? 1 : L::kChunks;
+        const int full_b = is_v ? kVFull : kKFull;
+        const int empty_b = is_v ? kVEmpty : kKEmpty;
+        const uint32_t slots = sb + (is_v ? L::kV : L::kK);
+        int tc = 0, ic = 0;
+        int ok = 1;
+        for (;;) {
+            if (lane == 0)
+                ok = wait_bounded(bar(kItemFull + (ic & 3)), (ic >> 2) & 1, abort_word);
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (!ok) break;
+            bool last;
+            const Item I = slot_item(ring + (ic & 3), &last);
+            mbar_arrive(bar(kItemEmpty + (ic & 3)));     // all 32 lanes arrive
+            if (last) break;
+            const int key_end = min(I.k_begin + I.n_tiles * kTileKeys, I.ctx);
+            const int first = I.k_begin >> log2bs;
+            const int n_ent = min((key_end - I.k_begin + p.bs - 1) >> log2bs, kMaxTableEntries);
+            const int32_t* trow = p.block_table + int64_t(I.seq) * p.max_blocks + first;
+            __syncwarp();
+            for (int e = lane; e < n_ent; e += 32) {
+                int b = __ldg(trow + e);
+                if (b < 0 || b >= p.num_blocks) {
+                    // out of range: the box lands outside the tensor and reads zeros
+                    if (p.err && !is_v) atomicOr(p.err, PA_DEVERR_BLOCK);
+                    b = -1;
+                }
+                tbl[e] = b;
+            }
+            __syncwarp();
+            for (int jt = 0; jt < I.n_tiles; ++jt, ++tc) {
+                const int st = tc % S;
+                if (lane == 0 && tc >= S)
+                    ok = wait_bounded(bar(empty_b + st), ((tc / S) - 1) & 1, abort_word);
+                ok = __shfl_sync(0xffffffffu, ok, 0);
+                if (!ok) break;
+                const int kb = I.k_begin + jt * kTileKeys;
+                const int key_hi = min(kb + kTileKeys, I.ctx);   // real keys end at ctx
+                const int nblk = (key_hi - kb + p.bs - 1) >> log2bs;
+                if (lane == 0)
+                    mbar_expect_tx(bar(full_b + st), uint32_t(nblk) * p.bs * 128 * L::kChunks);
+                __syncwarp();
+                const uint32_t dst = slots + st * L::kKVTile;
+                const int e0 = (kb - I.k_begin) >> log2bs;
+                for (int j = lane; j < nblk * boxes_per_block; j += 32) {
+                    const int b = j / boxes_per_block;
+                    const int r = j - b * boxes_per_block;
+                    const int z = tbl[e0 + b] * p.bs;
+                    if (!is_v) {
+                        // K: half r of the block, rows of the 128-key tile at 128-byte stride
+                        tma_load_3d(dst + r * L::kKVHalf + b * p.bs * 128, tmap, bar(full_b + st),
+                                    64 * r, I.kvh, z);
+                    } else if constexpr (L::kChunks == 2) {
+                        // V: both halves of the block, [half][row] inside the block
+                        tma_load_4d(dst + b * p.bs * 256, tmap, bar(full_b + st), 0, z, 0, I.kvh);
+                    } else {
+                        tma_load_3d(dst + b * p.bs * 128, tmap, bar(full_b + st), 0, I.kvh, z);
+                    }
+                }
+            }
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (!ok) break;
+            ++ic;
+        }
+        if (lane == 0) {
+            // never leave with copies in flight into this CTA's shared memory
+            for (int t = max(0, tc - S); t < tc; ++t)
+                wait_bounded(bar(full_b + t % S), (t / S) & 1, abort_word);
         }
     } else {
         // ------------------------------------------------------------ softmax warps 0-3
@@ -689,13 +756,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // keys at or beyond ctx are stale or were never loaded: give them zero values
                 // so that their (zero) probabilities contribute exact zeros
                 if (kb + kTileKeys > I.ctx) {
+                    if (!(ok = wait_bounded(bar(kVFull + tc % S), (tc / S) & 1, abort_word))) break;
                     const int r0 = max(I.ctx - kb, 0);
                     const int nrow = kTileKeys - r0;
                     const uint32_t vb = sb + L::kV + (tc % S) * L::kKVTile;
                     for (int i = tid; i < nrow * 8 * L::kChunks; i += 128) {
-                        const int h = i / (nrow * 8);
+                        const int hh = i / (nrow * 8);
                         const int rem = i % (nrow * 8);
-                        st_shared_zero16(vb + h * L::kKVHalf + (r0 + rem / 8) * 128 + (rem % 8) * 16);
+                        const int key = r0 + rem / 8;
+                        st_shared_zero16(vb + (key / p.bs) * (p.bs * 128 * L::kChunks) +
+                                         hh * (p.bs * 128) + (key % p.bs) * 128 + (rem % 8) * 16);
                     }
                 }
                 fence_proxy_async();
@@ -867,7 +937,22 @@ int32_t make_maps(Maps* m, const void* q, const void* k_pool, const void* v_pool
     const int64_t rows = int64_t(s->num_blocks) * s->block_size;
     int32_t st;
     if ((st = make_map(&m->k, k_pool, D, s->num_kv_heads, rows, 1, s->block_size))) return st;
-    if ((st = make_map(&m->v, v_pool, D, s->num_kv_heads, rows, 1, s->block_size))) return st;
+    if (D == 128) {
+        // {64, rows, half, head}: one box holds both 64-column halves of one block, halves
+        // outermost, so that each half's rows are contiguous in shared memory
+        auto fn = encode_fn();
+        if (!fn) return PA_ERR_CUDA;
+        const cuuint64_t dims[4] = {64, cuuint64_t(rows), 2, cuuint64_t(s->num_kv_heads)};
+        const cuuint64_t strides[3] = {cuuint64_t(s->num_kv_heads) * D * 2, 128, cuuint64_t(D) * 2};
+        const cuuint32_t box[4] = {64, cuuint32_t(s->block_size), 2, 1};
+        const cuuint32_t estr[4] = {1, 1, 1, 1};
+        if (fn(&m->v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(v_pool), dims, strides,
+               box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return PA_ERR_CUDA;
+    } else if ((st = make_map(&m->v, v_pool, D, s->num_kv_heads, rows, 1, s->block_size))) {
+        return st;
+    }
     if ((st = make_map(&m->q1, q, D, s->num_q_heads, T, g, 1))) return st;
     return make_map(&m->qn, q, D, s->num_q_heads, T, g, kRows / g);
 }
@@ -934,6 +1019,8 @@ int32_t prepare_step(const void* q, const void* k_pool, const void* v_pool,
         return PA_ERR_INVALID;
     if ((st = make_maps(maps, q, k_pool, v_pool, T, shape))) return st;
     const int D = shape->head_dim;
+    prm->k_pool = static_cast<const __nv_bfloat16*>(k_pool);
+    prm->v_pool = static_cast<const __nv_bfloat16*>(v_pool);
     prm->block_table = block_table;
     prm->cu = cu_seqlens_q;
     prm->ctx = ctx_lens;
