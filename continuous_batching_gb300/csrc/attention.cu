@@ -15,7 +15,8 @@
 //   S  = Q K^T    tcgen05.mma kind::f16, M 128 x N 128 keys x K D, fp32 in TMEM
 //   softmax       fp32 online softmax over 128-key tiles aligned to absolute key positions;
 //                 a row is spread over 4 threads (tcgen05.ld 16x256b); fixed reduction order
-//   O += P V      tcgen05.mma, M 128 x N D x K 128 keys, P rounded to bf16 in shared memory
+//   O += P V      tcgen05.mma, M 128 x N D x K 128 keys, P rounded to bf16 and written back
+//                 into its tile's S buffer in TMEM (A operand from TMEM)
 // A tensor-core output element depends only on its own row of A and column of B, so a row's
 // bits do not depend on the other rows of the tile; the fixed splits
 // [s*1024, (s+1)*1024) and the ascending-order combine make them independent of the batch.
@@ -28,8 +29,8 @@
 // shared-memory slots across item boundaries; a K slot is free again as soon as S has read
 // it, a V slot once PV has. A paged tile is one box per block (K: one per 64-column half,
 // V: both halves in one box), issued from all 32 lanes of the loader warp. TMEM holds two S buffers (S of the
-// next tile is computed while the softmax works on the current one) and two O accumulators
-// (an item's epilogue overlaps the next item's MMAs). Every wait on an mbarrier is bounded.
+// next tile is computed while the softmax works on the current one; P overwrites the S it came
+// from) and two O accumulators (an item's epilogue overlaps the next item's MMAs). Every wait on an mbarrier is bounded.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
@@ -60,36 +61,44 @@ static_assert(kSplit % kTileKeys == 0, "splits are whole tiles");
 template <int D>
 struct Layout {
     static constexpr int kChunks = D / 64;                  // 128-byte column chunks of a row
-    static constexpr int kStages = D == 128 ? 2 : 4;        // K/V ring depth
+    static constexpr int kStagesK = D == 128 ? 2 : 4;       // K ring: a slot frees after S
+    static constexpr int kStagesV = D == 128 ? 3 : 6;       // V ring: a slot frees after PV
     static constexpr int kQHalf = kRows * 128;              // one 64-column chunk of a Q tile
     static constexpr int kQBuf = kChunks * kQHalf;
     static constexpr int kKVHalf = kTileKeys * 128;
     static constexpr int kKVTile = kChunks * kKVHalf;       // K (or V) of one key tile
     static constexpr int kQ = 0;                            // two Q buffers
-    static constexpr int kP = kQ + 2 * kQBuf;               // P: 128 rows x 128 keys, 2 chunks
-    static constexpr int kK = kP + 2 * kRows * 128;
-    static constexpr int kV = kK + kStages * kKVTile;
-    static constexpr int kBar = kV + kStages * kKVTile;     // barriers, item ring, tables
+    static constexpr int kK = kQ + 2 * kQBuf;
+    static constexpr int kV = kK + kStagesK * kKVTile;
+    static constexpr int kBar = kV + kStagesV * kKVTile;    // barriers, item ring, tables
     static constexpr int kBytes = kBar + 1792;
     static constexpr int kAlloc = kBytes + 1024;            // room to align the base to 1024
 };
 
-// mbarrier slots (8 bytes each) at Layout::kBar
+// mbarrier slots (8 bytes each) at Layout::kBar.
+// A waiter tests a phase by its parity, which is only sound while the barrier is within one
+// phase of the tested one: the previous phase must already be complete and the next one must
+// not be able to complete before the test. Barriers that a role waits on only sometimes (or
+// that another role can race ahead on) are therefore split by tile or item parity.
 enum Bar {
-    kKFull = 0,      // + stage (up to 4): TMA -> MMA (K of the tile landed)
-    kKEmpty = 4,     // + stage: MMA (after S) -> K loader
-    kVFull = 8,      // + stage: TMA -> MMA, softmax (V of the tile landed)
-    kVEmpty = 12,    // + stage: MMA (after PV) -> V loader
-    kQFull = 16,     // + buffer: TMA -> MMA
-    kQEmpty = 18,    // + buffer: MMA (after the item's last S) -> producer
-    kSFull = 20,     // + buffer: MMA -> softmax
-    kPFull = 22,     // softmax (128 arrivals) -> MMA: P stored, O rescaled, V tail zeroed
-    kPVDone = 23,    // MMA -> softmax: the previous PV has finished
-    kOFree = 24,     // + buffer: epilogue (128 arrivals) -> MMA
-    kDrain = 26,
-    kItemFull = 27,  // + slot (4): producer -> everyone: the slot holds the next item
-    kItemEmpty = 31, // + slot: consumers (MMA 2, softmax 128, loaders 64 arrivals) -> producer
-    kNumBars = 35
+    kKFull = 0,      // + slot (up to 4): TMA -> MMA (K of the tile landed)
+    kKEmpty = 4,     // + slot: MMA (after S) -> K loader
+    kVFull = 8,      // + slot (up to 6): TMA -> MMA, softmax (V of the tile landed)
+    kVEmpty = 14,    // + slot: MMA (after PV) -> V loader
+    kQFull = 20,     // + buffer: TMA -> MMA
+    kQEmpty = 22,    // + buffer: MMA (after the item's last S) -> producer
+    kSFull = 24,     // + S buffer: MMA -> softmax
+    kPFull = 26,     // + S buffer: softmax (128 arrivals) -> MMA: P stored, O rescaled,
+                     //   V tail zeroed (the softmax may finish tile t before the MMA has
+                     //   seen tile t-1)
+    kPVDone = 28,    // + S buffer: MMA -> softmax: the PV of a tile of that parity finished
+                     //   (the softmax waits only when it rescales O, and at the epilogue)
+    kOFree = 30,     // + buffer: epilogue (128 arrivals) -> MMA
+    kDrain = 32,
+    kItemFull = 33,  // + slot (4): producer -> everyone: the slot holds the next item
+    kItemEmpty = 37, // + slot: consumers (MMA 2, softmax 128, loaders 64 arrivals) -> producer
+    kPFree = 41,     // + S buffer: MMA (after PV) -> MMA: the P in that buffer has been read
+    kNumBars = 43
 };
 constexpr int kHolderOff = 8 * kNumBars;          // TMEM address written by tcgen05.alloc
 constexpr int kAbortOff = kHolderOff + 4;
@@ -228,6 +237,16 @@ __device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a_desc, uint
         : "memory");
 }
 
+// D[tmem] (+)= A[tmem] * B[smem]^T, kind::f16; A is 128 lanes (rows) x packed bf16 pairs.
+__device__ __forceinline__ void umma_bf16_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                                 uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
 // Instruction descriptor, kind::f16: fp32 accumulator (bits 4-5 = 1), A and B bf16 (bits 7-9,
 // 10-12 = 1), A K-major, B K-major or MN-major (bit 16), N >> 3 at bits 17-22, M >> 4 at
 // bits 24-28.
@@ -340,7 +359,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                       const __grid_constant__ CUtensorMap tm_q1,
                       const __grid_constant__ CUtensorMap tm_qn, const Params p) {
     using L = Layout<D>;
-    constexpr int S = L::kStages;
+    constexpr int SK = L::kStagesK;
+    constexpr int SV = L::kStagesV;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~uintptr_t(1023));
@@ -354,7 +374,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (threadIdx.x == 0) {
         for (int b = 0; b < kNumBars; ++b)
             mbar_init(bars + 8 * b,
-                      (b == kPFull || b == kOFree || b == kOFree + 1) ? 128
+                      (b == kPFull || b == kPFull + 1 || b == kOFree || b == kOFree + 1) ? 128
                       : (b >= kItemEmpty && b < kItemEmpty + 4)       ? 2 + 128 + 64
                                                                       : 1);
         *abort_word = 0;
@@ -447,7 +467,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             constexpr uint32_t idesc_o = make_idesc(kRows, D, true);
             const auto issue_s = [&](int qb, int st, uint32_t d) {
                 const uint32_t qbase = sb + L::kQ + qb * L::kQBuf;
-                const uint32_t kbase = sb + L::kK + st * L::kKVTile;
+                const uint32_t kbase = sb + L::kK + st * L::kKVTile;   // K ring slot
 #pragma unroll
                 for (int k = 0; k < D / 16; ++k) {
                     const uint32_t qa = qbase + (k >> 2) * L::kQHalf + (k & 3) * 32;
@@ -460,16 +480,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             // bs * 128 bytes apart (MN-major B operand: LBO = half stride, SBO = 8-key stride)
             const uint32_t v_lbo = uint32_t(p.bs) * 128;
             const uint32_t v_sbo = p.bs >= 16 ? 1024u : uint32_t(p.bs) * 128 * L::kChunks;
-            const auto issue_pv = [&](int st, uint32_t d, bool acc) {
-                const uint32_t vbase = sb + L::kV + st * L::kKVTile;
+            const auto issue_pv = [&](int st, uint32_t p_tmem, uint32_t d, bool acc) {
+                const uint32_t vbase = sb + L::kV + st * L::kKVTile;   // V ring slot
 #pragma unroll
                 for (int k = 0; k < kTileKeys / 16; ++k) {
-                    const uint32_t pa = sb + L::kP + (k >> 2) * (kRows * 128) + (k & 3) * 32;
                     const int key = 16 * k;                  // first key of this 16-key step
                     const uint32_t va = vbase + (key / p.bs) * (p.bs * 128 * L::kChunks) +
                                         (key % p.bs) * 128;
-                    umma_bf16(d, make_sdesc(pa, 16, 1024), make_sdesc(va, v_lbo, v_sbo),
-                              idesc_o, (acc || k > 0) ? 1u : 0u);
+                    // P of keys 16k .. 16k+15 is 8 packed columns of the S buffer
+                    umma_bf16_tmem_a(d, p_tmem + 8 * k, make_sdesc(va, v_lbo, v_sbo), idesc_o,
+                                     (acc || k > 0) ? 1u : 0u);
                 }
             };
             // Two cursors walk the same item sequence: one issues S = Q K^T for the next tile
@@ -509,26 +529,30 @@ __global__ void __launch_bounds__(kThreads, 1)
                 fetch(cv);
                 fetch(cs);
                 // O += P V for the oldest tile whose P is ready
-                if (cv.have && cv.tc < cs.tc && mbar_test_wait(bar(kPFull), cv.tc & 1) &&
-                    mbar_test_wait(bar(kVFull + cv.tc % S), (cv.tc / S) & 1) &&
+                if (cv.have && cv.tc < cs.tc &&
+                    mbar_test_wait(bar(kPFull + (cv.tc & 1)), (cv.tc >> 1) & 1) &&
+                    mbar_test_wait(bar(kVFull + cv.tc % SV), (cv.tc / SV) & 1) &&
                     (cv.jt > 0 || cv.ic < 2 ||
                      mbar_test_wait(bar(kOFree + (cv.ic & 1)), ((cv.ic >> 1) - 1) & 1))) {
                     tc_fence_after();
-                    const int st = cv.tc % S;
-                    issue_pv(st, tmem + kTmemO + (cv.ic & 1) * 128, cv.jt > 0);
+                    const int st = cv.tc % SV;
+                    issue_pv(st, tmem + (cv.tc & 1) * 128, tmem + kTmemO + (cv.ic & 1) * 128,
+                             cv.jt > 0);
+                    tc_commit(bar(kPFree + (cv.tc & 1)));
                     tc_commit(bar(kVEmpty + st));
-                    tc_commit(bar(kPVDone));
+                    tc_commit(bar(kPVDone + (cv.tc & 1)));
                     advance(cv);
                     progress = true;
                 }
-                // S = Q K^T for the next tile: its S buffer was last read by the softmax of
-                // tile cs.tc - 2, whose P the PV cursor has already consumed
+                // S = Q K^T for the next tile: its S buffer last held the P of tile cs.tc - 2,
+                // which must have been read by that tile's PV (finished, not just issued)
                 if (cs.have && cs.tc <= cv.tc + 1 &&
+                    (cs.tc < 2 || mbar_test_wait(bar(kPFree + (cs.tc & 1)), ((cs.tc >> 1) - 1) & 1)) &&
                     (cs.jt > 0 || mbar_test_wait(bar(kQFull + (cs.ic & 1)), (cs.ic >> 1) & 1)) &&
-                    mbar_test_wait(bar(kKFull + cs.tc % S), (cs.tc / S) & 1)) {
+                    mbar_test_wait(bar(kKFull + cs.tc % SK), (cs.tc / SK) & 1)) {
                     tc_fence_after();
-                    issue_s(cs.ic & 1, cs.tc % S, tmem + (cs.tc & 1) * 128);
-                    tc_commit(bar(kKEmpty + cs.tc % S));
+                    issue_s(cs.ic & 1, cs.tc % SK, tmem + (cs.tc & 1) * 128);
+                    tc_commit(bar(kKEmpty + cs.tc % SK));
                     tc_commit(bar(kSFull + (cs.tc & 1)));
                     if (cs.jt == cs.I.n_tiles - 1) tc_commit(bar(kQEmpty + (cs.ic & 1)));
                     advance(cs);
@@ -565,6 +589,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int boxes_per_block = is_v ? 1 : L::kChunks;
         const int full_b = is_v ? kVFull : kKFull;
         const int empty_b = is_v ? kVEmpty : kKEmpty;
+        const int S = is_v ? SV : SK;                    // slots in this tensor's ring
         const uint32_t slots = sb + (is_v ? L::kV : L::kK);
         int tc = 0, ic = 0;
         int ok = 1;
@@ -634,8 +659,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else {
         // ------------------------------------------------------------ softmax warps 0-3
         const int tid = threadIdx.x;              // 0..127
-        for (int i = tid; i < 2 * kRows * 8; i += 128) st_shared_zero16(sb + L::kP + i * 16);
-        fence_proxy_async();
         const int q4 = lane & 3;
         const int rs = lane >> 2;
         const float c = p.c;
@@ -670,14 +693,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                     break;
                 tc_fence_after();
                 const int kb = I.k_begin + jt * kTileKeys;
+                const uint32_t tm_s = tmem + (tc & 1) * 128;
                 float alpha[2][2];
-                uint32_t pk[2][2][16];               // P rounded to bf16, packed in pairs
 #pragma unroll
                 for (int hb = 0; hb < 2; ++hb) {
                     if (!half_on[hb]) continue;
+                    const uint32_t lanes = uint32_t(32 * warp + 16 * hb) << 16;
                     uint32_t r[64];
-                    tmem_ld_16x256b_x16(tmem + (tc & 1) * 128 + (uint32_t(32 * warp + 16 * hb) << 16), r);
+                    tmem_ld_16x256b_x16(tm_s + lanes, r);
                     tmem_wait_ld();
+                    uint32_t pk[32];                 // P rounded to bf16, packed in pairs
 #pragma unroll
                     for (int sr = 0; sr < 2; ++sr) {
                         const int pr = pos[hb][sr];
@@ -688,10 +713,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                             for (int e = 0; e < 2; ++e) {
                                 const int key = kb + 8 * cc + 2 * q4 + e;
-                                const float s = key <= pr ? __uint_as_float(r[4 * cc + 2 * sr + e])
-                                                          : -INFINITY;
-                                sv[2 * cc + e] = s;
-                                mx = fmaxf(mx, s);
+                                const float sc = key <= pr ? __uint_as_float(r[4 * cc + 2 * sr + e])
+                                                           : -INFINITY;
+                                sv[2 * cc + e] = sc;
+                                mx = fmaxf(mx, sc);
                             }
                         mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
                         mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
@@ -712,54 +737,56 @@ __global__ void __launch_bounds__(kThreads, 1)
                         l_run[hb][sr] = __fadd_rn(__fmul_rn(l_run[hb][sr], a), sum);
                         m_run[hb][sr] = m_new;
                         alpha[hb][sr] = a;
+                        // keys 8cc + 2q4 + {0, 1} -> packed column 4cc + q4 (16x128b layout)
 #pragma unroll
                         for (int cc = 0; cc < 16; ++cc)
-                            pk[hb][sr][cc] = pack_bf16(sv[2 * cc], sv[2 * cc + 1]);
+                            pk[2 * cc + sr] = pack_bf16(sv[2 * cc], sv[2 * cc + 1]);
                     }
+                    // P replaces S in the first 64 columns of this tile's S buffer
+                    tmem_st_16x128b_x16(tm_s + lanes, pk);
                 }
-                // P and O belong to the previous tile's PV until it has finished
-                if (tc > 0 && !(ok = wait_bounded(bar(kPVDone), (tc - 1) & 1, abort_word))) break;
-                tc_fence_after();
+                // O belongs to the previous tile's PV until it has finished: rescale only then,
+                // and only in warps where some row's running maximum moved
+                bool need = false;
 #pragma unroll
-                for (int hb = 0; hb < 2; ++hb) {
-                    if (!half_on[hb]) continue;
+                for (int hb = 0; hb < 2; ++hb)
+                    if (half_on[hb]) need |= alpha[hb][0] != 1.f || alpha[hb][1] != 1.f;
+                if (jt > 0 && __any_sync(0xffffffffu, need)) {
+                    if (!(ok = wait_bounded(bar(kPVDone + ((tc - 1) & 1)), ((tc - 1) >> 1) & 1,
+                                            abort_word)))
+                        break;
+                    tc_fence_after();
 #pragma unroll
-                    for (int sr = 0; sr < 2; ++sr) {
-                        const int row = 32 * warp + 16 * hb + rs + 8 * sr;
+                    for (int hb = 0; hb < 2; ++hb) {
+                        if (!half_on[hb]) continue;
+                        const uint32_t ta = tm_o + (uint32_t(32 * warp + 16 * hb) << 16);
+                        uint32_t o[D / 2];
+                        if constexpr (D == 128) tmem_ld_16x256b_x16(ta, o);
+                        else tmem_ld_16x256b_x8(ta, o);
+                        tmem_wait_ld();
 #pragma unroll
-                        for (int cc = 0; cc < 16; ++cc)
-                            st_shared_u32(sb + L::kP + (cc >> 3) * (kRows * 128) +
-                                              swz(row, cc & 7) + 4 * q4,
-                                          pk[hb][sr][cc]);
+                        for (int cc = 0; cc < D / 8; ++cc)
+#pragma unroll
+                            for (int sr = 0; sr < 2; ++sr)
+#pragma unroll
+                                for (int e = 0; e < 2; ++e) {
+                                    const int k = 4 * cc + 2 * sr + e;
+                                    o[k] = __float_as_uint(
+                                        __fmul_rn(__uint_as_float(o[k]), alpha[hb][sr]));
+                                }
+                        if constexpr (D == 128) tmem_st_16x256b_x16(ta, o);
+                        else tmem_st_16x256b_x8(ta, o);
                     }
-                    if (jt == 0) continue;
-                    const bool need = alpha[hb][0] != 1.f || alpha[hb][1] != 1.f;
-                    if (!__any_sync(0xffffffffu, need)) continue;
-                    const uint32_t ta = tm_o + (uint32_t(32 * warp + 16 * hb) << 16);
-                    uint32_t o[D / 2];
-                    if constexpr (D == 128) tmem_ld_16x256b_x16(ta, o);
-                    else tmem_ld_16x256b_x8(ta, o);
-                    tmem_wait_ld();
-#pragma unroll
-                    for (int cc = 0; cc < D / 8; ++cc)
-#pragma unroll
-                        for (int sr = 0; sr < 2; ++sr)
-#pragma unroll
-                            for (int e = 0; e < 2; ++e) {
-                                const int k = 4 * cc + 2 * sr + e;
-                                o[k] = __float_as_uint(__fmul_rn(__uint_as_float(o[k]), alpha[hb][sr]));
-                            }
-                    if constexpr (D == 128) tmem_st_16x256b_x16(ta, o);
-                    else tmem_st_16x256b_x8(ta, o);
                 }
                 tmem_wait_st();
                 // keys at or beyond ctx are stale or were never loaded: give them zero values
                 // so that their (zero) probabilities contribute exact zeros
                 if (kb + kTileKeys > I.ctx) {
-                    if (!(ok = wait_bounded(bar(kVFull + tc % S), (tc / S) & 1, abort_word))) break;
+                    if (!(ok = wait_bounded(bar(kVFull + tc % SV), (tc / SV) & 1, abort_word)))
+                        break;
                     const int r0 = max(I.ctx - kb, 0);
                     const int nrow = kTileKeys - r0;
-                    const uint32_t vb = sb + L::kV + (tc % S) * L::kKVTile;
+                    const uint32_t vb = sb + L::kV + (tc % SV) * L::kKVTile;
                     for (int i = tid; i < nrow * 8 * L::kChunks; i += 128) {
                         const int hh = i / (nrow * 8);
                         const int rem = i % (nrow * 8);
@@ -770,11 +797,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 fence_proxy_async();
                 tc_fence_before();
-                mbar_arrive(bar(kPFull));            // all 128 softmax threads arrive
+                mbar_arrive(bar(kPFull + (tc & 1)));            // all 128 softmax threads arrive
             }
             if (!ok) break;
             // ---------------------------------------------------------------- epilogue
-            if (!(ok = wait_bounded(bar(kPVDone), (tc - 1) & 1, abort_word))) break;
+            if (!(ok = wait_bounded(bar(kPVDone + ((tc - 1) & 1)), ((tc - 1) >> 1) & 1, abort_word)))
+                break;
             tc_fence_after();
 #pragma unroll
             for (int hb = 0; hb < 2; ++hb) {
