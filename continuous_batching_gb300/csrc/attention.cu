@@ -705,19 +705,41 @@ __global__ void __launch_bounds__(kThreads, 1)
                     uint32_t pk[32];                 // P rounded to bf16, packed in pairs
 #pragma unroll
                     for (int sr = 0; sr < 2; ++sr) {
+                        // an 8-row block with no valid row (the tail of a decode or a ragged
+                        // tile) needs no softmax: its P is never used for a written output
+                        if (32 * warp + 16 * hb + 8 * sr >= I.rows_valid) {
+                            alpha[hb][sr] = 1.f;
+#pragma unroll
+                            for (int cc = 0; cc < 16; ++cc) pk[2 * cc + sr] = 0u;
+                            continue;
+                        }
                         const int pr = pos[hb][sr];
+                        // the causal / ctx mask matters only when some key of the tile lies past
+                        // some row of this block
+                        const bool full = __all_sync(0xffffffffu, kb + kTileKeys - 1 <= pr);
                         float sv[32];
                         float mx = -INFINITY;
+                        if (full) {
 #pragma unroll
-                        for (int cc = 0; cc < 16; ++cc)
+                            for (int cc = 0; cc < 16; ++cc)
 #pragma unroll
-                            for (int e = 0; e < 2; ++e) {
-                                const int key = kb + 8 * cc + 2 * q4 + e;
-                                const float sc = key <= pr ? __uint_as_float(r[4 * cc + 2 * sr + e])
-                                                           : -INFINITY;
-                                sv[2 * cc + e] = sc;
-                                mx = fmaxf(mx, sc);
-                            }
+                                for (int e = 0; e < 2; ++e) {
+                                    const float sc = __uint_as_float(r[4 * cc + 2 * sr + e]);
+                                    sv[2 * cc + e] = sc;
+                                    mx = fmaxf(mx, sc);
+                                }
+                        } else {
+#pragma unroll
+                            for (int cc = 0; cc < 16; ++cc)
+#pragma unroll
+                                for (int e = 0; e < 2; ++e) {
+                                    const int key = kb + 8 * cc + 2 * q4 + e;
+                                    const float sc = key <= pr ? __uint_as_float(r[4 * cc + 2 * sr + e])
+                                                               : -INFINITY;
+                                    sv[2 * cc + e] = sc;
+                                    mx = fmaxf(mx, sc);
+                                }
+                        }
                         mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
                         mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
                         const float m_new = fmaxf(m_run[hb][sr], mx);
@@ -822,12 +844,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const int tok = I.q_start + row / p.g;
                     const int head = I.kvh * p.g + row % p.g;
                     if (nsp == 1) {
-                        const float lsum = l_run[hb][sr];
+                        const float inv = __frcp_rn(l_run[hb][sr]);
                         __nv_bfloat16* dst = p.out + (int64_t(tok) * p.Hq + head) * D;
 #pragma unroll
                         for (int cc = 0; cc < D / 8; ++cc) {
-                            const float x0 = __fdiv_rn(__uint_as_float(o[4 * cc + 2 * sr]), lsum);
-                            const float x1 = __fdiv_rn(__uint_as_float(o[4 * cc + 2 * sr + 1]), lsum);
+                            const float x0 = __fmul_rn(__uint_as_float(o[4 * cc + 2 * sr]), inv);
+                            const float x1 = __fmul_rn(__uint_as_float(o[4 * cc + 2 * sr + 1]), inv);
                             *reinterpret_cast<uint32_t*>(dst + 8 * cc + 2 * q4) = pack_bf16(x0, x1);
                         }
                     } else {
@@ -865,8 +887,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 // For every (row, q head) whose row spans more than one split: fold the partials of splits
 // 0, 1, ... in ascending order, starting from split 0's (m, l, acc) as they are:
 //   M' = max(M, m_s), a = 2^((M - M') c), b = 2^((m_s - M') c),
-//   L = L a + l_s b, ACC = ACC a + acc_s b;  out = bf16_rne(ACC / L).
-// A row with one split is finished by the attention kernel with the same division.
+//   L = L a + l_s b, ACC = ACC a + acc_s b;  out = bf16_rne(ACC * rcp_rn(L)).
+// A row with one split is finished by the attention kernel with the same two roundings.
 template <int D>
 __global__ void __launch_bounds__(128)
     combine_kernel(const float* __restrict__ ws_acc, const float* __restrict__ ws_ml,
@@ -914,10 +936,11 @@ __global__ void __launch_bounds__(128)
         M = mn;
     }
     __nv_bfloat16* dst = out + (tok * Hq + head) * D + lane * E;
+    const float inv = __frcp_rn(Lsum);
 #pragma unroll
     for (int e = 0; e < E; e += 2)
         *reinterpret_cast<uint32_t*>(dst + e) =
-            pack_bf16(__fdiv_rn(acc[e], Lsum), __fdiv_rn(acc[e + 1], Lsum));
+            pack_bf16(__fmul_rn(acc[e], inv), __fmul_rn(acc[e + 1], inv));
 }
 
 // ------------------------------------------------------------------------- host side
