@@ -13,8 +13,10 @@
 // by the g query heads of a group. A decode item simply has one token (g valid rows). Every
 // row runs the same instruction sequence whatever the item holds:
 //   S  = Q K^T    tcgen05.mma kind::f16, M 128 x N 128 keys x K D, fp32 in TMEM
-//   softmax       fp32 online softmax over 128-key tiles aligned to absolute key positions;
-//                 a row is spread over 4 threads (tcgen05.ld 16x256b); fixed reduction order
+//   softmax       fp32 online softmax over 128-key tiles aligned to absolute key positions,
+//                 with a reference maximum that moves only when the row maximum outgrows it
+//                 by 2^8; a row is spread over 4 threads (tcgen05.ld 16x256b); fixed
+//                 reduction order
 //   O += P V      tcgen05.mma, M 128 x N D x K 128 keys, P rounded to bf16 and written back
 //                 into its tile's S buffer in TMEM (A operand from TMEM)
 // A tensor-core output element depends only on its own row of A and column of B, so a row's
@@ -57,6 +59,8 @@ constexpr uint32_t kTmemO = 256;
 constexpr unsigned long long kWaitLimitNs = 1000000000ull;   // one second per wait
 
 static_assert(kSplit % kTileKeys == 0, "splits are whole tiles");
+// Growth of a row's maximum (log2 units) tolerated before its softmax reference moves.
+constexpr float kLazyLog2 = 8.f;
 
 template <int D>
 struct Layout {
@@ -742,11 +746,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                         mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
                         mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-                        const float m_new = fmaxf(m_run[hb][sr], mx);
-                        const float m_use = m_new == -INFINITY ? 0.f : m_new;
-                        const float a = m_run[hb][sr] == m_use
+                        // The reference maximum moves only when the row's maximum grows past it by
+                        // more than 8 in base-2 units, so P <= 2^8 and O needs rescaling rarely;
+                        // the decision depends on the row's own scores alone.
+                        const float m_old = m_run[hb][sr];
+                        const float m_new = fmaxf(m_old, mx);
+                        const bool move = m_old == -INFINITY
+                                              ? m_new != -INFINITY
+                                              : __fmul_rn(__fsub_rn(m_new, m_old), c) > kLazyLog2;
+                        const float m_ref = move ? m_new : m_old;
+                        const float m_use = m_ref == -INFINITY ? 0.f : m_ref;
+                        const float a = m_old == m_use
                                             ? 1.f
-                                            : ex2(__fmul_rn(__fsub_rn(m_run[hb][sr], m_use), c));
+                                            : ex2(__fmul_rn(__fsub_rn(m_old, m_use), c));
                         const float nmc = __fmul_rn(-m_use, c);
                         float sum = 0.f;
 #pragma unroll
@@ -757,7 +769,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         sum = __fadd_rn(sum, __shfl_xor_sync(0xffffffffu, sum, 1));
                         sum = __fadd_rn(sum, __shfl_xor_sync(0xffffffffu, sum, 2));
                         l_run[hb][sr] = __fadd_rn(__fmul_rn(l_run[hb][sr], a), sum);
-                        m_run[hb][sr] = m_new;
+                        m_run[hb][sr] = m_ref;
                         alpha[hb][sr] = a;
                         // keys 8cc + 2q4 + {0, 1} -> packed column 4cc + q4 (16x128b layout)
 #pragma unroll
