@@ -214,6 +214,25 @@ def time_steps(g: GpuStep, torch, steps: int, warmup: int, flush, attn_only=Fals
     return step_ms, attn_ms
 
 
+def rank_seed(name: str, rank: int) -> int:
+    """Each rank of a multi-GPU run draws its own batch of the same workload."""
+    base = {"decode": 1, "mixed": 2}[name]
+    return base + rank
+
+
+def combine_ranks(total_ms: float, units: float, dist=None, device="cpu"):
+    """Whole-job timing over ranks: (max of the ranks' timed totals, sum of their work units).
+    Ranks share nothing on the data path; this is the only cross-rank step."""
+    if dist is None or not dist.is_initialized() or dist.get_world_size() == 1:
+        return total_ms, units
+    import torch
+    t = torch.tensor([total_ms], dtype=torch.float64, device=device)
+    u = torch.tensor([units], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dist.all_reduce(u, op=dist.ReduceOp.SUM)
+    return float(t.item()), float(u.item())
+
+
 def load_for(g: GpuStep, torch, seconds: float) -> None:
     t = time.perf_counter()
     while time.perf_counter() - t < seconds:
@@ -236,7 +255,7 @@ def run_ours(args) -> dict:
     bd.load()
     peaks = load_peaks()
 
-    st = wl.make_config("decode", seed=1 + rank)
+    st = wl.make_config("decode", seed=rank_seed("decode", rank))
     g = GpuStep(st, torch, bd)
     flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
 
@@ -259,15 +278,13 @@ def run_ours(args) -> dict:
         wall = time.perf_counter() - t0
         if not args.no_clocks:
             load_for(g, torch, 1.0)
-    total_ms = sum(step_ms)
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([total_ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
-    ms_per_step = total_ms / args.steps
     bytes_step = kv_bytes(st)
-    value = bytes_step * world / (ms_per_step * 1e-3) / 1e9
+    dist_mod = None
+    if world > 1:
+        import torch.distributed as dist_mod
+    total_ms, all_bytes = combine_ranks(sum(step_ms), float(bytes_step), dist_mod, "cuda")
+    ms_per_step = total_ms / args.steps
+    value = all_bytes / (ms_per_step * 1e-3) / 1e9
 
     # end to end through the public API with host buffers
     for _ in range(2):
@@ -290,7 +307,7 @@ def run_ours(args) -> dict:
     # the mixed ragged step (tokens/s) alongside
     mixed = None
     if not args.no_mixed:
-        sm = wl.make_config("mixed", seed=2 + rank)
+        sm = wl.make_config("mixed", seed=rank_seed("mixed", rank))
         gm = GpuStep(sm, torch, bd)
         m_step, m_attn = time_steps(gm, torch, args.steps, args.warmup, flush)
         mm = statistics.mean(m_step)

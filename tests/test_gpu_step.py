@@ -44,7 +44,8 @@ MID_NQ = [1, 1, 1, 1, 1, 1, 1, 1, 1, 1, 200, 77, 33, 5, 129]
 
 
 @pytest.mark.parametrize("Hq,Hkv,D,bs", [(32, 8, 128, 16), (8, 8, 128, 32), (16, 2, 64, 8),
-                                         (64, 8, 128, 64), (16, 1, 128, 128), (4, 2, 64, 16)])
+                                         (64, 8, 128, 64), (16, 1, 128, 128), (4, 2, 64, 16),
+                                         (32, 8, 128, 8), (64, 4, 128, 16), (32, 2, 64, 128)])
 def test_mixed_step_all_rows(Hq, Hkv, D, bs):
     st = wl.make_step(Hq, Hkv, D, bs, MID_CTX, MID_NQ, seed=Hq * 7 + D + bs)
     out, kp, vp, err = run_step(st, torch)
