@@ -24,10 +24,11 @@
 // [s*1024, (s+1)*1024) and the ascending-order combine make them independent of the batch.
 //
 // Persistent schedule: one CTA per SM walks the items blockIdx.x, blockIdx.x + gridDim.x, ...
-// (the host orders items longest first). Warp roles (256 threads): warps 0-3 softmax /
-// rescale / epilogue, warp 4 producer (reads the work items, publishes them in a ring, loads
-// each item's Q tile by TMA into one of two Q buffers), warp 5 MMA issuer and TMEM owner,
-// warp 6 K loader, warp 7 V loader. The loaders stream tiles by TMA through rings of
+// (the host orders items longest first). Warp roles (384 threads): warps 0-7 softmax /
+// rescale / epilogue (two warps per TMEM sub-partition, one per 16-lane half), warp 8
+// producer (reads the work items, publishes them in a ring, loads each item's Q tile by TMA
+// into one of two Q buffers), warp 9 MMA issuer and TMEM owner, warp 10 K loader, warp 11 V
+// loader. The loaders stream tiles by TMA through rings of
 // shared-memory slots across item boundaries; a K slot is free again as soon as S has read
 // it, a V slot once PV has. A paged tile is one box per block (K: one per 64-column half,
 // V: both halves in one box), issued from all 32 lanes of the loader warp. TMEM holds two S buffers (S of the
@@ -53,7 +54,7 @@ namespace {
 constexpr int kRows = PA_ROWS;
 constexpr int kTileKeys = PA_TILE_KEYS;
 constexpr int kSplit = PA_SPLIT_TOKENS;
-constexpr int kThreads = 256;
+constexpr int kThreads = 384;
 constexpr uint32_t kTmemCols = 512;     // S0 [0,128) S1 [128,256) O0 [256,384) O1 [384,512)
 constexpr uint32_t kTmemO = 256;
 constexpr unsigned long long kWaitLimitNs = 1000000000ull;   // one second per wait
@@ -92,15 +93,15 @@ enum Bar {
     kQFull = 20,     // + buffer: TMA -> MMA
     kQEmpty = 22,    // + buffer: MMA (after the item's last S) -> producer
     kSFull = 24,     // + S buffer: MMA -> softmax
-    kPFull = 26,     // + S buffer: softmax (128 arrivals) -> MMA: P stored, O rescaled,
+    kPFull = 26,     // + S buffer: softmax (256 arrivals) -> MMA: P stored, O rescaled,
                      //   V tail zeroed (the softmax may finish tile t before the MMA has
                      //   seen tile t-1)
     kPVDone = 28,    // + S buffer: MMA -> softmax: the PV of a tile of that parity finished
                      //   (the softmax waits only when it rescales O, and at the epilogue)
-    kOFree = 30,     // + buffer: epilogue (128 arrivals) -> MMA
+    kOFree = 30,     // + buffer: epilogue (256 arrivals) -> MMA
     kDrain = 32,
     kItemFull = 33,  // + slot (4): producer -> everyone: the slot holds the next item
-    kItemEmpty = 37, // + slot: consumers (MMA 2, softmax 128, loaders 64 arrivals) -> producer
+    kItemEmpty = 37, // + slot: consumers (MMA 2, softmax 256, loaders 64 arrivals) -> producer
     kPFree = 41,     // + S buffer: MMA (after PV) -> MMA: the P in that buffer has been read
     kNumBars = 43
 };
@@ -378,13 +379,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (threadIdx.x == 0) {
         for (int b = 0; b < kNumBars; ++b)
             mbar_init(bars + 8 * b,
-                      (b == kPFull || b == kPFull + 1 || b == kOFree || b == kOFree + 1) ? 128
-                      : (b >= kItemEmpty && b < kItemEmpty + 4)       ? 2 + 128 + 64
+                      (b == kPFull || b == kPFull + 1 || b == kOFree || b == kOFree + 1) ? 256
+                      : (b >= kItemEmpty && b < kItemEmpty + 4)       ? 2 + 256 + 64
                                                                       : 1);
         *abort_word = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
-    if (warp == 5) {
+    if (warp == 9) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                          bars + kHolderOff),
                      "r"(kTmemCols)
@@ -396,7 +397,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + L::kBar + kHolderOff);
 
-    if (warp == 4) {
+    if (warp == 8) {
         // ------------------------------------------------------------ producer
         // Reads the work items from global memory, publishes each one in a slot of the item
         // ring for the other roles, and loads its Q tile by TMA.
@@ -464,7 +465,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int i = max(0, ic - 2); i < ic; ++i)
                 wait_bounded(bar(kQFull + (i & 1)), (i >> 1) & 1, abort_word);
         }
-    } else if (warp == 5) {
+    } else if (warp == 9) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
             constexpr uint32_t idesc_s = make_idesc(kRows, kTileKeys, false);
@@ -578,11 +579,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_commit(bar(kDrain));
             wait_bounded(bar(kDrain), 0, abort_word);
         }
-    } else if (warp >= 6) {
+    } else if (warp >= 10) {
         // ------------------------------------------------------------ K (warp 6) / V (warp 7)
-        const bool is_v = warp == 7;
+        const bool is_v = warp == 11;
         int32_t* tbl = reinterpret_cast<int32_t*>(smem + L::kBar + kTableOff) +
-                       (warp - 6) * kMaxTableEntries;
+                       (warp - 10) * kMaxTableEntries;
         const volatile ItemSlot* ring =
             reinterpret_cast<const volatile ItemSlot*>(smem + L::kBar + kRingOff);
         const CUtensorMap* tmap = is_v ? &tm_v : &tm_k;
@@ -661,8 +662,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 wait_bounded(bar(full_b + t % S), (t / S) & 1, abort_word);
         }
     } else {
-        // ------------------------------------------------------------ softmax warps 0-3
-        const int tid = threadIdx.x;              // 0..127
+        // ------------------------------------------------------------ softmax warps 0-7
+        // Warps w and w + 4 share TMEM sub-partition w % 4 (lanes 32 (w % 4) .. + 31): warp w
+        // takes the first 16 lanes, warp w + 4 the second 16.
+        const int tid = threadIdx.x;              // 0..255
+        const int sp = warp & 3;                  // TMEM sub-partition
+        const int my_hb = warp >> 2;              // which 16-lane half of it
         const int q4 = lane & 3;
         const int rs = lane >> 2;
         const float c = p.c;
@@ -683,10 +688,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             float m_run[2][2], l_run[2][2];
 #pragma unroll
             for (int hb = 0; hb < 2; ++hb) {
-                half_on[hb] = (32 * warp + 16 * hb) < I.rows_valid;
+                half_on[hb] = hb == my_hb && (32 * sp + 16 * hb) < I.rows_valid;
 #pragma unroll
                 for (int sr = 0; sr < 2; ++sr) {
-                    const int row = 32 * warp + 16 * hb + rs + 8 * sr;
+                    const int row = 32 * sp + 16 * hb + rs + 8 * sr;
                     pos[hb][sr] = row < I.rows_valid ? I.pos0 + row / p.g : -1;
                     m_run[hb][sr] = -INFINITY;
                     l_run[hb][sr] = 0.f;
@@ -702,7 +707,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int hb = 0; hb < 2; ++hb) {
                     if (!half_on[hb]) continue;
-                    const uint32_t lanes = uint32_t(32 * warp + 16 * hb) << 16;
+                    const uint32_t lanes = uint32_t(32 * sp + 16 * hb) << 16;
                     uint32_t r[64];
                     tmem_ld_16x256b_x16(tm_s + lanes, r);
                     tmem_wait_ld();
@@ -711,7 +716,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int sr = 0; sr < 2; ++sr) {
                         // an 8-row block with no valid row (the tail of a decode or a ragged
                         // tile) needs no softmax: its P is never used for a written output
-                        if (32 * warp + 16 * hb + 8 * sr >= I.rows_valid) {
+                        if (32 * sp + 16 * hb + 8 * sr >= I.rows_valid) {
                             alpha[hb][sr] = 1.f;
 #pragma unroll
                             for (int cc = 0; cc < 16; ++cc) pk[2 * cc + sr] = 0u;
@@ -793,7 +798,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int hb = 0; hb < 2; ++hb) {
                         if (!half_on[hb]) continue;
-                        const uint32_t ta = tm_o + (uint32_t(32 * warp + 16 * hb) << 16);
+                        const uint32_t ta = tm_o + (uint32_t(32 * sp + 16 * hb) << 16);
                         uint32_t o[D / 2];
                         if constexpr (D == 128) tmem_ld_16x256b_x16(ta, o);
                         else tmem_ld_16x256b_x8(ta, o);
@@ -821,7 +826,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const int r0 = max(I.ctx - kb, 0);
                     const int nrow = kTileKeys - r0;
                     const uint32_t vb = sb + L::kV + (tc % SV) * L::kKVTile;
-                    for (int i = tid; i < nrow * 8 * L::kChunks; i += 128) {
+                    for (int i = tid; i < nrow * 8 * L::kChunks; i += 256) {
                         const int hh = i / (nrow * 8);
                         const int rem = i % (nrow * 8);
                         const int key = r0 + rem / 8;
@@ -831,7 +836,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 fence_proxy_async();
                 tc_fence_before();
-                mbar_arrive(bar(kPFull + (tc & 1)));            // all 128 softmax threads arrive
+                mbar_arrive(bar(kPFull + (tc & 1)));            // all 256 softmax threads arrive
             }
             if (!ok) break;
             // ---------------------------------------------------------------- epilogue
@@ -841,14 +846,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int hb = 0; hb < 2; ++hb) {
                 if (!half_on[hb]) continue;
-                const uint32_t ta = tm_o + (uint32_t(32 * warp + 16 * hb) << 16);
+                const uint32_t ta = tm_o + (uint32_t(32 * sp + 16 * hb) << 16);
                 uint32_t o[D / 2];
                 if constexpr (D == 128) tmem_ld_16x256b_x16(ta, o);
                 else tmem_ld_16x256b_x8(ta, o);
                 tmem_wait_ld();
 #pragma unroll
                 for (int sr = 0; sr < 2; ++sr) {
-                    const int row = 32 * warp + 16 * hb + rs + 8 * sr;
+                    const int row = 32 * sp + 16 * hb + rs + 8 * sr;
                     if (row >= I.rows_valid) continue;
                     const int pr = pos[hb][sr];
                     const int nsp = pr / kSplit + 1;
@@ -879,14 +884,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
             tc_fence_before();
-            mbar_arrive(bar(kOFree + ob));           // all 128 softmax threads arrive
+            mbar_arrive(bar(kOFree + ob));           // all 256 softmax threads arrive
             ++ic;
         }
     }
     if (*abort_word && threadIdx.x == 0 && p.err) atomicOr(p.err, PA_DEVERR_TIMEOUT);
     tc_fence_before();
     __syncthreads();
-    if (warp == 5) {
+    if (warp == 9) {
         __syncwarp();
         tc_fence_after();
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),

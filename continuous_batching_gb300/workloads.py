@@ -27,7 +27,7 @@ from typing import Optional
 
 import numpy as np
 
-__all__ = ["Step", "CONFIG_NAMES", "make_config", "make_step", "f32_to_bf16_bits",
+__all__ = ["Step", "CONFIG_NAMES", "make_config", "make_step", "subset", "f32_to_bf16_bits",
            "random_bf16"]
 
 
@@ -242,3 +242,23 @@ def make_step(Hq: int, Hkv: int, D: int, block_size: int, ctx_lens, n_q, seed: i
     else:
         raise ValueError(table)
     return _finish(name, rng, Hq, Hkv, D, block_size, nb, ctx, n_q, tab, with_pool, seed)
+
+
+def subset(step: Step, idx, k_pool=None, v_pool=None, name: str = "subset"):
+    """A step made of sequences ``idx`` of ``step`` (same tables, rows and pool).
+
+    Returns (Step, rows) where rows[j] are the token indices of sequence idx[j] in ``step``."""
+    idx = [int(i) for i in idx]
+    rows = [np.arange(step.cu_seqlens_q[s], step.cu_seqlens_q[s + 1]) for s in idx]
+    n_q = np.array([len(r) for r in rows], np.int32)
+    cu = np.zeros(len(idx) + 1, np.int32)
+    cu[1:] = np.cumsum(n_q)
+    allr = np.concatenate(rows) if rows else np.zeros(0, np.int64)
+    mb = step.block_table.shape[1]
+    sub = Step(name=name, Hq=step.Hq, Hkv=step.Hkv, D=step.D, block_size=step.block_size,
+               num_blocks=step.num_blocks, ctx_lens=step.ctx_lens[idx].copy(), n_q=n_q,
+               cu_seqlens_q=cu, block_table=step.block_table[idx].reshape(len(idx), mb).copy(),
+               q=step.q[allr], k_new=step.k_new[allr], v_new=step.v_new[allr],
+               k_pool=step.k_pool if k_pool is None else k_pool,
+               v_pool=step.v_pool if v_pool is None else v_pool, seed=step.seed)
+    return sub, rows

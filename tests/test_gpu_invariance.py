@@ -25,18 +25,7 @@ def lib():
 
 def sub_step(st: wl.Step, idx, k_pool, v_pool):
     """A step made of sequences `idx` of st (same tables, same pool, same rows)."""
-    idx = list(idx)
-    rows = [np.arange(st.cu_seqlens_q[s], st.cu_seqlens_q[s + 1]) for s in idx]
-    n_q = np.array([len(r) for r in rows], np.int32)
-    cu = np.zeros(len(idx) + 1, np.int32)
-    cu[1:] = np.cumsum(n_q)
-    allr = np.concatenate(rows) if rows else np.zeros(0, np.int64)
-    mb = st.block_table.shape[1]
-    return wl.Step(name="sub", Hq=st.Hq, Hkv=st.Hkv, D=st.D, block_size=st.block_size,
-                   num_blocks=st.num_blocks, ctx_lens=st.ctx_lens[idx].copy(), n_q=n_q,
-                   cu_seqlens_q=cu, block_table=st.block_table[idx].reshape(len(idx), mb).copy(),
-                   q=st.q[allr], k_new=st.k_new[allr], v_new=st.v_new[allr], k_pool=k_pool,
-                   v_pool=v_pool), rows
+    return wl.subset(st, list(idx), k_pool, v_pool)
 
 
 def test_alone_vs_among_others():
