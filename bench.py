@@ -1,6 +1,7 @@
 """Benchmark of one flat ragged paged-attention step on GB300 (one JSON line on stdout).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload decode|mixed|longtail|prefix|prefill]
 
 A step is the whole hot path over one batch of synthetic input: the KV-write scatter of the
 step's new K/V rows, then paged attention for every query row (plus the fixed-order split
@@ -18,6 +19,12 @@ on the host cores, with the same metric and unit.
 
 Under torchrun (N > 1) every rank runs its own decode batch (seed + rank) with no data-path
 collective: the path shards by sequence, so scaling is weak.
+
+--workload selects another of the synthetic workloads for the same JSON line (the default,
+decode, is the headline): longtail (Hq 64, bs 32, 115 rows of 1k-4k and 13 of 16k-40k
+context), prefix (16 prompts x 8 samples sharing 64 read-only blocks; the roofline counts the
+unique K/V bytes), mixed (value in tokens/s) and prefill (the mixed step's four 512-row
+prefill segments alone, tokens/s, tensor roofline).
 """
 from __future__ import annotations
 
@@ -61,6 +68,43 @@ def prefill_flops(st: wl.Step) -> float:
     return f
 
 
+WORKLOADS = {
+    "decode": WORKLOAD,
+    "mixed": MIXED,
+    "longtail": ("long-tail rollout decode: Hq=64, Hkv=8, D=128, block_size=32, 128 decode rows, "
+                 "115 ctx U[1k,4k] + 13 ctx U[16k,40k] at seeded positions, permuted tables, "
+                 "bf16 ~N(0,1), seed 3"),
+    "prefix": ("prefix-shared GRPO decode: Hq=32, Hkv=8, D=128, block_size=16, 16 prompts of 1024 "
+               "tokens x 8 samples sharing the prompt's 64 read-only blocks + own U[1,3000] "
+               "continuation, 128 decode rows, bf16 ~N(0,1), seed 4"),
+    "prefill": ("prefill segments: the mixed step's 4 chunked-prefill segments of 512 rows at "
+                "prior offsets {0,512,4096,9000} alone, Hq=32, Hkv=8, D=128, block_size=16, causal, "
+                "T=2048, seed 2"),
+}
+# the value of these workloads is tokens/s (ragged steps); the others report KV GB/s
+TOKEN_WORKLOADS = ("mixed", "prefill")
+
+
+def unique_kv_bytes(st: wl.Step) -> int:
+    """K/V bytes that must leave HBM once: token rows of distinct blocks (shared blocks once)."""
+    used = {}
+    bs = st.block_size
+    for s in range(st.B):
+        L = int(st.ctx_lens[s])
+        for j in range((L + bs - 1) // bs):
+            b = int(st.block_table[s, j])
+            used[b] = max(used.get(b, 0), min(bs, L - j * bs))
+    return sum(used.values()) * 2 * st.Hkv * st.D * 2
+
+
+def make_workload(name: str, rank: int) -> wl.Step:
+    if name == "prefill":
+        m = wl.make_config("mixed", seed=rank_seed("mixed", rank))
+        st, _ = wl.subset(m, range(48, 52), name="prefill")
+        return st
+    return wl.make_config(name, seed=rank_seed(name, rank))
+
+
 def load_peaks() -> dict:
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -78,10 +122,10 @@ def kernel_source_hash() -> str:
     return h.hexdigest()[:16]
 
 
-def measured_traffic():
+def measured_traffic(workload: str = "decode"):
     """DRAM bytes per attention launch from the committed ncu summary, if it was taken on the
     current kernel source (else None)."""
-    p = os.path.join(ROOT, "profiles", "attention_decode_traffic.json")
+    p = os.path.join(ROOT, "profiles", f"attention_{workload}_traffic.json")
     if not os.path.exists(p):
         return None
     d = json.load(open(p))
@@ -216,7 +260,7 @@ def time_steps(g: GpuStep, torch, steps: int, warmup: int, flush, attn_only=Fals
 
 def rank_seed(name: str, rank: int) -> int:
     """Each rank of a multi-GPU run draws its own batch of the same workload."""
-    base = {"decode": 1, "mixed": 2}[name]
+    base = {"decode": 1, "mixed": 2, "longtail": 3, "prefix": 4}[name]
     return base + rank
 
 
@@ -255,7 +299,8 @@ def run_ours(args) -> dict:
     bd.load()
     peaks = load_peaks()
 
-    st = wl.make_config("decode", seed=rank_seed("decode", rank))
+    name = args.workload
+    st = make_workload(name, rank)
     g = GpuStep(st, torch, bd)
     flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
 
@@ -278,13 +323,17 @@ def run_ours(args) -> dict:
         wall = time.perf_counter() - t0
         if not args.no_clocks:
             load_for(g, torch, 1.0)
+    tokens = name in TOKEN_WORKLOADS
     bytes_step = kv_bytes(st)
+    units_step = float(st.T) if tokens else float(bytes_step)
+    unit = "tokens/s" if tokens else UNIT
+    scale = 1.0 if tokens else 1e-9
     dist_mod = None
     if world > 1:
         import torch.distributed as dist_mod
-    total_ms, all_bytes = combine_ranks(sum(step_ms), float(bytes_step), dist_mod, "cuda")
+    total_ms, all_units = combine_ranks(sum(step_ms), units_step, dist_mod, "cuda")
     ms_per_step = total_ms / args.steps
-    value = all_bytes / (ms_per_step * 1e-3) / 1e9
+    value = all_units / (ms_per_step * 1e-3) * scale
 
     # end to end through the public API with host buffers
     for _ in range(2):
@@ -297,16 +346,29 @@ def run_ours(args) -> dict:
     h2d, d2h = g.e2e_bytes()
 
     attn_avg = statistics.mean(attn_ms)
-    achieved = bytes_step / (attn_avg * 1e-3) / 1e9
-    roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
-            "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
-            "traffic": measured_traffic(),
-            "kernel": "paged_attention_step (tile routine + split combine)",
-            "peak_src": peaks["src"]}
+    if name == "prefill":
+        achieved = prefill_flops(st) / (attn_avg * 1e-3) / 1e12
+        roof = {"bound": "tensor", "achieved": round(achieved, 1), "peak": peaks["bf16_tflops"],
+                "unit": "TFLOP/s", "frac": round(achieved / peaks["bf16_tflops"], 4),
+                "traffic": measured_traffic(name),
+                "kernel": "paged_attention_step (tile routine), causal algorithmic FLOPs "
+                          "4*D*Hq*(n*o + n(n+1)/2)",
+                "peak_src": peaks["src"] + " (burst)"}
+    else:
+        roof_bytes = unique_kv_bytes(st) if name == "prefix" else bytes_step
+        achieved = roof_bytes / (attn_avg * 1e-3) / 1e9
+        roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
+                "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
+                "traffic": measured_traffic(name),
+                "kernel": "paged_attention_step (tile routine + split combine)",
+                "peak_src": peaks["src"]}
+        if name == "prefix":
+            roof["bytes"] = "unique K/V bytes (shared prompt blocks counted once)"
+            roof["logical_gbs"] = round(bytes_step / (attn_avg * 1e-3) / 1e9, 1)
 
-    # the mixed ragged step (tokens/s) alongside
+    # the mixed ragged step (tokens/s) alongside the decode headline
     mixed = None
-    if not args.no_mixed:
+    if name == "decode" and not args.no_mixed:
         sm = wl.make_config("mixed", seed=rank_seed("mixed", rank))
         gm = GpuStep(sm, torch, bd)
         m_step, m_attn = time_steps(gm, torch, args.steps, args.warmup, flush)
@@ -319,15 +381,15 @@ def run_ours(args) -> dict:
         del gm
 
     line = {
-        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
+        "metric": METRIC, "value": round(value, 2), "unit": unit, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic",
-        "config": {"workload": WORKLOAD, "kv_bytes_per_step": bytes_step, "T": st.T,
+        "config": {"workload": WORKLOADS[name], "kv_bytes_per_step": bytes_step, "T": st.T,
                    "l2": f"inputs larger than L2 ({bytes_step / 1e9:.2f} GB K/V) and L2 flushed "
                          "by a 256 MiB write between timed steps",
                    "parallelism": f"replicas{world}"},
-        "e2e": {"value": round(bytes_step / e2e_s / 1e9, 2), "unit": UNIT,
+        "e2e": {"value": round(units_step / e2e_s * scale, 2), "unit": unit,
                 "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                 "ms_per_step": round(e2e_s * 1e3, 4)},
         "roofline": roof,
@@ -338,7 +400,7 @@ def run_ours(args) -> dict:
     if mixed:
         line["ragged_step"] = mixed
     if rank == 0 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(st, budget_s=args.cpu_budget)
+        line["cpu_baseline"] = cpu_baseline(st, budget_s=args.cpu_budget, tokens=tokens)
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
@@ -347,54 +409,71 @@ def run_ours(args) -> dict:
 
 # ---------------------------------------------------------------------- CPU oracle arm
 
-def cpu_baseline(st: wl.Step, budget_s: float = 15.0, rows=None) -> dict:
-    """Times the oracle (fp64 numpy, as it stands) on whole sequences of the workload until
-    about budget_s of CPU work; reports KV GB/s of the sample."""
+def cpu_baseline(st: wl.Step, budget_s: float = 15.0, tokens: bool = False) -> dict:
+    """Times the oracle (fp64 numpy, as it stands) on the workload until about budget_s of CPU
+    work. KV workloads: whole sequences in a seeded order, KV GB/s of the sample. Token
+    workloads: query rows in seeded chunks of 8, tokens/s of the sample."""
     import oracle.paged_attention as pa
     rng = np.random.default_rng(0)
-    order = rng.permutation(st.B)
+    if tokens:
+        order = rng.permutation(st.T)
+        groups = [np.sort(order[i:i + 8]) for i in range(0, st.T, 8)]
+    else:
+        groups = [np.arange(st.cu_seqlens_q[s], st.cu_seqlens_q[s + 1])
+                  for s in rng.permutation(st.B)]
+    seq_of = np.searchsorted(st.cu_seqlens_q, np.arange(st.T), side="right") - 1
     done_bytes = 0
-    n_seq = 0
+    done_rows = 0
+    n_groups = 0
     t0 = time.perf_counter()
-    for s in order:
-        r = np.arange(st.cu_seqlens_q[s], st.cu_seqlens_q[s + 1])
+    for r in groups:
         pa.attention_rows(st.q, st.k_pool, st.v_pool, st.block_table, st.cu_seqlens_q,
                           st.ctx_lens, st.Hq, r)
-        done_bytes += int(st.ctx_lens[s]) * 2 * st.Hkv * st.D * 2
-        n_seq += 1
+        done_rows += len(r)
+        if not tokens:
+            done_bytes += int(st.ctx_lens[seq_of[r[0]]]) * 2 * st.Hkv * st.D * 2
+        n_groups += 1
         if time.perf_counter() - t0 > budget_s:
             break
     dt = time.perf_counter() - t0
+    where = f"numpy fp64 einsum on one thread (host has {os.cpu_count()} cores)"
+    if tokens:
+        return {"value": round(done_rows / dt, 2), "unit": "tokens/s", "cores": 1,
+                "kind": "oracle",
+                "sample": f"{done_rows} of {st.T} query rows (seeded chunks of 8, all {st.Hq} "
+                          f"heads) in {dt:.1f} s; {where}"}
     return {"value": round(done_bytes / dt / 1e9, 4), "unit": UNIT, "cores": 1,
             "kind": "oracle",
-            "sample": f"{n_seq} of {st.B} decode rows (whole sequences, all 32 heads), "
-                      f"{done_bytes / 1e9:.3f} GB of K/V in {dt:.1f} s; numpy fp64 einsum on "
-                      f"one thread (host has {os.cpu_count()} cores)"}
+            "sample": f"{n_groups} of {st.B} decode rows (whole sequences, all {st.Hq} heads), "
+                      f"{done_bytes / 1e9:.3f} GB of K/V in {dt:.1f} s; {where}"}
 
 
 def run_reference(args) -> dict:
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return None
-    st = wl.make_config("decode")
+    name = args.workload
+    st = make_workload(name, 0)
+    tokens = name in TOKEN_WORKLOADS
     for _ in range(args.warmup):
-        cpu_baseline(st, budget_s=0.5)
+        cpu_baseline(st, budget_s=0.5, tokens=tokens)
     vals = []
     t0 = time.perf_counter()
     per = max(1.0, min(20.0, 90.0 / max(args.steps, 1)))
     for _ in range(args.steps):
-        vals.append(cpu_baseline(st, budget_s=per))
+        vals.append(cpu_baseline(st, budget_s=per, tokens=tokens))
     wall = time.perf_counter() - t0
     v = statistics.mean(x["value"] for x in vals)
     base = vals[0]
     base["value"] = round(v, 4)
-    return {"impl": "reference", "metric": METRIC, "value": round(v, 4), "unit": UNIT,
+    unit = base["unit"]
+    return {"impl": "reference", "metric": METRIC, "value": round(v, 4), "unit": unit,
             "n_gpus": int(os.environ.get("WORLD_SIZE", "1")), "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": round(wall / args.steps * 1e3, 2),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-            "data": "synthetic", "config": {"workload": WORKLOAD},
+            "data": "synthetic", "config": {"workload": WORKLOADS[name]},
             "cpu_baseline": base,
-            "e2e": {"value": round(v, 4), "unit": UNIT, "h2d_bytes_per_step": 0,
+            "e2e": {"value": round(v, 4), "unit": unit, "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
 
 
@@ -404,6 +483,8 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="decode", choices=sorted(WORKLOADS),
+                    help="synthetic workload of the timed step (decode is the headline)")
     ap.add_argument("--no-mixed", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
