@@ -396,6 +396,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + L::kBar + kHolderOff);
+    // launched as a programmatic dependent: nothing written by the previous kernel on the
+    // stream (the KV write, or whatever produced q) is read before this point
+    asm volatile("griddepcontrol.wait;" ::: "memory");
 
     if (warp == 8) {
         // ------------------------------------------------------------ producer
@@ -418,6 +421,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (lane == 0 && p.err) atomicOr(p.err, PA_DEVERR_META);
             }
             const bool have = idx < p.n_items;
+            // out of items: the dependent combine may start launching as CTAs retire
+            if (!have && lane == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
             const int slot = ic & 3;
             if (lane == 0) {
                 if (ic >= 4)
@@ -663,11 +668,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else {
         // ------------------------------------------------------------ softmax warps 0-7
-        // Warps w and w + 4 share TMEM sub-partition w % 4 (lanes 32 (w % 4) .. + 31): warp w
-        // takes the first 16 lanes, warp w + 4 the second 16.
+        // Warp w reads TMEM sub-partition w % 4 and takes its 16-lane half w / 4: rows
+        // r0 + rs and r0 + rs + 8 of the tile (r0 = 32 (w % 4) + 16 (w / 4), rs = lane / 4),
+        // each row spread over the 4 threads q4 = lane % 4 (tcgen05.ld 16x256b layout).
         const int tid = threadIdx.x;              // 0..255
-        const int sp = warp & 3;                  // TMEM sub-partition
-        const int my_hb = warp >> 2;              // which 16-lane half of it
+        const int r0 = 32 * (warp & 3) + 16 * (warp >> 2);
+        const uint32_t lanes = uint32_t(r0) << 16;
         const int q4 = lane & 3;
         const int rs = lane >> 2;
         const float c = p.c;
@@ -682,47 +688,39 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_arrive(bar(kItemEmpty + (ic & 3)));
             if (last) break;
             const int ob = ic & 1;
-            const uint32_t tm_o = tmem + kTmemO + ob * 128;
-            bool half_on[2];
-            int pos[2][2];
-            float m_run[2][2], l_run[2][2];
+            const uint32_t tm_o = tmem + kTmemO + ob * 128 + lanes;
+            const bool on = r0 < I.rows_valid;    // warp-uniform: the warp holds a valid row
+            int pos[2];
+            float m_run[2], l_run[2];
 #pragma unroll
-            for (int hb = 0; hb < 2; ++hb) {
-                half_on[hb] = hb == my_hb && (32 * sp + 16 * hb) < I.rows_valid;
-#pragma unroll
-                for (int sr = 0; sr < 2; ++sr) {
-                    const int row = 32 * sp + 16 * hb + rs + 8 * sr;
-                    pos[hb][sr] = row < I.rows_valid ? I.pos0 + row / p.g : -1;
-                    m_run[hb][sr] = -INFINITY;
-                    l_run[hb][sr] = 0.f;
-                }
+            for (int sr = 0; sr < 2; ++sr) {
+                const int row = r0 + rs + 8 * sr;
+                pos[sr] = row < I.rows_valid ? I.pos0 + row / p.g : -1;
+                m_run[sr] = -INFINITY;
+                l_run[sr] = 0.f;
             }
             for (int jt = 0; jt < I.n_tiles; ++jt, ++tc) {
                 if (!(ok = wait_bounded(bar(kSFull + (tc & 1)), (tc >> 1) & 1, abort_word)))
                     break;
                 tc_fence_after();
                 const int kb = I.k_begin + jt * kTileKeys;
-                const uint32_t tm_s = tmem + (tc & 1) * 128;
-                float alpha[2][2];
-#pragma unroll
-                for (int hb = 0; hb < 2; ++hb) {
-                    if (!half_on[hb]) continue;
-                    const uint32_t lanes = uint32_t(32 * sp + 16 * hb) << 16;
+                const uint32_t tm_s = tmem + (tc & 1) * 128 + lanes;
+                float alpha[2] = {1.f, 1.f};
+                if (on) {
                     uint32_t r[64];
-                    tmem_ld_16x256b_x16(tm_s + lanes, r);
+                    tmem_ld_16x256b_x16(tm_s, r);
                     tmem_wait_ld();
                     uint32_t pk[32];                 // P rounded to bf16, packed in pairs
 #pragma unroll
                     for (int sr = 0; sr < 2; ++sr) {
                         // an 8-row block with no valid row (the tail of a decode or a ragged
                         // tile) needs no softmax: its P is never used for a written output
-                        if (32 * sp + 16 * hb + 8 * sr >= I.rows_valid) {
-                            alpha[hb][sr] = 1.f;
+                        if (r0 + 8 * sr >= I.rows_valid) {
 #pragma unroll
                             for (int cc = 0; cc < 16; ++cc) pk[2 * cc + sr] = 0u;
                             continue;
                         }
-                        const int pr = pos[hb][sr];
+                        const int pr = pos[sr];
                         // the causal / ctx mask matters only when some key of the tile lies past
                         // some row of this block
                         const bool full = __all_sync(0xffffffffu, kb + kTileKeys - 1 <= pr);
@@ -754,7 +752,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         // The reference maximum moves only when the row's maximum grows past it by
                         // more than 8 in base-2 units, so P <= 2^8 and O needs rescaling rarely;
                         // the decision depends on the row's own scores alone.
-                        const float m_old = m_run[hb][sr];
+                        const float m_old = m_run[sr];
                         const float m_new = fmaxf(m_old, mx);
                         const bool move = m_old == -INFINITY
                                               ? m_new != -INFINITY
@@ -773,49 +771,40 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                         sum = __fadd_rn(sum, __shfl_xor_sync(0xffffffffu, sum, 1));
                         sum = __fadd_rn(sum, __shfl_xor_sync(0xffffffffu, sum, 2));
-                        l_run[hb][sr] = __fadd_rn(__fmul_rn(l_run[hb][sr], a), sum);
-                        m_run[hb][sr] = m_ref;
-                        alpha[hb][sr] = a;
+                        l_run[sr] = __fadd_rn(__fmul_rn(l_run[sr], a), sum);
+                        m_run[sr] = m_ref;
+                        alpha[sr] = a;
                         // keys 8cc + 2q4 + {0, 1} -> packed column 4cc + q4 (16x128b layout)
 #pragma unroll
                         for (int cc = 0; cc < 16; ++cc)
                             pk[2 * cc + sr] = pack_bf16(sv[2 * cc], sv[2 * cc + 1]);
                     }
                     // P replaces S in the first 64 columns of this tile's S buffer
-                    tmem_st_16x128b_x16(tm_s + lanes, pk);
+                    tmem_st_16x128b_x16(tm_s, pk);
                 }
                 // O belongs to the previous tile's PV until it has finished: rescale only then,
                 // and only in warps where some row's running maximum moved
-                bool need = false;
-#pragma unroll
-                for (int hb = 0; hb < 2; ++hb)
-                    if (half_on[hb]) need |= alpha[hb][0] != 1.f || alpha[hb][1] != 1.f;
+                const bool need = alpha[0] != 1.f || alpha[1] != 1.f;
                 if (jt > 0 && __any_sync(0xffffffffu, need)) {
                     if (!(ok = wait_bounded(bar(kPVDone + ((tc - 1) & 1)), ((tc - 1) >> 1) & 1,
                                             abort_word)))
                         break;
                     tc_fence_after();
+                    uint32_t o[D / 2];
+                    if constexpr (D == 128) tmem_ld_16x256b_x16(tm_o, o);
+                    else tmem_ld_16x256b_x8(tm_o, o);
+                    tmem_wait_ld();
 #pragma unroll
-                    for (int hb = 0; hb < 2; ++hb) {
-                        if (!half_on[hb]) continue;
-                        const uint32_t ta = tm_o + (uint32_t(32 * sp + 16 * hb) << 16);
-                        uint32_t o[D / 2];
-                        if constexpr (D == 128) tmem_ld_16x256b_x16(ta, o);
-                        else tmem_ld_16x256b_x8(ta, o);
-                        tmem_wait_ld();
+                    for (int cc = 0; cc < D / 8; ++cc)
 #pragma unroll
-                        for (int cc = 0; cc < D / 8; ++cc)
+                        for (int sr = 0; sr < 2; ++sr)
 #pragma unroll
-                            for (int sr = 0; sr < 2; ++sr)
-#pragma unroll
-                                for (int e = 0; e < 2; ++e) {
-                                    const int k = 4 * cc + 2 * sr + e;
-                                    o[k] = __float_as_uint(
-                                        __fmul_rn(__uint_as_float(o[k]), alpha[hb][sr]));
-                                }
-                        if constexpr (D == 128) tmem_st_16x256b_x16(ta, o);
-                        else tmem_st_16x256b_x8(ta, o);
-                    }
+                            for (int e = 0; e < 2; ++e) {
+                                const int k = 4 * cc + 2 * sr + e;
+                                o[k] = __float_as_uint(__fmul_rn(__uint_as_float(o[k]), alpha[sr]));
+                            }
+                    if constexpr (D == 128) tmem_st_16x256b_x16(tm_o, o);
+                    else tmem_st_16x256b_x8(tm_o, o);
                 }
                 tmem_wait_st();
                 // keys at or beyond ctx are stale or were never loaded: give them zero values
@@ -823,13 +812,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (kb + kTileKeys > I.ctx) {
                     if (!(ok = wait_bounded(bar(kVFull + tc % SV), (tc / SV) & 1, abort_word)))
                         break;
-                    const int r0 = max(I.ctx - kb, 0);
-                    const int nrow = kTileKeys - r0;
+                    const int z0 = max(I.ctx - kb, 0);
+                    const int nrow = kTileKeys - z0;
                     const uint32_t vb = sb + L::kV + (tc % SV) * L::kKVTile;
                     for (int i = tid; i < nrow * 8 * L::kChunks; i += 256) {
                         const int hh = i / (nrow * 8);
                         const int rem = i % (nrow * 8);
-                        const int key = r0 + rem / 8;
+                        const int key = z0 + rem / 8;
                         st_shared_zero16(vb + (key / p.bs) * (p.bs * 128 * L::kChunks) +
                                          hh * (p.bs * 128) + (key % p.bs) * 128 + (rem % 8) * 16);
                     }
@@ -843,25 +832,27 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!(ok = wait_bounded(bar(kPVDone + ((tc - 1) & 1)), ((tc - 1) >> 1) & 1, abort_word)))
                 break;
             tc_fence_after();
-#pragma unroll
-            for (int hb = 0; hb < 2; ++hb) {
-                if (!half_on[hb]) continue;
-                const uint32_t ta = tm_o + (uint32_t(32 * sp + 16 * hb) << 16);
+            if (!on) {
+                tc_fence_before();
+                mbar_arrive(bar(kOFree + ob));
+            } else {
                 uint32_t o[D / 2];
-                if constexpr (D == 128) tmem_ld_16x256b_x16(ta, o);
-                else tmem_ld_16x256b_x8(ta, o);
+                if constexpr (D == 128) tmem_ld_16x256b_x16(tm_o, o);
+                else tmem_ld_16x256b_x8(tm_o, o);
                 tmem_wait_ld();
+                tc_fence_before();
+                mbar_arrive(bar(kOFree + ob));       // O is in registers: its buffer is free
 #pragma unroll
                 for (int sr = 0; sr < 2; ++sr) {
-                    const int row = 32 * sp + 16 * hb + rs + 8 * sr;
+                    const int row = r0 + rs + 8 * sr;
                     if (row >= I.rows_valid) continue;
-                    const int pr = pos[hb][sr];
+                    const int pr = pos[sr];
                     const int nsp = pr / kSplit + 1;
                     if (I.split >= nsp) continue;        // the row has no keys in this split
                     const int tok = I.q_start + row / p.g;
                     const int head = I.kvh * p.g + row % p.g;
                     if (nsp == 1) {
-                        const float inv = __frcp_rn(l_run[hb][sr]);
+                        const float inv = __frcp_rn(l_run[sr]);
                         __nv_bfloat16* dst = p.out + (int64_t(tok) * p.Hq + head) * D;
 #pragma unroll
                         for (int cc = 0; cc < D / 8; ++cc) {
@@ -879,12 +870,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                                             __uint_as_float(o[4 * cc + 2 * sr + 1]));
                         if (q4 == 0)
                             *reinterpret_cast<float2*>(p.ws_ml + slot * 2) =
-                                make_float2(m_run[hb][sr], l_run[hb][sr]);
+                                make_float2(m_run[sr], l_run[sr]);
                     }
                 }
             }
-            tc_fence_before();
-            mbar_arrive(bar(kOFree + ob));           // all 256 softmax threads arrive
             ++ic;
         }
     }
@@ -906,58 +895,82 @@ __global__ void __launch_bounds__(kThreads, 1)
 //   M' = max(M, m_s), a = 2^((M - M') c), b = 2^((m_s - M') c),
 //   L = L a + l_s b, ACC = ACC a + acc_s b;  out = bf16_rne(ACC * rcp_rn(L)).
 // A row with one split is finished by the attention kernel with the same two roundings.
+// One thread per (row, q head, 4 columns); the partials of up to kBatch splits are loaded
+// before they are folded, so a row costs about nsplit / kBatch memory round trips. Launched
+// as a programmatic dependent of the attention kernel (its launch overlaps the attention
+// tail); griddepcontrol.wait holds every thread until that grid has completed and its
+// writes are visible.
 template <int D>
-__global__ void __launch_bounds__(128)
+__global__ void __launch_bounds__(256)
     combine_kernel(const float* __restrict__ ws_acc, const float* __restrict__ ws_ml,
                    const int32_t* __restrict__ cu, const int32_t* __restrict__ ctx, int32_t B,
                    int32_t T, int32_t Hq, int32_t max_splits, float c,
                    __nv_bfloat16* __restrict__ out) {
-    constexpr int E = D / 32;
-    const int64_t w = int64_t(blockIdx.x) * 4 + (threadIdx.x >> 5);
-    const int lane = threadIdx.x & 31;
+    constexpr int kCols = 4;                  // columns per thread (one float4)
+    constexpr int kUnits = D / kCols;         // threads per (row, q head)
+    constexpr int kBatch = 8;                 // splits loaded ahead of their fold
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    const int64_t n = int64_t(T) * Hq * kUnits;
+    const int64_t u = int64_t(blockIdx.x) * 256 + threadIdx.x;
+    if (u >= n) return;
+    const int64_t w = u / kUnits;
+    const int col = int(u % kUnits) * kCols;
     const int64_t tok = w / Hq;
     const int head = int(w % Hq);
-    if (tok >= T) return;
-    int lo = 0, hi = B - 1;                     // sequence s with cu[s] <= tok < cu[s+1]
+    int lo = 0, hi = B - 1;                   // sequence s with cu[s] <= tok < cu[s+1]
     while (lo < hi) {
         const int mid = (lo + hi + 1) >> 1;
-        if (cu[mid] <= tok) lo = mid;
+        if (__ldg(cu + mid) <= tok) lo = mid;
         else hi = mid - 1;
     }
-    const int pos = ctx[lo] - cu[lo + 1] + int(tok);
-    if (pos < 0) return;                         // inconsistent metadata: flagged by the kernel
+    const int pos = __ldg(ctx + lo) - __ldg(cu + lo + 1) + int(tok);
+    if (pos < 0) return;                      // inconsistent metadata: flagged by the kernel
     const int nsp = pos / kSplit + 1;
     if (nsp == 1 || nsp > max_splits) return;
     const int64_t base = tok * max_splits;
-    float acc[E];
-    float M, Lsum;
+    const float2* ml = reinterpret_cast<const float2*>(ws_ml);
+    float M, Lsum, acc[kCols];
     {
         const int64_t slot = base * Hq + head;
-        const float2 ml = *reinterpret_cast<const float2*>(ws_ml + slot * 2);
-        M = ml.x;
-        Lsum = ml.y;
-#pragma unroll
-        for (int e = 0; e < E; ++e) acc[e] = ws_acc[slot * D + lane * E + e];
+        const float2 m0 = ml[slot];
+        const float4 a0 = *reinterpret_cast<const float4*>(ws_acc + slot * D + col);
+        M = m0.x;
+        Lsum = m0.y;
+        acc[0] = a0.x;
+        acc[1] = a0.y;
+        acc[2] = a0.z;
+        acc[3] = a0.w;
     }
-    for (int s = 1; s < nsp; ++s) {
-        const int64_t slot = (base + s) * Hq + head;
-        const float2 ml = *reinterpret_cast<const float2*>(ws_ml + slot * 2);
-        const float mn = fmaxf(M, ml.x);
-        const float fa = M == mn ? 1.f : ex2(__fmul_rn(__fsub_rn(M, mn), c));
-        const float fb = ml.x == mn ? 1.f : ex2(__fmul_rn(__fsub_rn(ml.x, mn), c));
-        Lsum = __fadd_rn(__fmul_rn(Lsum, fa), __fmul_rn(ml.y, fb));
+    for (int s0 = 1; s0 < nsp; s0 += kBatch) {
+        float2 ms[kBatch];
+        float4 as[kBatch];
 #pragma unroll
-        for (int e = 0; e < E; ++e)
-            acc[e] = __fadd_rn(__fmul_rn(acc[e], fa),
-                               __fmul_rn(ws_acc[slot * D + lane * E + e], fb));
-        M = mn;
+        for (int j = 0; j < kBatch; ++j) {
+            if (s0 + j < nsp) {
+                const int64_t slot = (base + s0 + j) * Hq + head;
+                ms[j] = ml[slot];
+                as[j] = *reinterpret_cast<const float4*>(ws_acc + slot * D + col);
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < kBatch; ++j) {
+            if (s0 + j >= nsp) break;
+            const float mn = fmaxf(M, ms[j].x);
+            const float fa = M == mn ? 1.f : ex2(__fmul_rn(__fsub_rn(M, mn), c));
+            const float fb = ms[j].x == mn ? 1.f : ex2(__fmul_rn(__fsub_rn(ms[j].x, mn), c));
+            Lsum = __fadd_rn(__fmul_rn(Lsum, fa), __fmul_rn(ms[j].y, fb));
+            const float av[kCols] = {as[j].x, as[j].y, as[j].z, as[j].w};
+#pragma unroll
+            for (int e = 0; e < kCols; ++e)
+                acc[e] = __fadd_rn(__fmul_rn(acc[e], fa), __fmul_rn(av[e], fb));
+            M = mn;
+        }
     }
-    __nv_bfloat16* dst = out + (tok * Hq + head) * D + lane * E;
     const float inv = __frcp_rn(Lsum);
-#pragma unroll
-    for (int e = 0; e < E; e += 2)
-        *reinterpret_cast<uint32_t*>(dst + e) =
-            pack_bf16(__fmul_rn(acc[e], inv), __fmul_rn(acc[e + 1], inv));
+    __nv_bfloat16* dst = out + (tok * Hq + head) * D + col;
+    *reinterpret_cast<uint2*>(dst) =
+        make_uint2(pack_bf16(__fmul_rn(acc[0], inv), __fmul_rn(acc[1], inv)),
+                   pack_bf16(__fmul_rn(acc[2], inv), __fmul_rn(acc[3], inv)));
 }
 
 // ------------------------------------------------------------------------- host side
@@ -1057,15 +1070,30 @@ int32_t launch(const Maps& maps, const Params& prm, int32_t max_ctx, cudaStream_
     int sms = 0;
     if ((st = sm_count_for_current_device(&sms))) return st;
     const int grid = std::min(prm.n_items, sms);
-    paged_attn_kernel<D><<<grid, kThreads, Layout<D>::kAlloc, stream>>>(maps.k, maps.v, maps.q1,
-                                                                       maps.qn, prm);
-    if ((st = note_cuda(cudaGetLastError()))) return st;
+    // Both kernels are programmatic dependents of what precedes them on the stream: each
+    // launches while its predecessor drains and waits (griddepcontrol.wait) before it reads
+    // anything.
+    cudaLaunchAttribute pdl[1];
+    pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    pdl[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(unsigned(grid));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = Layout<D>::kAlloc;
+    cfg.stream = stream;
+    cfg.attrs = pdl;
+    cfg.numAttrs = 1;
+    st = note_cuda(cudaLaunchKernelEx(&cfg, paged_attn_kernel<D>, maps.k, maps.v, maps.q1,
+                                      maps.qn, prm));
+    if (st) return st;
     if (max_ctx > kSplit) {
-        const int64_t warps = int64_t(prm.T) * prm.Hq;
-        combine_kernel<D><<<unsigned((warps + 3) / 4), 128, 0, stream>>>(
-            prm.ws_acc, prm.ws_ml, prm.cu, prm.ctx, prm.B, prm.T, prm.Hq, prm.max_splits, prm.c,
-            prm.out);
-        st = note_cuda(cudaGetLastError());
+        const int64_t threads = int64_t(prm.T) * prm.Hq * (D / 4);
+        cfg.gridDim = dim3(unsigned((threads + 255) / 256));
+        cfg.blockDim = dim3(256);
+        cfg.dynamicSmemBytes = 0;
+        st = note_cuda(cudaLaunchKernelEx(&cfg, combine_kernel<D>, (const float*)prm.ws_acc,
+                                          (const float*)prm.ws_ml, prm.cu, prm.ctx, prm.B, prm.T,
+                                          prm.Hq, prm.max_splits, prm.c, prm.out));
     }
     return st;
 }
@@ -1111,6 +1139,7 @@ int32_t prepare_step(const void* q, const void* k_pool, const void* v_pool,
     return PA_OK;
 }
 
+// Workspace: acc [T][max_splits][Hq][D] fp32, then (m, l) [T][max_splits][Hq][2] fp32.
 void point_workspace(Params* prm, float* ws, int32_t T, int32_t Hq, int D) {
     prm->ws_acc = ws;
     prm->ws_ml = ws ? ws + size_t(T) * prm->max_splits * Hq * D : nullptr;

@@ -19,6 +19,9 @@ __global__ void __launch_bounds__(128) kv_write_kernel(const uint4* __restrict__
                                                        uint4* __restrict__ v_pool,
                                                        int32_t row_vecs, int64_t num_slots,
                                                        int32_t* err) {
+    // the attention kernel that follows on the stream may launch now: it waits for this
+    // grid to complete before it reads the pools
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int64_t t = blockIdx.x;
     const int32_t slot = slots[t];
     if (slot < 0) return;                         // "no write" marker

@@ -217,6 +217,10 @@ int32_t paged_kv_write(const void* k_new, const void* v_new, const int32_t* slot
  * accumulation, fp32 online softmax per fixed KV split, splits combined in ascending order,
  * result rounded to bf16 (nearest even). Every row, decode or prefill, runs the same tile
  * routine, so its bits depend only on its own query, keys and position.
+ * Launches: the attention kernel, then (when max_ctx > PA_SPLIT_TOKENS) the split-combine
+ * kernel, both as programmatic dependent launches: each may start while the previous kernel
+ * on the stream drains, and waits for that kernel to complete before it reads anything, so
+ * stream order is kept for every input.
  * Device inputs: q [T, Hq, D] bf16; k_pool, v_pool [num_blocks, block_size, Hkv, D] bf16;
  * block_table [B, max_blocks] int32; cu_seqlens_q [B+1], ctx_lens [B] int32 (the same values
  * given to pa_plan_step); items [n_items] from pa_plan_step; workspace of ws_bytes >=
