@@ -411,16 +411,26 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         int ic = 0;
         int ok = 1;
-        int idx = blockIdx.x;
+        // Snake order over the (longest-first) item list: round r gives CTA c the item
+        // r G + c when r is even and r G + (G - 1 - c) when r is odd, which evens out the
+        // CTAs' totals (a plain stride would hand CTA 0 the longest item of every round).
+        int round = 0;
+        const int G = int(gridDim.x);
         for (;;) {
             Item I;
             I.good = false;
-            for (; idx < p.n_items; idx += gridDim.x) {
-                I = load_item(p, idx);
-                if (I.good) break;
+            bool have = false;
+            for (; int64_t(round) * G < p.n_items; ++round) {
+                const int x = (round & 1) ? G - 1 - int(blockIdx.x) : int(blockIdx.x);
+                const int64_t idx = int64_t(round) * G + x;
+                if (idx >= p.n_items) continue;           // a hole in the last, partial round
+                I = load_item(p, int(idx));
+                if (I.good) {
+                    have = true;
+                    break;
+                }
                 if (lane == 0 && p.err) atomicOr(p.err, PA_DEVERR_META);
             }
-            const bool have = idx < p.n_items;
             // out of items: the dependent combine may start launching as CTAs retire
             if (!have && lane == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
             const int slot = ic & 3;
@@ -462,7 +472,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             ok = __shfl_sync(0xffffffffu, ok, 0);
             if (!ok) break;
-            idx += gridDim.x;
+            ++round;
             ++ic;
         }
         if (lane == 0) {
