@@ -769,7 +769,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                                               : __fmul_rn(__fsub_rn(m_new, m_old), c) > kLazyLog2;
                         const float m_ref = move ? m_new : m_old;
                         const float m_use = m_ref == -INFINITY ? 0.f : m_ref;
-                        const float a = m_old == m_use
+                        // A row that has not seen a key yet (a padding row of the block, or a
+                        // row whose position precedes this split) has O = 0 and l = 0: its
+                        // factor stays 1 so that it never asks for a rescale of O.
+                        const float a = (m_old == m_use || m_ref == -INFINITY)
                                             ? 1.f
                                             : ex2(__fmul_rn(__fsub_rn(m_old, m_use), c));
                         const float nmc = __fmul_rn(-m_use, c);
