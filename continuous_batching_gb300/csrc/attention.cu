@@ -193,6 +193,16 @@ __device__ bool wait_bounded(uint32_t bar, uint32_t parity, volatile int* abort_
     }
 }
 
+// Waits for an mbarrier phase that the CTA's own copies or MMAs complete, before the CTA
+// leaves: it ignores the abort word (the copies are in flight whatever happened) but still
+// gives up after kWaitLimitNs.
+__device__ void wait_drain(uint32_t bar, uint32_t parity) {
+    if (mbar_try_wait(bar, parity)) return;
+    const unsigned long long t0 = global_ns();
+    while (!mbar_try_wait(bar, parity))
+        if (global_ns() - t0 > kWaitLimitNs) return;
+}
+
 __device__ __forceinline__ void fence_proxy_async() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
@@ -357,6 +367,187 @@ __device__ __forceinline__ Item load_item(const Params& p, int idx) {
     return I;
 }
 
+// ---------------------------------------------------------------- the per-row routine
+// Every query row, whichever kernel runs it, goes through these three functions, so that its
+// bits depend only on its own scores. A thread owns two rows of a 16-row half of the 128-row
+// tile (rows r0 + rs and r0 + rs + 8, rs = lane / 4), each spread over the 4 threads
+// q4 = lane % 4 (tcgen05.ld 16x256b layout: columns 8 cc + 2 q4 + {0, 1}).
+struct Rows2 {
+    int pos[2];        // absolute position of the row, -1 for a padding row
+    float m[2], l[2];  // softmax reference maximum (raw score units) and running sum
+};
+
+__device__ __forceinline__ void rows_init(Rows2& R, int r0, int rs, int rows_valid, int pos0,
+                                          int g) {
+#pragma unroll
+    for (int sr = 0; sr < 2; ++sr) {
+        const int row = r0 + rs + 8 * sr;
+        R.pos[sr] = row < rows_valid ? pos0 + row / g : -1;
+        R.m[sr] = -INFINITY;
+        R.l[sr] = 0.f;
+    }
+}
+
+// Online softmax of one 128-key tile (keys kb .. kb + 127) for the half at TMEM address tm_s
+// (lane offset included): S is read, the rows' state is updated and P, rounded to bf16, is
+// stored over the first 64 columns. alpha[sr] is the factor the row's O must be scaled by.
+__device__ __forceinline__ void softmax_half(uint32_t tm_s, int r0, int q4, int rows_valid,
+                                             int kb, float c, Rows2& R, float alpha[2]) {
+    uint32_t r[64];
+    tmem_ld_16x256b_x16(tm_s, r);
+    tmem_wait_ld();
+    uint32_t pk[32];                 // P rounded to bf16, packed in pairs
+#pragma unroll
+    for (int sr = 0; sr < 2; ++sr) {
+        alpha[sr] = 1.f;
+        // an 8-row block with no valid row (the tail of a decode or a ragged tile) needs no
+        // softmax: its P is never used for a written output
+        if (r0 + 8 * sr >= rows_valid) {
+#pragma unroll
+            for (int cc = 0; cc < 16; ++cc) pk[2 * cc + sr] = 0u;
+            continue;
+        }
+        const int pr = R.pos[sr];
+        // the causal / ctx mask matters only when some key of the tile lies past some row of
+        // this block
+        const bool full = __all_sync(0xffffffffu, kb + kTileKeys - 1 <= pr);
+        float sv[32];
+        float mx = -INFINITY;
+        if (full) {
+#pragma unroll
+            for (int cc = 0; cc < 16; ++cc)
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const float sc = __uint_as_float(r[4 * cc + 2 * sr + e]);
+                    sv[2 * cc + e] = sc;
+                    mx = fmaxf(mx, sc);
+                }
+        } else {
+#pragma unroll
+            for (int cc = 0; cc < 16; ++cc)
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const int key = kb + 8 * cc + 2 * q4 + e;
+                    const float sc = key <= pr ? __uint_as_float(r[4 * cc + 2 * sr + e]) : -INFINITY;
+                    sv[2 * cc + e] = sc;
+                    mx = fmaxf(mx, sc);
+                }
+        }
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+        // The reference maximum moves only when the row's maximum grows past it by more than
+        // 8 in base-2 units, so P <= 2^8 and O needs rescaling rarely; the decision depends on
+        // the row's own scores alone.
+        const float m_old = R.m[sr];
+        const float m_new = fmaxf(m_old, mx);
+        const bool move = m_old == -INFINITY ? m_new != -INFINITY
+                                             : __fmul_rn(__fsub_rn(m_new, m_old), c) > kLazyLog2;
+        const float m_ref = move ? m_new : m_old;
+        const float m_use = m_ref == -INFINITY ? 0.f : m_ref;
+        // A row that has not seen a key yet (a padding row of the block, or a row whose
+        // position precedes this split) has O = 0 and l = 0: its factor stays 1 so that it
+        // never asks for a rescale of O.
+        const float a = (m_old == m_use || m_ref == -INFINITY)
+                            ? 1.f
+                            : ex2(__fmul_rn(__fsub_rn(m_old, m_use), c));
+        const float nmc = __fmul_rn(-m_use, c);
+        float sum = 0.f;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+            sv[i] = ex2(__fmaf_rn(sv[i], c, nmc));
+            sum = __fadd_rn(sum, sv[i]);
+        }
+        sum = __fadd_rn(sum, __shfl_xor_sync(0xffffffffu, sum, 1));
+        sum = __fadd_rn(sum, __shfl_xor_sync(0xffffffffu, sum, 2));
+        R.l[sr] = __fadd_rn(__fmul_rn(R.l[sr], a), sum);
+        R.m[sr] = m_ref;
+        alpha[sr] = a;
+        // keys 8cc + 2q4 + {0, 1} -> packed column 4cc + q4 (16x128b layout)
+#pragma unroll
+        for (int cc = 0; cc < 16; ++cc) pk[2 * cc + sr] = pack_bf16(sv[2 * cc], sv[2 * cc + 1]);
+    }
+    // P replaces S in the first 64 columns of this tile's S buffer
+    tmem_st_16x128b_x16(tm_s, pk);
+}
+
+// O of the half (TMEM address tm_o, lane offset included) scaled row by row by alpha.
+template <int D>
+__device__ __forceinline__ void rescale_half(uint32_t tm_o, const float alpha[2]) {
+    uint32_t o[D / 2];
+    if constexpr (D == 128) tmem_ld_16x256b_x16(tm_o, o);
+    else tmem_ld_16x256b_x8(tm_o, o);
+    tmem_wait_ld();
+#pragma unroll
+    for (int cc = 0; cc < D / 8; ++cc)
+#pragma unroll
+        for (int sr = 0; sr < 2; ++sr)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                const int k = 4 * cc + 2 * sr + e;
+                o[k] = __float_as_uint(__fmul_rn(__uint_as_float(o[k]), alpha[sr]));
+            }
+    if constexpr (D == 128) tmem_st_16x256b_x16(tm_o, o);
+    else tmem_st_16x256b_x8(tm_o, o);
+}
+
+// Epilogue of the half, O already in registers: a row whose position lies in one split is
+// finished here (out = bf16(O * rcp(l))); a row spanning several splits stores this split's
+// partial (acc = O, m, l) for the fixed-order combine. Rows are those of a tile whose first
+// row is token q_start at position pos0 (rows_valid rows, g heads per token).
+template <int D>
+__device__ __forceinline__ void store_half(const Params& p, const uint32_t* o, int r0, int rs,
+                                           int q4, int rows_valid, int q_start, int kvh,
+                                           int split, const Rows2& R) {
+#pragma unroll
+    for (int sr = 0; sr < 2; ++sr) {
+        const int row = r0 + rs + 8 * sr;
+        if (row >= rows_valid) continue;
+        const int pr = R.pos[sr];
+        const int nsp = pr / kSplit + 1;
+        if (split >= nsp) continue;              // the row has no keys in this split
+        const int tok = q_start + row / p.g;
+        const int head = kvh * p.g + row % p.g;
+        if (nsp == 1) {
+            const float inv = __frcp_rn(R.l[sr]);
+            __nv_bfloat16* dst = p.out + (int64_t(tok) * p.Hq + head) * D;
+#pragma unroll
+            for (int cc = 0; cc < D / 8; ++cc) {
+                const float x0 = __fmul_rn(__uint_as_float(o[4 * cc + 2 * sr]), inv);
+                const float x1 = __fmul_rn(__uint_as_float(o[4 * cc + 2 * sr + 1]), inv);
+                *reinterpret_cast<uint32_t*>(dst + 8 * cc + 2 * q4) = pack_bf16(x0, x1);
+            }
+        } else {
+            const int64_t slot = (int64_t(tok) * p.max_splits + split) * p.Hq + head;
+            float* acc = p.ws_acc + slot * D;
+#pragma unroll
+            for (int cc = 0; cc < D / 8; ++cc)
+                *reinterpret_cast<float2*>(acc + 8 * cc + 2 * q4) =
+                    make_float2(__uint_as_float(o[4 * cc + 2 * sr]),
+                                __uint_as_float(o[4 * cc + 2 * sr + 1]));
+            if (q4 == 0)
+                *reinterpret_cast<float2*>(p.ws_ml + slot * 2) = make_float2(R.m[sr], R.l[sr]);
+        }
+    }
+}
+
+// Keys at or beyond ctx in the tile starting at key kb are stale or were never loaded: their
+// V rows in the slot at vb are zeroed (threads tid of nthr share the work) so that their zero
+// probabilities contribute exact zeros.
+template <int D>
+__device__ __forceinline__ void zero_v_tail(uint32_t vb, int kb, int ctx, int bs, int tid,
+                                            int nthr) {
+    constexpr int kChunks = D / 64;
+    const int z0 = max(ctx - kb, 0);
+    const int nrow = kTileKeys - z0;
+    for (int i = tid; i < nrow * 8 * kChunks; i += nthr) {
+        const int hh = i / (nrow * 8);
+        const int rem = i % (nrow * 8);
+        const int key = z0 + rem / 8;
+        st_shared_zero16(vb + (key / bs) * (bs * 128 * kChunks) + hh * (bs * 128) +
+                         (key % bs) * 128 + (rem % 8) * 16);
+    }
+}
+
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     paged_attn_kernel(const __grid_constant__ CUtensorMap tm_k,
@@ -478,7 +669,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
             // never leave with copies in flight into this CTA's shared memory
             for (int i = max(0, ic - 2); i < ic; ++i)
-                wait_bounded(bar(kQFull + (i & 1)), (i >> 1) & 1, abort_word);
+                wait_drain(bar(kQFull + (i & 1)), (i >> 1) & 1);
         }
     } else if (warp == 9) {
         // ------------------------------------------------------------ MMA issuer
@@ -500,16 +691,26 @@ __global__ void __launch_bounds__(kThreads, 1)
             // bs * 128 bytes apart (MN-major B operand: LBO = half stride, SBO = 8-key stride)
             const uint32_t v_lbo = uint32_t(p.bs) * 128;
             const uint32_t v_sbo = p.bs >= 16 ? 1024u : uint32_t(p.bs) * 128 * L::kChunks;
+            // offset of the 16-key step k inside a V slot (block of the step, row in the
+            // block), computed once: the issuing thread shares its scheduler with the softmax
+            // warps, and a division per MMA would throttle the tensor pipe
+            uint32_t v_off[kTileKeys / 16];
+            {
+                const int log2bs = __ffs(p.bs) - 1;
+#pragma unroll
+                for (int k = 0; k < kTileKeys / 16; ++k) {
+                    const int key = 16 * k;
+                    v_off[k] = uint32_t(key >> log2bs) * (uint32_t(p.bs) * 128 * L::kChunks) +
+                               uint32_t(key & (p.bs - 1)) * 128;
+                }
+            }
             const auto issue_pv = [&](int st, uint32_t p_tmem, uint32_t d, bool acc) {
                 const uint32_t vbase = sb + L::kV + st * L::kKVTile;   // V ring slot
 #pragma unroll
                 for (int k = 0; k < kTileKeys / 16; ++k) {
-                    const int key = 16 * k;                  // first key of this 16-key step
-                    const uint32_t va = vbase + (key / p.bs) * (p.bs * 128 * L::kChunks) +
-                                        (key % p.bs) * 128;
                     // P of keys 16k .. 16k+15 is 8 packed columns of the S buffer
-                    umma_bf16_tmem_a(d, p_tmem + 8 * k, make_sdesc(va, v_lbo, v_sbo), idesc_o,
-                                     (acc || k > 0) ? 1u : 0u);
+                    umma_bf16_tmem_a(d, p_tmem + 8 * k, make_sdesc(vbase + v_off[k], v_lbo, v_sbo),
+                                     idesc_o, (acc || k > 0) ? 1u : 0u);
                 }
             };
             // Two cursors walk the same item sequence: one issues S = Q K^T for the next tile
@@ -592,7 +793,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             // drain: every MMA this thread issued has finished before TMEM is released
             tc_commit(bar(kDrain));
-            wait_bounded(bar(kDrain), 0, abort_word);
+            wait_drain(bar(kDrain), 0);
         }
     } else if (warp >= 10) {
         // ------------------------------------------------------------ K (warp 6) / V (warp 7)
@@ -674,13 +875,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
             // never leave with copies in flight into this CTA's shared memory
             for (int t = max(0, tc - S); t < tc; ++t)
-                wait_bounded(bar(full_b + t % S), (t / S) & 1, abort_word);
+                wait_drain(bar(full_b + t % S), (t / S) & 1);
         }
     } else {
         // ------------------------------------------------------------ softmax warps 0-7
         // Warp w reads TMEM sub-partition w % 4 and takes its 16-lane half w / 4: rows
-        // r0 + rs and r0 + rs + 8 of the tile (r0 = 32 (w % 4) + 16 (w / 4), rs = lane / 4),
-        // each row spread over the 4 threads q4 = lane % 4 (tcgen05.ld 16x256b layout).
+        // r0 + rs and r0 + rs + 8 of the tile (r0 = 32 (w % 4) + 16 (w / 4), rs = lane / 4).
         const int tid = threadIdx.x;              // 0..255
         const int r0 = 32 * (warp & 3) + 16 * (warp >> 2);
         const uint32_t lanes = uint32_t(r0) << 16;
@@ -700,101 +900,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int ob = ic & 1;
             const uint32_t tm_o = tmem + kTmemO + ob * 128 + lanes;
             const bool on = r0 < I.rows_valid;    // warp-uniform: the warp holds a valid row
-            int pos[2];
-            float m_run[2], l_run[2];
-#pragma unroll
-            for (int sr = 0; sr < 2; ++sr) {
-                const int row = r0 + rs + 8 * sr;
-                pos[sr] = row < I.rows_valid ? I.pos0 + row / p.g : -1;
-                m_run[sr] = -INFINITY;
-                l_run[sr] = 0.f;
-            }
+            Rows2 R;
+            rows_init(R, r0, rs, I.rows_valid, I.pos0, p.g);
             for (int jt = 0; jt < I.n_tiles; ++jt, ++tc) {
                 if (!(ok = wait_bounded(bar(kSFull + (tc & 1)), (tc >> 1) & 1, abort_word)))
                     break;
                 tc_fence_after();
                 const int kb = I.k_begin + jt * kTileKeys;
-                const uint32_t tm_s = tmem + (tc & 1) * 128 + lanes;
                 float alpha[2] = {1.f, 1.f};
-                if (on) {
-                    uint32_t r[64];
-                    tmem_ld_16x256b_x16(tm_s, r);
-                    tmem_wait_ld();
-                    uint32_t pk[32];                 // P rounded to bf16, packed in pairs
-#pragma unroll
-                    for (int sr = 0; sr < 2; ++sr) {
-                        // an 8-row block with no valid row (the tail of a decode or a ragged
-                        // tile) needs no softmax: its P is never used for a written output
-                        if (r0 + 8 * sr >= I.rows_valid) {
-#pragma unroll
-                            for (int cc = 0; cc < 16; ++cc) pk[2 * cc + sr] = 0u;
-                            continue;
-                        }
-                        const int pr = pos[sr];
-                        // the causal / ctx mask matters only when some key of the tile lies past
-                        // some row of this block
-                        const bool full = __all_sync(0xffffffffu, kb + kTileKeys - 1 <= pr);
-                        float sv[32];
-                        float mx = -INFINITY;
-                        if (full) {
-#pragma unroll
-                            for (int cc = 0; cc < 16; ++cc)
-#pragma unroll
-                                for (int e = 0; e < 2; ++e) {
-                                    const float sc = __uint_as_float(r[4 * cc + 2 * sr + e]);
-                                    sv[2 * cc + e] = sc;
-                                    mx = fmaxf(mx, sc);
-                                }
-                        } else {
-#pragma unroll
-                            for (int cc = 0; cc < 16; ++cc)
-#pragma unroll
-                                for (int e = 0; e < 2; ++e) {
-                                    const int key = kb + 8 * cc + 2 * q4 + e;
-                                    const float sc = key <= pr ? __uint_as_float(r[4 * cc + 2 * sr + e])
-                                                               : -INFINITY;
-                                    sv[2 * cc + e] = sc;
-                                    mx = fmaxf(mx, sc);
-                                }
-                        }
-                        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-                        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-                        // The reference maximum moves only when the row's maximum grows past it by
-                        // more than 8 in base-2 units, so P <= 2^8 and O needs rescaling rarely;
-                        // the decision depends on the row's own scores alone.
-                        const float m_old = m_run[sr];
-                        const float m_new = fmaxf(m_old, mx);
-                        const bool move = m_old == -INFINITY
-                                              ? m_new != -INFINITY
-                                              : __fmul_rn(__fsub_rn(m_new, m_old), c) > kLazyLog2;
-                        const float m_ref = move ? m_new : m_old;
-                        const float m_use = m_ref == -INFINITY ? 0.f : m_ref;
-                        // A row that has not seen a key yet (a padding row of the block, or a
-                        // row whose position precedes this split) has O = 0 and l = 0: its
-                        // factor stays 1 so that it never asks for a rescale of O.
-                        const float a = (m_old == m_use || m_ref == -INFINITY)
-                                            ? 1.f
-                                            : ex2(__fmul_rn(__fsub_rn(m_old, m_use), c));
-                        const float nmc = __fmul_rn(-m_use, c);
-                        float sum = 0.f;
-#pragma unroll
-                        for (int i = 0; i < 32; ++i) {
-                            sv[i] = ex2(__fmaf_rn(sv[i], c, nmc));
-                            sum = __fadd_rn(sum, sv[i]);
-                        }
-                        sum = __fadd_rn(sum, __shfl_xor_sync(0xffffffffu, sum, 1));
-                        sum = __fadd_rn(sum, __shfl_xor_sync(0xffffffffu, sum, 2));
-                        l_run[sr] = __fadd_rn(__fmul_rn(l_run[sr], a), sum);
-                        m_run[sr] = m_ref;
-                        alpha[sr] = a;
-                        // keys 8cc + 2q4 + {0, 1} -> packed column 4cc + q4 (16x128b layout)
-#pragma unroll
-                        for (int cc = 0; cc < 16; ++cc)
-                            pk[2 * cc + sr] = pack_bf16(sv[2 * cc], sv[2 * cc + 1]);
-                    }
-                    // P replaces S in the first 64 columns of this tile's S buffer
-                    tmem_st_16x128b_x16(tm_s, pk);
-                }
+                if (on) softmax_half(tmem + (tc & 1) * 128 + lanes, r0, q4, I.rows_valid, kb, c, R, alpha);
                 // O belongs to the previous tile's PV until it has finished: rescale only then,
                 // and only in warps where some row's running maximum moved
                 const bool need = alpha[0] != 1.f || alpha[1] != 1.f;
@@ -803,21 +917,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                             abort_word)))
                         break;
                     tc_fence_after();
-                    uint32_t o[D / 2];
-                    if constexpr (D == 128) tmem_ld_16x256b_x16(tm_o, o);
-                    else tmem_ld_16x256b_x8(tm_o, o);
-                    tmem_wait_ld();
-#pragma unroll
-                    for (int cc = 0; cc < D / 8; ++cc)
-#pragma unroll
-                        for (int sr = 0; sr < 2; ++sr)
-#pragma unroll
-                            for (int e = 0; e < 2; ++e) {
-                                const int k = 4 * cc + 2 * sr + e;
-                                o[k] = __float_as_uint(__fmul_rn(__uint_as_float(o[k]), alpha[sr]));
-                            }
-                    if constexpr (D == 128) tmem_st_16x256b_x16(tm_o, o);
-                    else tmem_st_16x256b_x8(tm_o, o);
+                    rescale_half<D>(tm_o, alpha);
                 }
                 tmem_wait_st();
                 // keys at or beyond ctx are stale or were never loaded: give them zero values
@@ -825,16 +925,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (kb + kTileKeys > I.ctx) {
                     if (!(ok = wait_bounded(bar(kVFull + tc % SV), (tc / SV) & 1, abort_word)))
                         break;
-                    const int z0 = max(I.ctx - kb, 0);
-                    const int nrow = kTileKeys - z0;
-                    const uint32_t vb = sb + L::kV + (tc % SV) * L::kKVTile;
-                    for (int i = tid; i < nrow * 8 * L::kChunks; i += 256) {
-                        const int hh = i / (nrow * 8);
-                        const int rem = i % (nrow * 8);
-                        const int key = z0 + rem / 8;
-                        st_shared_zero16(vb + (key / p.bs) * (p.bs * 128 * L::kChunks) +
-                                         hh * (p.bs * 128) + (key % p.bs) * 128 + (rem % 8) * 16);
-                    }
+                    zero_v_tail<D>(sb + L::kV + (tc % SV) * L::kKVTile, kb, I.ctx, p.bs, tid, 256);
                 }
                 fence_proxy_async();
                 tc_fence_before();
@@ -855,37 +946,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tmem_wait_ld();
                 tc_fence_before();
                 mbar_arrive(bar(kOFree + ob));       // O is in registers: its buffer is free
-#pragma unroll
-                for (int sr = 0; sr < 2; ++sr) {
-                    const int row = r0 + rs + 8 * sr;
-                    if (row >= I.rows_valid) continue;
-                    const int pr = pos[sr];
-                    const int nsp = pr / kSplit + 1;
-                    if (I.split >= nsp) continue;        // the row has no keys in this split
-                    const int tok = I.q_start + row / p.g;
-                    const int head = I.kvh * p.g + row % p.g;
-                    if (nsp == 1) {
-                        const float inv = __frcp_rn(l_run[sr]);
-                        __nv_bfloat16* dst = p.out + (int64_t(tok) * p.Hq + head) * D;
-#pragma unroll
-                        for (int cc = 0; cc < D / 8; ++cc) {
-                            const float x0 = __fmul_rn(__uint_as_float(o[4 * cc + 2 * sr]), inv);
-                            const float x1 = __fmul_rn(__uint_as_float(o[4 * cc + 2 * sr + 1]), inv);
-                            *reinterpret_cast<uint32_t*>(dst + 8 * cc + 2 * q4) = pack_bf16(x0, x1);
-                        }
-                    } else {
-                        const int64_t slot = (int64_t(tok) * p.max_splits + I.split) * p.Hq + head;
-                        float* acc = p.ws_acc + slot * D;
-#pragma unroll
-                        for (int cc = 0; cc < D / 8; ++cc)
-                            *reinterpret_cast<float2*>(acc + 8 * cc + 2 * q4) =
-                                make_float2(__uint_as_float(o[4 * cc + 2 * sr]),
-                                            __uint_as_float(o[4 * cc + 2 * sr + 1]));
-                        if (q4 == 0)
-                            *reinterpret_cast<float2*>(p.ws_ml + slot * 2) =
-                                make_float2(m_run[sr], l_run[sr]);
-                    }
-                }
+                store_half<D>(p, o, r0, rs, q4, I.rows_valid, I.q_start, I.kvh, I.split, R);
             }
             ++ic;
         }
@@ -1075,8 +1136,9 @@ int32_t launch(const Maps& maps, const Params& prm, int32_t max_ctx, cudaStream_
     int32_t st = note_cuda(cudaGetDevice(&dev));
     if (st) return st;
     if (attr_device != dev) {
-        st = note_cuda(cudaFuncSetAttribute(
-            paged_attn_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, Layout<D>::kAlloc));
+        st = note_cuda(cudaFuncSetAttribute(paged_attn_kernel<D>,
+                                            cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                            Layout<D>::kAlloc));
         if (st) return st;
         attr_device = dev;
     }
