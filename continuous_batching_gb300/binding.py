@@ -328,19 +328,49 @@ def paged_attention_step(q, k_pool, v_pool, block_table, cu_seqlens_q, ctx_lens,
         "paged_attention_step")
 
 
+class StepLimits:
+    """Fixed sizes of a step that is captured in a CUDA graph: B sequences, T query rows,
+    block-table width max_blocks and a context bound max_ctx. Every step prepared under these
+    limits reuses the same device buffers and launches the same kernels with the same
+    arguments, so a graph captured once replays any of them."""
+
+    def __init__(self, B: int, T: int, max_blocks: int, max_ctx: int):
+        self.B, self.T, self.max_blocks, self.max_ctx = int(B), int(T), int(max_blocks), int(max_ctx)
+
+
 class StepRunner:
     """One layer's step on the device: holds the plan buffers and workspace, runs
     paged_kv_write then paged_attention_step on the current stream.
 
-    prepare() takes host metadata (the plan is computed on the host); run() launches."""
+    prepare() takes host metadata (the plan is computed on the host); run() launches.
+    With limits (StepLimits), prepare() writes the metadata into fixed device buffers in place
+    (the plan padded to a fixed item count with n_q == 0 items, the table padded with -1), so
+    capture() can record run() once in a CUDA graph and replay() runs any later prepared step.
+    """
 
-    def __init__(self, shape: Shape, device="cuda"):
+    def __init__(self, shape: Shape, device="cuda", limits: Optional[StepLimits] = None):
         import torch
         self.torch = torch
         self.shape = shape
         self.device = torch.device(device)
+        self.limits = limits
         self.ws = None
+        self.graph = None
         self.err = torch.zeros(1, dtype=torch.int32, device=self.device)
+        if limits is not None:
+            L = limits
+            d = self.device
+            cap = int(load().pa_plan_max_items(C.byref(shape), L.B, L.T, L.max_ctx))
+            self.n_items_cap = max(cap, 1)
+            self.items = torch.zeros(self.n_items_cap * 8, dtype=torch.int32, device=d)
+            self.cu = torch.zeros(L.B + 1, dtype=torch.int32, device=d)
+            self.ctx = torch.zeros(L.B, dtype=torch.int32, device=d)
+            self.table = torch.full((L.B, L.max_blocks), -1, dtype=torch.int32, device=d)
+            self.slots = torch.full((L.T,), -1, dtype=torch.int32, device=d)
+            self.max_ctx = L.max_ctx
+            self.T = L.T
+            need = pa_workspace_bytes(shape, L.T, L.max_ctx)
+            self.ws = torch.empty((need + 3) // 4, dtype=torch.float32, device=d)
 
     def prepare(self, cu_seqlens_q: np.ndarray, ctx_lens: np.ndarray, block_table: np.ndarray,
                 slot_mapping: Optional[np.ndarray] = None):
@@ -349,10 +379,30 @@ class StepRunner:
         items = pa_plan_step(self.shape, cu, ctx)
         if slot_mapping is None:
             slot_mapping = pa_compute_slots(self.shape, block_table, cu, ctx)
+        self.h_items = items
+        d = self.device
+        if self.limits is not None:
+            L = self.limits
+            B = len(ctx)
+            T = int(cu[-1]) if B else 0
+            table = _i32(block_table)
+            if B != L.B or T != L.T or table.shape[1] > L.max_blocks or \
+                    (B and int(ctx.max()) > L.max_ctx) or len(items) > self.n_items_cap:
+                raise ValueError("step exceeds the limits the runner was built for")
+            padded = np.zeros(self.n_items_cap, dtype=WORK_ITEM_DTYPE)   # n_q == 0: padding
+            padded[:len(items)] = items
+            tab = np.full((L.B, L.max_blocks), -1, dtype=np.int32)
+            tab[:, :table.shape[1]] = table
+            non_blocking = True
+            self.items.copy_(torch.from_numpy(padded.view(np.int32).reshape(-1)),
+                             non_blocking=non_blocking)
+            self.cu.copy_(torch.from_numpy(cu), non_blocking=non_blocking)
+            self.ctx.copy_(torch.from_numpy(ctx), non_blocking=non_blocking)
+            self.table.copy_(torch.from_numpy(tab), non_blocking=non_blocking)
+            self.slots.copy_(torch.from_numpy(_i32(slot_mapping)), non_blocking=non_blocking)
+            return self
         self.max_ctx = int(ctx.max()) if len(ctx) else 0
         self.T = int(cu[-1]) if len(ctx) else 0
-        d = self.device
-        self.h_items = items
         self.items = torch.from_numpy(items.view(np.int32).reshape(-1).copy()).to(d)
         self.cu = torch.from_numpy(cu.copy()).to(d)
         self.ctx = torch.from_numpy(ctx.copy()).to(d)
@@ -362,6 +412,33 @@ class StepRunner:
         if self.ws is None or self.ws.numel() * 4 < need:
             self.ws = torch.empty((need + 3) // 4, dtype=torch.float32, device=d)
         return self
+
+    def capture(self, q, k_new, v_new, k_pool, v_pool, out, write: bool = True,
+                attend: bool = True):
+        """Records run() (or only its write or attention part) in a CUDA graph. Needs limits;
+        the tensors passed here are the ones every replay reads and writes."""
+        torch = self.torch
+        if self.limits is None:
+            raise ValueError("capture needs a runner built with StepLimits")
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):              # warm-up outside the graph
+            if write:
+                self.write(k_new, v_new, k_pool, v_pool)
+            if attend:
+                self.attend(q, k_pool, v_pool, out)
+        torch.cuda.current_stream().wait_stream(side)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            if write:
+                self.write(k_new, v_new, k_pool, v_pool)
+            if attend:
+                self.attend(q, k_pool, v_pool, out)
+        self.graph = graph
+        return graph
+
+    def replay(self):
+        self.graph.replay()
 
     def write(self, k_new, v_new, k_pool, v_pool, stream=None):
         paged_kv_write(k_new, v_new, self.slots, k_pool, v_pool, self.shape, self.err, stream)

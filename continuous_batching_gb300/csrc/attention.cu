@@ -615,6 +615,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int x = (round & 1) ? G - 1 - int(blockIdx.x) : int(blockIdx.x);
                 const int64_t idx = int64_t(round) * G + x;
                 if (idx >= p.n_items) continue;           // a hole in the last, partial round
+                // an item with n_q == 0 is padding (a plan padded to a fixed item count, so
+                // that a captured step can be replayed with new metadata); padding follows all
+                // real items, so every later round of this CTA is padding too
+                if (p.items[idx].n_q == 0) {
+                    round = int((int64_t(p.n_items) + G - 1) / G);
+                    break;
+                }
                 I = load_item(p, int(idx));
                 if (I.good) {
                     have = true;

@@ -79,7 +79,11 @@ typedef struct pa_shape {
 
 /* One unit of attention work: query rows [q_start, q_start + n_q) of sequence `seq`, one KV
  * head, one KV split. Produced by pa_plan_step on the host; copied to the device by the
- * caller and passed to paged_attention_step. */
+ * caller and passed to paged_attention_step. An item with n_q == 0 is padding and is skipped
+ * without error; padding must follow every real item (the kernel stops at the first one). A
+ * caller that captures a step in a CUDA graph pads every plan at its end to one fixed item
+ * count (pa_plan_max_items for its limits) and rewrites the device buffers in place before
+ * each replay. */
 typedef struct pa_work_item {
     int32_t seq;        /* index into cu_seqlens_q / ctx_lens / block_table rows */
     int32_t q_start;    /* first query row (token index into q and out) */

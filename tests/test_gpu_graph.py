@@ -1,0 +1,97 @@
+"""A step captured once in a CUDA graph and replayed with new metadata gives the same bits as
+the same steps launched directly ("Finish RL Training Faster: Bitwise-Consistent,
+High-Performance, Agent-Driven", section 4.6: decode runs under CUDA graphs and stays
+bitwise consistent). The metadata of every step goes into fixed device buffers (plan padded
+with n_q == 0 items, table padded with -1) and the graph reads them at replay."""
+import numpy as np
+import pytest
+
+from continuous_batching_gb300 import binding as bd
+from continuous_batching_gb300 import workloads as wl
+from tests.gpu_util import bf16_dev, shape_of
+
+pytestmark = pytest.mark.gpu
+torch = pytest.importorskip("torch")
+if not torch.cuda.is_available():
+    pytest.skip("no CUDA device", allow_module_level=True)
+
+
+@pytest.fixture(scope="module", autouse=True)
+def lib():
+    from continuous_batching_gb300 import build
+    build.build()
+    return bd.load()
+
+
+def _steps(B=24, Hq=32, Hkv=8, D=128, bs=16, seed=21):
+    """Two consecutive decode steps of the same B sequences: step 2 has one more token per
+    sequence. Tables cover the longer context from the start; the pool is shared."""
+    rng = np.random.default_rng(seed)
+    ctx2 = rng.integers(100, 5000, size=B).astype(np.int32)
+    full = wl.make_step(Hq, Hkv, D, bs, ctx2, np.ones(B, np.int32), seed=seed)
+    step1, _ = wl.subset(full, range(B), name="step1")
+    step1.ctx_lens = (ctx2 - 1).astype(np.int32)
+    step1.q = wl.random_bf16(rng, step1.q.shape)
+    step1.k_new = wl.random_bf16(rng, step1.k_new.shape)
+    step1.v_new = wl.random_bf16(rng, step1.v_new.shape)
+    return step1, full
+
+
+def _eager(st, kp, vp, q, kn, vn):
+    r = bd.StepRunner(shape_of(st)).prepare(st.cu_seqlens_q, st.ctx_lens, st.block_table)
+    out = torch.empty((st.T, st.Hq, st.D), dtype=torch.bfloat16, device="cuda")
+    r.run(q, kn, vn, kp, vp, out)
+    torch.cuda.synchronize()
+    assert r.device_error() == 0
+    return out.view(torch.int16).cpu().numpy()
+
+
+def test_captured_decode_step_replays_new_metadata_bitwise():
+    step1, step2 = _steps()
+    kp, vp = bf16_dev(step2.k_pool, torch), bf16_dev(step2.v_pool, torch)
+    lim = bd.StepLimits(B=step2.B, T=step2.T, max_blocks=step2.block_table.shape[1],
+                        max_ctx=8192)
+    runner = bd.StepRunner(shape_of(step2), limits=lim)
+    q = torch.empty((step2.T, step2.Hq, step2.D), dtype=torch.bfloat16, device="cuda")
+    kn = torch.empty((step2.T, step2.Hkv, step2.D), dtype=torch.bfloat16, device="cuda")
+    vn = torch.empty_like(kn)
+    out = torch.empty_like(q)
+    runner.prepare(step1.cu_seqlens_q, step1.ctx_lens, step1.block_table)
+    runner.capture(q, kn, vn, kp, vp, out)
+    for st in (step1, step2, step1):
+        # new inputs and metadata into the captured buffers, then one replay
+        q.copy_(bf16_dev(st.q, torch))
+        kn.copy_(bf16_dev(st.k_new, torch))
+        vn.copy_(bf16_dev(st.v_new, torch))
+        runner.prepare(st.cu_seqlens_q, st.ctx_lens, st.block_table)
+        runner.replay()
+        torch.cuda.synchronize()
+        got = out.view(torch.int16).cpu().numpy()
+        want = _eager(st, kp, vp, bf16_dev(st.q, torch), bf16_dev(st.k_new, torch),
+                      bf16_dev(st.v_new, torch))
+        assert runner.device_error() == 0
+        assert np.array_equal(got, want)
+
+
+def test_captured_mixed_step_equals_direct_launch():
+    st = wl.make_step(32, 8, 128, 16, [300, 1800, 2500, 640], [1, 1, 200, 37], seed=22)
+    kp, vp = bf16_dev(st.k_pool, torch), bf16_dev(st.v_pool, torch)
+    lim = bd.StepLimits(B=st.B, T=st.T, max_blocks=st.block_table.shape[1] + 3, max_ctx=4096)
+    runner = bd.StepRunner(shape_of(st), limits=lim)
+    q, kn, vn = bf16_dev(st.q, torch), bf16_dev(st.k_new, torch), bf16_dev(st.v_new, torch)
+    out = torch.empty((st.T, st.Hq, st.D), dtype=torch.bfloat16, device="cuda")
+    runner.prepare(st.cu_seqlens_q, st.ctx_lens, st.block_table)
+    runner.capture(q, kn, vn, kp, vp, out)
+    runner.replay()
+    torch.cuda.synchronize()
+    got = out.view(torch.int16).cpu().numpy()
+    assert runner.device_error() == 0
+    assert np.array_equal(got, _eager(st, kp, vp, q, kn, vn))
+
+
+def test_limits_are_enforced_on_the_host():
+    st = wl.make_step(8, 2, 64, 16, [40, 50], [1, 1], seed=23)
+    lim = bd.StepLimits(B=2, T=2, max_blocks=st.block_table.shape[1], max_ctx=45)
+    runner = bd.StepRunner(shape_of(st), limits=lim)
+    with pytest.raises(ValueError):
+        runner.prepare(st.cu_seqlens_q, st.ctx_lens, st.block_table)    # ctx 50 > 45
