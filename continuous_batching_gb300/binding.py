@@ -109,6 +109,20 @@ def load() -> C.CDLL:
         _sig(lib, "pa_alloc_slots", C.c_int32, [ap, C.c_int32, C.c_int32, C.c_int32, _i32p])
         _sig(lib, "pa_alloc_build_step", C.c_int32,
              [ap, _i32p, _i32p, _i32p, C.c_int32, _i32p, _i32p, _i32p, C.c_int32])
+        _sig(lib, "pa_alloc_trim", C.c_int32, [ap, C.c_int32, C.c_int32])
+        _sig(lib, "pa_alloc_fork", C.c_int32, [ap, C.c_int32, C.c_int32])
+        _sig(lib, "pa_alloc_cow", C.c_int32,
+             [ap, C.c_int32, C.c_int32, C.c_int32, _i32p, C.c_int32, _i32p])
+        sc = C.c_void_p                  # pa_scheduler*
+        _sig(lib, "pa_sched_create", C.c_int32,
+             [C.c_int32, C.c_int32, C.c_int32, C.c_int32, C.POINTER(sc)])
+        _sig(lib, "pa_sched_destroy", C.c_int32, [sc])
+        _sig(lib, "pa_sched_allocator", ap, [sc])
+        _sig(lib, "pa_sched_add", C.c_int32, [sc, C.c_int32, C.c_int32, C.c_int32, C.c_int32])
+        _sig(lib, "pa_sched_step", C.c_int32, [sc, _i32p, _i32p, _i32p, C.c_int32, _i32p])
+        _sig(lib, "pa_sched_commit", C.c_int32, [sc, _i32p, C.c_int32, _i32p])
+        _sig(lib, "pa_sched_counts", C.c_int32, [sc, _i32p, _i32p, C.POINTER(C.c_int64)])
+        _sig(lib, "pa_sched_seq", C.c_int32, [sc, C.c_int32, _i32p, _i32p, _i32p])
         _sig(lib, "pa_compute_slots", C.c_int32,
              [sp, _i32p, C.c_int32, C.c_int32, _i32p, _i32p, _i32p])
         _sig(lib, "pa_plan_max_items", C.c_int64, [sp, C.c_int32, C.c_int32, C.c_int32])
@@ -119,6 +133,7 @@ def load() -> C.CDLL:
              [sp, _i32p, _vp, C.c_int32, C.c_int32, _vp])
         _sig(lib, "paged_kv_write", C.c_int32,
              [_vp, _vp, _vp, C.c_int32, _vp, _vp, sp, _vp, _vp])
+        _sig(lib, "paged_copy_blocks", C.c_int32, [_vp, C.c_int32, _vp, _vp, sp, _vp, _vp])
         _sig(lib, "paged_attention_step", C.c_int32,
              [_vp, _vp, _vp, _vp, C.c_int32, _vp, _vp, C.c_int32, C.c_int32, C.c_int32,
               _vp, C.c_int32, _vp, C.c_size_t, _vp, sp, _vp, _vp])
@@ -182,21 +197,26 @@ def pa_device_sm_count() -> int:
 # ---------------------------------------------------------------------- host allocator
 
 class Allocator:
-    """Owns a pa_allocator (LIFO blocks, refcounts, read-only shared prefix blocks)."""
+    """A pa_allocator (LIFO blocks, refcounts, read-only shared prefix blocks): owned, or
+    borrowed from a Scheduler (then the scheduler frees it)."""
 
-    def __init__(self, num_blocks: int, block_size: int):
+    def __init__(self, num_blocks: int, block_size: int, _borrow=None):
         self._lib = load()
+        self.num_blocks = int(num_blocks)
+        self.block_size = int(block_size)
+        self._owned = _borrow is None
+        if _borrow is not None:
+            self._h = _borrow
+            return
         h = C.c_void_p()
         _check(self._lib.pa_alloc_create(int(num_blocks), int(block_size), C.byref(h)),
                "pa_alloc_create")
         self._h = h
-        self.num_blocks = int(num_blocks)
-        self.block_size = int(block_size)
 
     def close(self):
-        if getattr(self, "_h", None):
+        if getattr(self, "_h", None) and getattr(self, "_owned", False):
             self._lib.pa_alloc_destroy(self._h)
-            self._h = None
+        self._h = None
 
     __del__ = close
 
@@ -248,6 +268,21 @@ class Allocator:
                "pa_alloc_slots")
         return out[:n].tolist()
 
+    def trim(self, seq: int, n_tokens: int) -> None:
+        _check(self._lib.pa_alloc_trim(self._h, int(seq), int(n_tokens)), "pa_alloc_trim")
+
+    def fork(self, src: int, dst: int) -> None:
+        _check(self._lib.pa_alloc_fork(self._h, int(src), int(dst)), "pa_alloc_fork")
+
+    def cow(self, seq: int, start: int, n: int) -> list:
+        """Private blocks for positions start..start+n-1; returns [(old, new)] block copies."""
+        cap = max(n // self.block_size + 2, 1)
+        pairs = np.empty(2 * cap, np.int32)
+        k = C.c_int32()
+        _check(self._lib.pa_alloc_cow(self._h, int(seq), int(start), int(n), _p32(pairs), cap,
+                                      C.byref(k)), "pa_alloc_cow")
+        return [(int(pairs[2 * i]), int(pairs[2 * i + 1])) for i in range(k.value)]
+
     def build_step(self, seqs, ctx_lens, n_new, max_blocks: int):
         """Returns (cu_seqlens_q, slot_mapping, block_table) host arrays for one step."""
         seqs, ctx_lens, n_new = _i32(seqs), _i32(ctx_lens), _i32(n_new)
@@ -260,6 +295,65 @@ class Allocator:
                                              _p32(cu), _p32(slots), _p32(table), int(max_blocks)),
                "pa_alloc_build_step")
         return cu, slots[:T], table[:B]
+
+
+class Scheduler:
+    """Owns a pa_scheduler: requests in, flat ragged steps out (see pagedattn.h)."""
+
+    def __init__(self, num_blocks: int, block_size: int, chunk: int, budget: int):
+        self._lib = load()
+        h = C.c_void_p()
+        _check(self._lib.pa_sched_create(int(num_blocks), int(block_size), int(chunk),
+                                         int(budget), C.byref(h)), "pa_sched_create")
+        self._h = h
+        self._live = 0
+        self.block_size = int(block_size)
+        self.allocator = Allocator(num_blocks, block_size,
+                                   _borrow=C.c_void_p(self._lib.pa_sched_allocator(h)))
+
+    def close(self):
+        if getattr(self, "_h", None):
+            self.allocator._h = None
+            self._lib.pa_sched_destroy(self._h)
+            self._h = None
+
+    __del__ = close
+
+    def add(self, seq: int, prompt_len: int, max_new: int, leader: Optional[int] = None):
+        _check(self._lib.pa_sched_add(self._h, int(seq), int(prompt_len), int(max_new),
+                                      -1 if leader is None else int(leader)), "pa_sched_add")
+        self._live += 1
+
+    def step(self):
+        """[(seq, n_new, ctx)] in step order."""
+        cap = max(self._live, 1)
+        seqs, n_new, ctx = (np.empty(cap, np.int32) for _ in range(3))
+        n = C.c_int32()
+        _check(self._lib.pa_sched_step(self._h, _p32(seqs), _p32(n_new), _p32(ctx), cap,
+                                       C.byref(n)), "pa_sched_step")
+        k = n.value
+        return list(zip(seqs[:k].tolist(), n_new[:k].tolist(), ctx[:k].tolist()))
+
+    def commit(self) -> list:
+        cap = max(self._live, 1)
+        fin = np.empty(cap, np.int32)
+        n = C.c_int32()
+        _check(self._lib.pa_sched_commit(self._h, _p32(fin), cap, C.byref(n)), "pa_sched_commit")
+        self._live -= n.value
+        return fin[:n.value].tolist()
+
+    def counts(self):
+        w, r, p = C.c_int32(), C.c_int32(), C.c_int64()
+        _check(self._lib.pa_sched_counts(self._h, C.byref(w), C.byref(r), C.byref(p)),
+               "pa_sched_counts")
+        return int(w.value), int(r.value), int(p.value)
+
+    def seq(self, q: int):
+        """(n_tokens, num_computed, generated) of sequence q."""
+        a, b, c = C.c_int32(), C.c_int32(), C.c_int32()
+        _check(self._lib.pa_sched_seq(self._h, int(q), C.byref(a), C.byref(b), C.byref(c)),
+               "pa_sched_seq")
+        return int(a.value), int(b.value), int(c.value)
 
 
 # ------------------------------------------------------------------ host step metadata
@@ -305,6 +399,14 @@ def pa_upload_block_table(shape: Shape, host: np.ndarray, dev, stream=None) -> N
 
 
 # ------------------------------------------------------------------------- device step
+
+def paged_copy_blocks(pairs, k_pool, v_pool, shape: Shape, err=None, stream=None) -> None:
+    """pairs: device int32 tensor [2 * n] of (old, new) block ids from Allocator.cow."""
+    n = int(pairs.numel() // 2)
+    _check(load().paged_copy_blocks(_dev(pairs) if n else None, n, _dev(k_pool), _dev(v_pool),
+                                    C.byref(shape), _dev(err), _stream(stream)),
+           "paged_copy_blocks")
+
 
 def paged_kv_write(k_new, v_new, slot_mapping, k_pool, v_pool, shape: Shape, err=None,
                    stream=None) -> None:

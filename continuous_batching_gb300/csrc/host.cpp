@@ -210,6 +210,64 @@ int32_t pa_alloc_free_seq(pa_allocator* a, int32_t seq) {
     return PA_OK;
 }
 
+int32_t pa_alloc_trim(pa_allocator* a, int32_t seq, int32_t n_tokens) {
+    if (!a || n_tokens < 0) return PA_ERR_INVALID;
+    auto it = a->tables.find(seq);
+    if (it == a->tables.end()) return PA_ERR_STATE;
+    std::vector<int32_t>& t = it->second;
+    const int64_t keep = blocks_for(n_tokens, a->block_size);
+    if (keep > int64_t(t.size())) return PA_ERR_BOUNDS;
+    // the tail goes back last block first, so the block next to the kept part is reused first
+    while (int64_t(t.size()) > keep) {
+        const int32_t st = pa_alloc_free_block(a, t.back());
+        if (st) return st;
+        t.pop_back();
+    }
+    return PA_OK;
+}
+
+int32_t pa_alloc_fork(pa_allocator* a, int32_t src, int32_t dst) {
+    if (!a || dst < 0) return PA_ERR_INVALID;
+    if (a->tables.count(dst)) return PA_ERR_STATE;
+    auto it = a->tables.find(src);
+    if (it == a->tables.end()) return PA_ERR_STATE;
+    for (int32_t b : it->second) a->ref[b] += 1;
+    std::vector<int32_t> copy = it->second;
+    a->tables.emplace(dst, std::move(copy));
+    return PA_OK;
+}
+
+int32_t pa_alloc_cow(pa_allocator* a, int32_t seq, int32_t start, int32_t n, int32_t* pairs,
+                     int32_t max_pairs, int32_t* n_pairs) {
+    if (!a || !n_pairs || n < 0 || start < 0 || max_pairs < 0) return PA_ERR_INVALID;
+    auto it = a->tables.find(seq);
+    if (it == a->tables.end()) return PA_ERR_STATE;
+    std::vector<int32_t>& t = it->second;
+    *n_pairs = 0;
+    if (n == 0) return PA_OK;
+    const int64_t first = int64_t(start) / a->block_size;
+    const int64_t last = (int64_t(start) + n - 1) / a->block_size;
+    if (last >= int64_t(t.size())) return PA_ERR_BOUNDS;
+    int32_t shared = 0;
+    for (int64_t j = first; j <= last; ++j) shared += a->ref[t[j]] > 1;
+    if (shared > max_pairs || (shared > 0 && !pairs)) return PA_ERR_INVALID;
+    if (shared > int32_t(a->free_stack.size())) return PA_ERR_OOM;
+    int32_t k = 0;
+    for (int64_t j = first; j <= last; ++j) {
+        if (a->ref[t[j]] <= 1) continue;
+        int32_t fresh;
+        pa_alloc_block(a, &fresh);
+        const int32_t old = t[j];
+        a->ref[old] -= 1;                 // this table's reference only: still > 0
+        t[j] = fresh;
+        pairs[2 * k] = old;
+        pairs[2 * k + 1] = fresh;
+        ++k;
+    }
+    *n_pairs = k;
+    return PA_OK;
+}
+
 int32_t pa_alloc_check_consistent(const pa_allocator* a) {
     if (!a) return PA_ERR_INVALID;
     std::vector<uint8_t> on_free(a->num_blocks, 0);

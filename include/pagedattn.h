@@ -141,6 +141,28 @@ int32_t pa_alloc_admit(pa_allocator* a, int32_t seq, int32_t n_tokens, int32_t s
 int32_t pa_alloc_ensure_capacity(pa_allocator* a, int32_t seq, int32_t n_tokens);
 /* Releases every block of seq's table and forgets seq. */
 int32_t pa_alloc_free_seq(pa_allocator* a, int32_t seq);
+/* Rollback ("Optional paged KV cache (vLLM-style) - v1 design", Design: trim(n) rewinds the
+ * offset and frees the now-unoccupied tail blocks; stale bytes past the offset are never
+ * read). Keeps the ceil(n_tokens / block_size) leading blocks of seq and releases the rest,
+ * last block first (a block shared with another table only loses this table's reference).
+ * PA_ERR_BOUNDS if n_tokens needs more blocks than the table holds; nothing changes then. */
+int32_t pa_alloc_trim(pa_allocator* a, int32_t seq, int32_t n_tokens);
+
+/* Copy-on-write fork (same page, "Block-level CoW prefix sharing": refcounted block tables,
+ * fork on divergent write). dst (a new id) gets every block of src, the partial last block
+ * included; every block's refcount goes up by one. */
+int32_t pa_alloc_fork(pa_allocator* a, int32_t src, int32_t dst);
+
+/* Before seq writes positions [start, start + n): every block holding one of them that is
+ * referenced by more than one table is replaced, in table order, by a fresh block, and the
+ * (old, new) pairs are returned in pairs[2 * k], pairs[2 * k + 1] (host, up to max_pairs
+ * pairs, count in *n_pairs). The caller copies each old block to its new block on the device
+ * (paged_copy_blocks) before the write. All or nothing: PA_ERR_OOM if the pool cannot supply
+ * every replacement, PA_ERR_INVALID if max_pairs is too small, PA_ERR_BOUNDS past the table;
+ * nothing changes then. */
+int32_t pa_alloc_cow(pa_allocator* a, int32_t seq, int32_t start, int32_t n, int32_t* pairs,
+                     int32_t max_pairs, int32_t* n_pairs);
+
 /* PA_OK if free + referenced == total, the free list has no duplicates and every refcount
  * equals the references held by live tables; PA_ERR_INCONSISTENT otherwise. */
 int32_t pa_alloc_check_consistent(const pa_allocator* a);
@@ -164,6 +186,52 @@ int32_t pa_alloc_build_step(const pa_allocator* a, const int32_t* seqs, const in
                             int32_t* slot_mapping, int32_t* block_table, int32_t max_blocks);
 
 /* ------------------------------------------------------- host step metadata -------- */
+
+/* ------------------------------------------------------------ host step scheduler --- */
+/* "P3: native paged-KV continuous-batching sampler", Design / engine.py (Scheduler,
+ * Admit/evict, Prefix sharing). The scheduler owns a block allocator and turns requests
+ * (prompt length, tokens to generate, optional prefix leader) into flat ragged steps:
+ *   - a step schedules n_new = min(remaining, chunk, budget) per sequence, remaining being
+ *     tokens not yet in the cache; decodes (remaining 1) come first, then the other running
+ *     sequences, each in admission order, then waiting sequences are admitted in FIFO order
+ *     while budget remains (admission reserves blocks for the whole current token list and
+ *     stops at the first request that does not fit or defers);
+ *   - when a running sequence cannot grow, the youngest running sequence not yet scheduled in
+ *     the step is preempted by recompute (blocks freed, num_computed = 0, back to the head of
+ *     the waiting queue); with no such sequence the one being scheduled sits the step out;
+ *   - a request with a leader shares (prompt - 1) / block_size leading full blocks of the
+ *     leader once the leader has computed them (read-only, refcounted), defers while the
+ *     leader waits or computes, is admitted without sharing once the leader has finished, and
+ *     recomputes its own tokens from the first unshared position (its last prompt token
+ *     always);
+ *   - after a step, pa_sched_commit adds each sequence's n_new to its cache; a sequence whose
+ *     cache reaches its token count samples one token: after max_new samples it finishes and
+ *     its blocks are freed (the last sampled token is never written), else it gains a token.
+ * Sequence ids are any non-negative int32. Not thread-safe. */
+typedef struct pa_scheduler pa_scheduler;
+
+int32_t pa_sched_create(int32_t num_blocks, int32_t block_size, int32_t chunk, int32_t budget,
+                        pa_scheduler** out);
+int32_t pa_sched_destroy(pa_scheduler* s);
+/* The scheduler's allocator (owned by the scheduler; tables, slots, build_step, checks). */
+pa_allocator* pa_sched_allocator(pa_scheduler* s);
+/* Queues a request: prompt_len >= 1 tokens, max_new >= 1 tokens to sample, leader = a
+ * sequence id whose prompt it shares, or -1. PA_ERR_STATE if seq was added before. */
+int32_t pa_sched_add(pa_scheduler* s, int32_t seq, int32_t prompt_len, int32_t max_new,
+                     int32_t leader);
+/* Schedules one step (host out): for i < *n_out, sequence seqs[i] computes n_new[i] tokens
+ * ending at context ctx_lens[i], in step order. cap must be at least the number of waiting
+ * plus running sequences. Feed the result to pa_alloc_build_step on pa_sched_allocator(s).
+ * PA_ERR_STATE if the previous step was not committed. */
+int32_t pa_sched_step(pa_scheduler* s, int32_t* seqs, int32_t* n_new, int32_t* ctx_lens,
+                      int32_t cap, int32_t* n_out);
+/* Applies the pending step; the sequences that finished go to finished[] (host). */
+int32_t pa_sched_commit(pa_scheduler* s, int32_t* finished, int32_t cap, int32_t* n_finished);
+int32_t pa_sched_counts(const pa_scheduler* s, int32_t* n_waiting, int32_t* n_running,
+                        int64_t* preemptions);
+/* Token count, tokens in the cache and samples taken so far of one sequence. */
+int32_t pa_sched_seq(const pa_scheduler* s, int32_t seq, int32_t* n_tokens,
+                     int32_t* num_computed, int32_t* generated);
 
 /* Slot mapping from explicit host tables (P3 page, Design / paged.py: copy-free append).
  * Token i of sequence s sits at position p = ctx_lens[s] - n_q(s) + i, where
@@ -212,6 +280,14 @@ int32_t pa_upload_block_table(const pa_shape* shape, const int32_t* host, int32_
 int32_t paged_kv_write(const void* k_new, const void* v_new, const int32_t* slot_mapping,
                        int32_t T, void* k_pool, void* v_pool, const pa_shape* shape,
                        int32_t* err_flag, pa_stream_t stream);
+
+/* Copy-on-write block copies (pairs from pa_alloc_cow, uploaded by the caller): for k in
+ * [0, n_pairs), the K and V of block pairs[2k] are copied unchanged to block pairs[2k + 1].
+ * Device: pairs [2 * n_pairs] int32; k_pool, v_pool as for paged_kv_write. A pair with an id
+ * outside [0, num_blocks) or equal ids is skipped and sets PA_DEVERR_BLOCK. n_pairs == 0
+ * launches nothing. Order it before the step's paged_kv_write on the same stream. */
+int32_t paged_copy_blocks(const int32_t* pairs, int32_t n_pairs, void* k_pool, void* v_pool,
+                          const pa_shape* shape, int32_t* err_flag, pa_stream_t stream);
 
 /* Attention for one flat ragged step over an already-written pool (call paged_kv_write
  * first: ctx_lens count this step's tokens, P3 page "write new K/V, return [T, H, D]").

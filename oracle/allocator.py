@@ -18,6 +18,18 @@ truncation).
 Reading where the pages leave it open: the free stack starts so that the first alloc
 returns block 0; free pushes on top, so the next alloc reuses the most recently freed
 block.
+
+Rollback and copy-on-write follow "Optional paged KV cache (vLLM-style) — v1 design":
+  * trim(n) rewinds a sequence to n tokens and frees the now-unoccupied tail blocks (stale
+    bytes past the offset are never read). Reading: tail blocks are freed from the last one
+    backwards, so the block nearest the kept part is handed out first when the sequence
+    grows again.
+  * Block-level CoW sharing (refcounted block tables, fork-on-divergent-write): fork gives
+    a new sequence every block of an existing one (refcounts up, partial last block
+    included); before a write into positions that lie in blocks with refcount > 1, each such
+    block is replaced by a fresh private block, and the (old, new) pairs are returned so the
+    caller copies the old contents first. Reading: blocks are replaced in table order, all
+    or nothing (if the pool cannot supply every replacement nothing changes).
 """
 from __future__ import annotations
 
@@ -145,6 +157,47 @@ class PagedCacheModel:
                 raise ReadOnlyBlock(f"block {b} is shared (refcount {self.alloc.ref[b]})")
             out.append(b * self.block_size + p % self.block_size)
         return out
+
+    def trim(self, seq: int, n_tokens: int) -> None:
+        """Rewind seq to n_tokens: keep the blocks that cover them, free the rest (last
+        block first)."""
+        t = self.tables[seq]
+        keep = self._need(n_tokens)
+        if n_tokens < 0 or keep > len(t):
+            raise ValueError("trim beyond the table's capacity")
+        for b in reversed(t[keep:]):
+            self.alloc.free(b)
+        del t[keep:]
+
+    def fork(self, src: int, dst: int) -> None:
+        """dst shares every block of src (copy-on-write)."""
+        if dst in self.tables:
+            raise ValueError(f"sequence {dst} already admitted")
+        t = self.tables[src]
+        for b in t:
+            self.alloc.incref(b)
+        self.tables[dst] = list(t)
+
+    def cow(self, seq: int, start: int, n: int) -> List[tuple]:
+        """Make the blocks holding positions start..start+n-1 private to seq. Returns the
+        (old block, new block) pairs whose contents the caller must copy before writing."""
+        t = self.tables[seq]
+        if n <= 0:
+            return []
+        first, last = start // self.block_size, (start + n - 1) // self.block_size
+        if start < 0 or last >= len(t):
+            raise IndexError("position beyond the table's capacity")
+        shared = [j for j in range(first, last + 1) if self.alloc.ref[t[j]] > 1]
+        if len(shared) > self.alloc.num_free:
+            raise PoolExhausted(f"need {len(shared)}, have {self.alloc.num_free}")
+        pairs = []
+        for j in shared:
+            old = t[j]
+            new = self.alloc.alloc()
+            self.alloc.free(old)              # drops this table's reference only
+            t[j] = new
+            pairs.append((old, new))
+        return pairs
 
     def check_consistent(self) -> None:
         self.alloc.check_consistent(self.tables)
