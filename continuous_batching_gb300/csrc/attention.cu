@@ -933,8 +933,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (!(ok = wait_bounded(bar(kVFull + tc % SV), (tc / SV) & 1, abort_word)))
                         break;
                     zero_v_tail<D>(sb + L::kV + (tc % SV) * L::kKVTile, kb, I.ctx, p.bs, tid, 256);
+                    // the zeros were written through the generic proxy and the PV MMA reads
+                    // them through the async proxy: only these tiles need the proxy fence
+                    fence_proxy_async();
                 }
-                fence_proxy_async();
                 tc_fence_before();
                 mbar_arrive(bar(kPFull + (tc & 1)));            // all 256 softmax threads arrive
             }
