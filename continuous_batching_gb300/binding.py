@@ -59,7 +59,7 @@ class Shape(C.Structure):
 class WorkItem(C.Structure):
     _fields_ = [("seq", C.c_int32), ("q_start", C.c_int32), ("n_q", C.c_int32),
                 ("kv_head", C.c_int32), ("split", C.c_int32), ("n_tiles", C.c_int32),
-                ("reserved0", C.c_int32), ("reserved1", C.c_int32)]
+                ("n_splits", C.c_int32), ("reserved1", C.c_int32)]
 
 
 WORK_ITEM_DTYPE = np.dtype([(n, np.int32) for n, _ in WorkItem._fields_])

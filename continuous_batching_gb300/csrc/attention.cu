@@ -8,7 +8,9 @@
 // Consistent, High-Performance, Agent-Driven", section 2 (phase consistency) and 4.2 (decode
 // routed through the prefill read path).
 //
-// Work item = (sequence, KV head, tile of up to 128/g query tokens, KV split). The M = 128
+// Work item = (sequence, KV head, tile of up to 128/g query tokens, KV splits): a decode
+// row's item reads one split (its splits are folded by the combine kernel), a prefill tile's
+// item reads all of its splits and folds them itself in the combine's order. The M = 128
 // rows of every MMA are (token, head-in-group) pairs of one KV head, so K/V tiles are shared
 // by the g query heads of a group. A decode item simply has one token (g valid rows). Every
 // row runs the same instruction sequence whatever the item holds:
@@ -33,7 +35,9 @@
 // it, a V slot once PV has. A paged tile is one box per block (K: one per 64-column half,
 // V: both halves in one box), issued from all 32 lanes of the loader warp. TMEM holds two S buffers (S of the
 // next tile is computed while the softmax works on the current one; P overwrites the S it came
-// from) and two O accumulators (an item's epilogue overlaps the next item's MMAs). Every wait on an mbarrier is bounded.
+// from) and two O accumulators used by alternate splits (a split's epilogue or fold overlaps
+// the next split's MMAs; the running result of a prefill tile's earlier splits sits in one of
+// them). Every wait on an mbarrier is bounded.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
@@ -60,6 +64,8 @@ constexpr uint32_t kTmemO = 256;
 constexpr unsigned long long kWaitLimitNs = 1000000000ull;   // one second per wait
 
 static_assert(kSplit % kTileKeys == 0, "splits are whole tiles");
+constexpr int kSplitTiles = kSplit / kTileKeys;
+static_assert((kSplitTiles & (kSplitTiles - 1)) == 0, "tiles per split: a power of two");
 // Growth of a row's maximum (log2 units) tolerated before its softmax reference moves.
 constexpr float kLazyLog2 = 8.f;
 
@@ -309,13 +315,14 @@ __device__ __forceinline__ uint32_t swz(int row, int chunk) {
 // no work in any role and raises PA_DEVERR_META (reported by the softmax warps).
 struct Item {
     bool good;
-    int seq, ctx, q_start, n_q, kvh, split, pos0, k_begin, n_tiles, rows_valid;
+    int seq, ctx, q_start, n_q, kvh, split, n_splits, pos0, k_begin, n_tiles, rows_valid;
 };
 
 // What the producer publishes in an item slot (64 bytes); `last` marks the end of the CTA's
 // item list.
 struct ItemSlot {
-    int seq, ctx, q_start, n_q, kvh, split, pos0, k_begin, n_tiles, rows_valid, last, pad[5];
+    int seq, ctx, q_start, n_q, kvh, split, n_splits, pos0, k_begin, n_tiles, rows_valid, last,
+        pad[4];
 };
 static_assert(sizeof(ItemSlot) == 64, "item slot size");
 
@@ -328,6 +335,7 @@ __device__ __forceinline__ Item slot_item(const volatile ItemSlot* sl, bool* las
     I.n_q = sl->n_q;
     I.kvh = sl->kvh;
     I.split = sl->split;
+    I.n_splits = sl->n_splits;
     I.pos0 = sl->pos0;
     I.k_begin = sl->k_begin;
     I.n_tiles = sl->n_tiles;
@@ -352,7 +360,11 @@ __device__ __forceinline__ Item load_item(const Params& p, int idx) {
     const int p_max = pos0 + it.n_q - 1;
     const int k_begin = it.split * kSplit;
     good = good && k_begin <= p_max && (p_max < kSplit || p_max / kSplit < p.max_splits);
-    const int k_end = min(k_begin + kSplit, p_max + 1);
+    // a decode row's splits are separate items (folded by the combine kernel); a prefill
+    // tile's item starts at split 0 and covers every split its last row reaches
+    const int ns = max(it.n_splits, 1);
+    good = good && (cu1 - cu0 == 1 ? ns == 1 : it.split == 0 && ns == p_max / kSplit + 1);
+    const int k_end = min(k_begin + ns * kSplit, p_max + 1);
     I.good = good;
     I.seq = seq;
     I.ctx = ctx_s;
@@ -360,6 +372,7 @@ __device__ __forceinline__ Item load_item(const Params& p, int idx) {
     I.n_q = it.n_q;
     I.kvh = it.kv_head;
     I.split = it.split;
+    I.n_splits = ns;
     I.pos0 = pos0;
     I.k_begin = k_begin;
     I.n_tiles = good ? (k_end - k_begin + kTileKeys - 1) / kTileKeys : 0;
@@ -530,6 +543,80 @@ __device__ __forceinline__ void store_half(const Params& p, const uint32_t* o, i
     }
 }
 
+// Running result of a prefill tile's splits 0 .. j-1, per row: reference maximum and sum
+// (its accumulator stays in TMEM).
+struct Fold2 {
+    float M[2], L[2];
+};
+
+// End of split js >= 1 of an item that covers all splits of its rows: the split's partial (O
+// at TMEM address tm_p, the rows' (m, l) in R) is folded into the running result of the
+// earlier splits (accumulator at tm_a, (M, L) in F) with the split combine's arithmetic, in
+// the same order: M' = max(M, m), a = 2^((M - M') c), b = 2^((m - M') c), L = L a + l b,
+// ACC = ACC a + O b. A row whose position precedes the split has no keys in it and keeps its
+// running result unchanged, as the combine would not fold it. Unless fin, the result goes to
+// tm_p, whose buffer holds the running result from here on; with fin the rows are finished,
+// out = bf16(ACC * rcp(L)), like every other row of the step.
+template <int D>
+__device__ __forceinline__ void fold_half(const Params& p, uint32_t tm_a, uint32_t tm_p, int r0,
+                                          int rs, int q4, int rows_valid, int q_start, int kvh,
+                                          int js, bool fin, const Rows2& R, Fold2& F) {
+    float fa[2], fb[2], inv[2];
+    bool take[2];
+#pragma unroll
+    for (int sr = 0; sr < 2; ++sr) {
+        take[sr] = R.pos[sr] >= js * kSplit;
+        fa[sr] = 1.f;
+        fb[sr] = 0.f;
+        if (take[sr]) {
+            const float mn = fmaxf(F.M[sr], R.m[sr]);
+            fa[sr] = F.M[sr] == mn ? 1.f : ex2(__fmul_rn(__fsub_rn(F.M[sr], mn), p.c));
+            fb[sr] = R.m[sr] == mn ? 1.f : ex2(__fmul_rn(__fsub_rn(R.m[sr], mn), p.c));
+            F.L[sr] = __fadd_rn(__fmul_rn(F.L[sr], fa[sr]), __fmul_rn(R.l[sr], fb[sr]));
+            F.M[sr] = mn;
+        }
+        inv[sr] = fin ? __frcp_rn(F.L[sr]) : 0.f;
+    }
+#pragma unroll
+    for (int h = 0; h < D / 64; ++h) {
+        uint32_t a[32], o[32];
+        tmem_ld_16x256b_x8(tm_a + 64 * h, a);
+        tmem_ld_16x256b_x8(tm_p + 64 * h, o);
+        tmem_wait_ld();
+#pragma unroll
+        for (int cc = 0; cc < 8; ++cc)
+#pragma unroll
+            for (int sr = 0; sr < 2; ++sr)
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const int k = 4 * cc + 2 * sr + e;
+                    if (take[sr])
+                        a[k] = __float_as_uint(
+                            __fadd_rn(__fmul_rn(__uint_as_float(a[k]), fa[sr]),
+                                      __fmul_rn(__uint_as_float(o[k]), fb[sr])));
+                }
+        if (!fin) {
+            tmem_st_16x256b_x8(tm_p + 64 * h, a);
+            continue;
+        }
+#pragma unroll
+        for (int sr = 0; sr < 2; ++sr) {
+            const int row = r0 + rs + 8 * sr;
+            if (row >= rows_valid) continue;
+            const int tok = q_start + row / p.g;
+            const int head = kvh * p.g + row % p.g;
+            __nv_bfloat16* dst = p.out + (int64_t(tok) * p.Hq + head) * D + 64 * h;
+#pragma unroll
+            for (int cc = 0; cc < 8; ++cc) {
+                const float x0 = __fmul_rn(__uint_as_float(a[4 * cc + 2 * sr]), inv[sr]);
+                const float x1 = __fmul_rn(__uint_as_float(a[4 * cc + 2 * sr + 1]), inv[sr]);
+                *reinterpret_cast<uint32_t*>(dst + 8 * cc + 2 * q4) = pack_bf16(x0, x1);
+            }
+        }
+    }
+    if (!fin) tmem_wait_st();
+}
+
 // Keys at or beyond ctx in the tile starting at key kb are stale or were never loaded: their
 // V rows in the slot at vb are zeroed (threads tid of nthr share the work) so that their zero
 // probabilities contribute exact zeros.
@@ -643,6 +730,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     sl->n_q = I.n_q;
                     sl->kvh = I.kvh;
                     sl->split = I.split;
+                    sl->n_splits = I.n_splits;
                     sl->pos0 = I.pos0;
                     sl->k_begin = I.k_begin;
                     sl->n_tiles = I.n_tiles;
@@ -724,8 +812,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             // as soon as its K has landed (and its S buffer is free), the other issues O += P V
             // as soon as the softmax has produced P. Neither waits for the other, so the
             // stage of a finished tile is released without waiting for the next tile's data.
+            // Each split of an item (its tiles from a multiple of kSplitTiles on) accumulates
+            // in an O buffer of its own, alternating with the split counter sg.
             struct Cursor {
-                int ic, jt, tc;
+                int ic, jt, tc, sg;
                 bool have, done;
                 Item I;
             };
@@ -747,25 +837,30 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (++c.jt == c.I.n_tiles) {
                     c.jt = 0;
                     ++c.ic;
+                    ++c.sg;
                     c.have = false;
+                } else if ((c.jt & (kSplitTiles - 1)) == 0) {
+                    ++c.sg;
                 }
             };
-            Cursor cs{0, 0, 0, false, false, Item{}}, cv{0, 0, 0, false, false, Item{}};
+            Cursor cs{0, 0, 0, 0, false, false, Item{}}, cv{0, 0, 0, 0, false, false, Item{}};
             unsigned long long idle_since = 0;
             while (!(cs.done && cv.done)) {
                 bool progress = false;
                 fetch(cv);
                 fetch(cs);
-                // O += P V for the oldest tile whose P is ready
+                // O += P V for the oldest tile whose P is ready (the first tile of a split
+                // starts its O buffer once the epilogue has released it)
+                const bool cont = (cv.jt & (kSplitTiles - 1)) != 0;
                 if (cv.have && cv.tc < cs.tc &&
                     mbar_test_wait(bar(kPFull + (cv.tc & 1)), (cv.tc >> 1) & 1) &&
                     mbar_test_wait(bar(kVFull + cv.tc % SV), (cv.tc / SV) & 1) &&
-                    (cv.jt > 0 || cv.ic < 2 ||
-                     mbar_test_wait(bar(kOFree + (cv.ic & 1)), ((cv.ic >> 1) - 1) & 1))) {
+                    (cont || cv.sg < 2 ||
+                     mbar_test_wait(bar(kOFree + (cv.sg & 1)), ((cv.sg >> 1) - 1) & 1))) {
                     tc_fence_after();
                     const int st = cv.tc % SV;
-                    issue_pv(st, tmem + (cv.tc & 1) * 128, tmem + kTmemO + (cv.ic & 1) * 128,
-                             cv.jt > 0);
+                    issue_pv(st, tmem + (cv.tc & 1) * 128, tmem + kTmemO + (cv.sg & 1) * 128,
+                             cont);
                     tc_commit(bar(kPFree + (cv.tc & 1)));
                     tc_commit(bar(kVEmpty + st));
                     tc_commit(bar(kPVDone + (cv.tc & 1)));
@@ -831,21 +926,26 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_arrive(bar(kItemEmpty + (ic & 3)));     // all 32 lanes arrive
             if (last) break;
             const int key_end = min(I.k_begin + I.n_tiles * kTileKeys, I.ctx);
-            const int first = I.k_begin >> log2bs;
-            const int n_ent = min((key_end - I.k_begin + p.bs - 1) >> log2bs, kMaxTableEntries);
-            const int32_t* trow = p.block_table + int64_t(I.seq) * p.max_blocks + first;
-            __syncwarp();
-            for (int e = lane; e < n_ent; e += 32) {
-                int b = __ldg(trow + e);
-                if (b < 0 || b >= p.num_blocks) {
-                    // out of range: the box lands outside the tensor and reads zeros
-                    if (p.err && !is_v) atomicOr(p.err, PA_DEVERR_BLOCK);
-                    b = -1;
-                }
-                tbl[e] = b;
-            }
-            __syncwarp();
             for (int jt = 0; jt < I.n_tiles; ++jt, ++tc) {
+                // the table entries of one split at a time (the split of tile jt starts at sk)
+                const int sk = I.k_begin + (jt & ~(kSplitTiles - 1)) * kTileKeys;
+                if ((jt & (kSplitTiles - 1)) == 0) {
+                    const int n_ent = min((min(sk + kSplit, key_end) - sk + p.bs - 1) >> log2bs,
+                                          kMaxTableEntries);
+                    const int32_t* trow =
+                        p.block_table + int64_t(I.seq) * p.max_blocks + (sk >> log2bs);
+                    __syncwarp();
+                    for (int e = lane; e < n_ent; e += 32) {
+                        int b = __ldg(trow + e);
+                        if (b < 0 || b >= p.num_blocks) {
+                            // out of range: the box lands outside the tensor and reads zeros
+                            if (p.err && !is_v) atomicOr(p.err, PA_DEVERR_BLOCK);
+                            b = -1;
+                        }
+                        tbl[e] = b;
+                    }
+                    __syncwarp();
+                }
                 const int st = tc % S;
                 if (lane == 0 && tc >= S)
                     ok = wait_bounded(bar(empty_b + st), ((tc / S) - 1) & 1, abort_word);
@@ -858,7 +958,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     mbar_expect_tx(bar(full_b + st), uint32_t(nblk) * p.bs * 128 * L::kChunks);
                 __syncwarp();
                 const uint32_t dst = slots + st * L::kKVTile;
-                const int e0 = (kb - I.k_begin) >> log2bs;
+                const int e0 = (kb - sk) >> log2bs;
                 for (int j = lane; j < nblk * boxes_per_block; j += 32) {
                     const int b = j / boxes_per_block;
                     const int r = j - b * boxes_per_block;
@@ -896,7 +996,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float c = p.c;
         const volatile ItemSlot* ring =
             reinterpret_cast<const volatile ItemSlot*>(smem + L::kBar + kRingOff);
-        int tc = 0, ic = 0;
+        int tc = 0, ic = 0, sg = 0;       // tiles, items and splits seen
         bool ok = true;
         for (;;) {
             if (!(ok = wait_bounded(bar(kItemFull + (ic & 3)), (ic >> 2) & 1, abort_word))) break;
@@ -904,12 +1004,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             const Item I = slot_item(ring + (ic & 3), &last);
             mbar_arrive(bar(kItemEmpty + (ic & 3)));
             if (last) break;
-            const int ob = ic & 1;
-            const uint32_t tm_o = tmem + kTmemO + ob * 128 + lanes;
             const bool on = r0 < I.rows_valid;    // warp-uniform: the warp holds a valid row
             Rows2 R;
-            rows_init(R, r0, rs, I.rows_valid, I.pos0, p.g);
+            Fold2 F;
             for (int jt = 0; jt < I.n_tiles; ++jt, ++tc) {
+                // every split starts afresh, exactly as an item of that split alone would
+                const int jin = jt & (kSplitTiles - 1);
+                if (jin == 0) rows_init(R, r0, rs, I.rows_valid, I.pos0, p.g);
+                const int ob = sg & 1;
+                const uint32_t tm_o = tmem + kTmemO + ob * 128 + lanes;
                 if (!(ok = wait_bounded(bar(kSFull + (tc & 1)), (tc >> 1) & 1, abort_word)))
                     break;
                 tc_fence_after();
@@ -919,7 +1022,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // O belongs to the previous tile's PV until it has finished: rescale only then,
                 // and only in warps where some row's running maximum moved
                 const bool need = alpha[0] != 1.f || alpha[1] != 1.f;
-                if (jt > 0 && __any_sync(0xffffffffu, need)) {
+                if (jin > 0 && __any_sync(0xffffffffu, need)) {
                     if (!(ok = wait_bounded(bar(kPVDone + ((tc - 1) & 1)), ((tc - 1) >> 1) & 1,
                                             abort_word)))
                         break;
@@ -939,24 +1042,45 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 tc_fence_before();
                 mbar_arrive(bar(kPFull + (tc & 1)));            // all 256 softmax threads arrive
+                if (jin != kSplitTiles - 1 && jt != I.n_tiles - 1) continue;
+                // ------------------------------------------------------ end of a split
+                const int js = jt / kSplitTiles;       // split of the item (0 for a decode's)
+                ++sg;
+                if (I.n_splits > 1 && js == 0) {
+                    // split 0's O stays where it is as the running result: nothing to wait for
+#pragma unroll
+                    for (int sr = 0; sr < 2; ++sr) {
+                        F.M[sr] = R.m[sr];
+                        F.L[sr] = R.l[sr];
+                    }
+                    continue;
+                }
+                if (!(ok = wait_bounded(bar(kPVDone + (tc & 1)), (tc >> 1) & 1, abort_word)))
+                    break;
+                tc_fence_after();
+                if (I.n_splits > 1) {
+                    const bool fin = js == I.n_splits - 1;
+                    const uint32_t tm_a = tmem + kTmemO + (ob ^ 1) * 128 + lanes;
+                    if (on)
+                        fold_half<D>(p, tm_a, tm_o, r0, rs, q4, I.rows_valid, I.q_start, I.kvh,
+                                     js, fin, R, F);
+                    tc_fence_before();
+                    mbar_arrive(bar(kOFree + (ob ^ 1)));     // the previous running result
+                    if (fin) mbar_arrive(bar(kOFree + ob));
+                } else if (!on) {
+                    tc_fence_before();
+                    mbar_arrive(bar(kOFree + ob));
+                } else {
+                    uint32_t o[D / 2];
+                    if constexpr (D == 128) tmem_ld_16x256b_x16(tm_o, o);
+                    else tmem_ld_16x256b_x8(tm_o, o);
+                    tmem_wait_ld();
+                    tc_fence_before();
+                    mbar_arrive(bar(kOFree + ob));       // O is in registers: its buffer is free
+                    store_half<D>(p, o, r0, rs, q4, I.rows_valid, I.q_start, I.kvh, I.split, R);
+                }
             }
             if (!ok) break;
-            // ---------------------------------------------------------------- epilogue
-            if (!(ok = wait_bounded(bar(kPVDone + ((tc - 1) & 1)), ((tc - 1) >> 1) & 1, abort_word)))
-                break;
-            tc_fence_after();
-            if (!on) {
-                tc_fence_before();
-                mbar_arrive(bar(kOFree + ob));
-            } else {
-                uint32_t o[D / 2];
-                if constexpr (D == 128) tmem_ld_16x256b_x16(tm_o, o);
-                else tmem_ld_16x256b_x8(tm_o, o);
-                tmem_wait_ld();
-                tc_fence_before();
-                mbar_arrive(bar(kOFree + ob));       // O is in registers: its buffer is free
-                store_half<D>(p, o, r0, rs, q4, I.rows_valid, I.q_start, I.kvh, I.split, R);
-            }
             ++ic;
         }
     }
@@ -973,13 +1097,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // ------------------------------------------------------------- fixed-order split combine
-// For every (row, q head) whose row spans more than one split: fold the partials of splits
-// 0, 1, ... in ascending order, starting from split 0's (m, l, acc) as they are:
+// For every (decode row, q head) whose row spans more than one split: fold the partials of
+// splits 0, 1, ... in ascending order, starting from split 0's (m, l, acc) as they are:
 //   M' = max(M, m_s), a = 2^((M - M') c), b = 2^((m_s - M') c),
 //   L = L a + l_s b, ACC = ACC a + acc_s b;  out = bf16_rne(ACC * rcp_rn(L)).
-// A row with one split is finished by the attention kernel with the same two roundings.
-// One thread per (row, q head, 4 columns); the partials of up to kBatch splits are loaded
-// before they are folded, so a row costs about nsplit / kBatch memory round trips. Launched
+// A row with one split is finished by the attention kernel with the same two roundings, and
+// so is every row of a sequence with several query rows, whose item folds its own splits in
+// this order (fold_half). One thread per (sequence, q head, 4 columns); sequences with other
+// than one query row return at once. The partials of up to kBatch splits are loaded before
+// they are folded, so a row costs about nsplit / kBatch memory round trips. Launched
 // as a programmatic dependent of the attention kernel (its launch overlaps the attention
 // tail); griddepcontrol.wait holds every thread until that grid has completed and its
 // writes are visible.
@@ -993,20 +1119,16 @@ __global__ void __launch_bounds__(256)
     constexpr int kUnits = D / kCols;         // threads per (row, q head)
     constexpr int kBatch = 8;                 // splits loaded ahead of their fold
     asm volatile("griddepcontrol.wait;" ::: "memory");
-    const int64_t n = int64_t(T) * Hq * kUnits;
+    const int64_t n = int64_t(B) * Hq * kUnits;
     const int64_t u = int64_t(blockIdx.x) * 256 + threadIdx.x;
     if (u >= n) return;
     const int64_t w = u / kUnits;
     const int col = int(u % kUnits) * kCols;
-    const int64_t tok = w / Hq;
+    const int s = int(w / Hq);
     const int head = int(w % Hq);
-    int lo = 0, hi = B - 1;                   // sequence s with cu[s] <= tok < cu[s+1]
-    while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        if (__ldg(cu + mid) <= tok) lo = mid;
-        else hi = mid - 1;
-    }
-    const int pos = __ldg(ctx + lo) - __ldg(cu + lo + 1) + int(tok);
+    const int64_t tok = __ldg(cu + s);
+    if (__ldg(cu + s + 1) - tok != 1 || tok >= T) return;
+    const int pos = __ldg(ctx + s) - 1;
     if (pos < 0) return;                      // inconsistent metadata: flagged by the kernel
     const int nsp = pos / kSplit + 1;
     if (nsp == 1 || nsp > max_splits) return;
@@ -1171,7 +1293,7 @@ int32_t launch(const Maps& maps, const Params& prm, int32_t max_ctx, cudaStream_
                                       maps.qn, prm));
     if (st) return st;
     if (max_ctx > kSplit) {
-        const int64_t threads = int64_t(prm.T) * prm.Hq * (D / 4);
+        const int64_t threads = int64_t(prm.B) * prm.Hq * (D / 4);
         cfg.gridDim = dim3(unsigned((threads + 255) / 256));
         cfg.blockDim = dim3(256);
         cfg.dynamicSmemBytes = 0;

@@ -427,10 +427,14 @@ int32_t pa_plan_step(const pa_shape* shape, int32_t B, const int32_t* cu, const 
             const int32_t nt = std::min(rpt, n - t0);
             const int64_t p_max = int64_t(ctx[s]) - n + t0 + nt - 1;
             const int32_t nsplit = int32_t(p_max / PA_SPLIT_TOKENS + 1);
+            // a decode row's splits go to separate items; a prefill tile keeps all of its
+            // splits in one item and folds them in the kernel
+            const int32_t per_item = n > 1 ? nsplit : 1;
             for (int32_t h = 0; h < shape->num_kv_heads; ++h)
-                for (int32_t sp = 0; sp < nsplit; ++sp) {
+                for (int32_t sp = 0; sp < nsplit; sp += per_item) {
                     const int64_t k0 = int64_t(sp) * PA_SPLIT_TOKENS;
-                    const int64_t k1 = std::min<int64_t>(k0 + PA_SPLIT_TOKENS, p_max + 1);
+                    const int64_t k1 =
+                        std::min<int64_t>(k0 + int64_t(per_item) * PA_SPLIT_TOKENS, p_max + 1);
                     pa_work_item it{};
                     it.seq = s;
                     it.q_start = cu[s] + t0;
@@ -438,6 +442,7 @@ int32_t pa_plan_step(const pa_shape* shape, int32_t B, const int32_t* cu, const 
                     it.kv_head = h;
                     it.split = sp;
                     it.n_tiles = int32_t((k1 - k0 + PA_TILE_KEYS - 1) / PA_TILE_KEYS);
+                    it.n_splits = per_item;
                     out.push_back(it);
                 }
         }

@@ -89,9 +89,9 @@ typedef struct pa_work_item {
     int32_t q_start;    /* first query row (token index into q and out) */
     int32_t n_q;        /* query rows, 1 .. 128 / group */
     int32_t kv_head;    /* KV head */
-    int32_t split;      /* KV split index */
+    int32_t split;      /* first KV split index */
     int32_t n_tiles;    /* key tiles of PA_TILE_KEYS the item reads (a cost estimate) */
-    int32_t reserved0;
+    int32_t n_splits;   /* consecutive splits from `split` the item covers (0 counts as 1) */
     int32_t reserved1;
 } pa_work_item;
 
@@ -249,10 +249,16 @@ int32_t pa_compute_slots(const pa_shape* shape, const int32_t* block_table, int3
 int64_t pa_plan_max_items(const pa_shape* shape, int32_t B, int32_t T, int32_t max_ctx);
 
 /* Splits the step into work items (host in, host out). Query rows of a sequence are cut
- * into tiles of 128 / group rows; every (tile, KV head, KV split the tile's last row reaches)
- * is one item. Items are ordered by decreasing n_tiles (ties keep the generation order), so
- * the order is a pure function of the metadata. Validates the metadata like
- * pa_compute_slots (minus the table). PA_ERR_INVALID if max_items is too small. */
+ * into tiles of 128 / group rows. A sequence with one query row (a decode) gives one item per
+ * (KV head, KV split its row reaches), so a long context is spread over many CTAs and its
+ * splits are folded by the split-combine kernel. A sequence with more query rows (a prefill
+ * chunk) gives one item per (tile, KV head) that covers every split the tile's last row
+ * reaches; the kernel folds those splits itself, in the same ascending order and arithmetic,
+ * so a row's bits are the same either way. paged_attention_step relies on this rule (an item
+ * that breaks it is flagged PA_DEVERR_META and skipped). Items are ordered by decreasing
+ * n_tiles (ties keep the generation order), so the order is a pure function of the metadata.
+ * Validates the metadata like pa_compute_slots (minus the table). PA_ERR_INVALID if
+ * max_items is too small. */
 int32_t pa_plan_step(const pa_shape* shape, int32_t B, const int32_t* cu_seqlens_q,
                      const int32_t* ctx_lens, pa_work_item* items, int32_t max_items,
                      int32_t* n_items);
@@ -298,7 +304,9 @@ int32_t paged_copy_blocks(const int32_t* pairs, int32_t n_pairs, void* k_pool, v
  * result rounded to bf16 (nearest even). Every row, decode or prefill, runs the same tile
  * routine, so its bits depend only on its own query, keys and position.
  * Launches: the attention kernel, then (when max_ctx > PA_SPLIT_TOKENS) the split-combine
- * kernel, both as programmatic dependent launches: each may start while the previous kernel
+ * kernel, which finishes the decode rows whose context spans several splits (a prefill tile's
+ * item folds its splits itself, in the same order and arithmetic), both as programmatic
+ * dependent launches: each may start while the previous kernel
  * on the stream drains, and waits for that kernel to complete before it reads anything, so
  * stream order is kept for every input.
  * Device inputs: q [T, Hq, D] bf16; k_pool, v_pool [num_blocks, block_size, Hkv, D] bf16;

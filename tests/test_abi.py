@@ -17,9 +17,8 @@ HEADER = os.path.join(ROOT, "include", "pagedattn.h")
 
 @pytest.fixture(scope="module", autouse=True)
 def built_library():
-    if not os.path.exists(bd.LIB_PATH):
-        from continuous_batching_gb300 import build
-        build.build()
+    from continuous_batching_gb300 import build
+    build.build()                     # incremental: recompiles only what changed
     return bd.load()
 
 
@@ -75,7 +74,9 @@ def test_slot_mapping_rejects_bad_metadata():
 
 @pytest.mark.parametrize("name", wl.CONFIG_NAMES)
 def test_plan_covers_every_row_head_split_once(name):
-    """Each (query row, KV head, split s <= pos // 1024) appears in exactly one item."""
+    """Each (query row, KV head, split s <= pos // 1024) appears in exactly one item. A decode
+    row's splits are items of one split each; a prefill tile's item starts at split 0 and
+    covers every split its last row reaches."""
     st = wl.make_config(name, with_pool=False)
     shape = bd.Shape.make(st.Hq, st.Hkv, st.D, st.block_size, st.num_blocks)
     items = bd.pa_plan_step(shape, st.cu_seqlens_q, st.ctx_lens)
@@ -85,12 +86,22 @@ def test_plan_covers_every_row_head_split_once(name):
     count = {}
     for it in items:
         assert 1 <= it["n_q"] <= 128 // g
-        assert st.cu_seqlens_q[it["seq"]] <= it["q_start"]
-        assert it["q_start"] + it["n_q"] <= st.cu_seqlens_q[it["seq"] + 1]
+        cu0, cu1 = st.cu_seqlens_q[it["seq"]], st.cu_seqlens_q[it["seq"] + 1]
+        assert cu0 <= it["q_start"] and it["q_start"] + it["n_q"] <= cu1
+        last = it["q_start"] + it["n_q"] - 1
+        if cu1 - cu0 == 1:
+            assert it["n_splits"] == 1
+        else:
+            assert it["split"] == 0 and it["n_splits"] == nsplit[last]
+        # tiles of 128 keys from the item's first split up to its last row's position
+        k0 = it["split"] * bd.PA_SPLIT_TOKENS
+        k1 = min(k0 + it["n_splits"] * bd.PA_SPLIT_TOKENS, pos_of[last] + 1)
+        assert it["n_tiles"] == -(-(k1 - k0) // bd.PA_TILE_KEYS)
         for t in range(it["q_start"], it["q_start"] + it["n_q"]):
-            if it["split"] < nsplit[t]:
-                key = (t, it["kv_head"], it["split"])
-                count[key] = count.get(key, 0) + 1
+            for sp in range(it["split"], it["split"] + it["n_splits"]):
+                if sp < nsplit[t]:
+                    key = (t, it["kv_head"], sp)
+                    count[key] = count.get(key, 0) + 1
     want = {(t, h, s) for t in range(st.T) for h in range(st.Hkv) for s in range(nsplit[t])}
     assert set(count) == want and all(v == 1 for v in count.values())
     # longest items first, deterministic

@@ -162,6 +162,40 @@ def test_device_error_word_for_bad_slot_and_block():
     assert_close(o[:3], ref[:3], "unaffected rows")
 
 
+def test_items_that_break_the_split_rule_are_flagged_and_skipped():
+    """A prefill tile's item must cover all of its splits from split 0 and a decode row's item
+    exactly one: forged items that do otherwise are skipped with PA_DEVERR_META, and the rows
+    of the other items are still right."""
+    st = wl.make_step(16, 4, 128, 16, [3000, 2500, 700], [40, 1, 1], seed=91)
+    shape = shape_of(st)
+    import tests.gpu_util as gu
+    kp, vp = gu.bf16_dev(st.k_pool, torch), gu.bf16_dev(st.v_pool, torch)
+    q = gu.bf16_dev(st.q, torch)
+    ref = pa.attention(st.q, st.k_pool, st.v_pool, st.block_table, st.cu_seqlens_q,
+                       st.ctx_lens, st.Hq)
+    items = bd.pa_plan_step(shape, st.cu_seqlens_q, st.ctx_lens)
+    pre = np.flatnonzero(items["seq"] == 0)
+    dec = np.flatnonzero((items["seq"] == 1) & (items["split"] == 0))
+    assert np.all(items["n_splits"][pre] == 3)
+    for forge in ("prefill_one_split", "prefill_late_start", "decode_two_splits"):
+        bad = items.copy()
+        if forge == "prefill_one_split":
+            bad["n_splits"][pre[0]] = 1
+        elif forge == "prefill_late_start":
+            bad["split"][pre[0]] = 1
+        else:
+            bad["n_splits"][dec[0]] = 2
+        runner = bd.StepRunner(shape).prepare(st.cu_seqlens_q, st.ctx_lens, st.block_table)
+        runner.items = torch.from_numpy(bad.view(np.int32).reshape(-1).copy()).cuda()
+        out = torch.zeros((st.T, st.Hq, st.D), dtype=torch.bfloat16, device="cuda")
+        runner.attend(q, kp, vp, out)
+        torch.cuda.synchronize()
+        assert runner.device_error() & bd.PA_DEVERR_META, forge
+        o = out.view(torch.int16).cpu().numpy().view(np.uint16)
+        # sequence 2 (a short decode) has one item, never forged
+        assert_close(o[41:42], ref[41:42], forge)
+
+
 def test_host_rejects_bad_arguments_before_launch():
     st = wl.make_config("tiny")
     shape = shape_of(st)
