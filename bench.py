@@ -251,6 +251,11 @@ class GpuStep:
         return h2d, st.T * st.Hq * st.D * 2
 
 
+def hold_gpu(torch, seconds: float) -> None:
+    """Keeps the current stream busy for about `seconds` (a spin kernel; 2.1 GHz assumed)."""
+    torch.cuda._sleep(int(seconds * 2.1e9))
+
+
 def time_steps(g: GpuStep, torch, steps: int, warmup: int, flush, attn_only=False):
     """Per-step CUDA events (L2 flushed before each step, outside the events) around replays
     of the captured step graphs. Returns (per-step ms list, per-attention-call ms list)."""
@@ -261,6 +266,9 @@ def time_steps(g: GpuStep, torch, steps: int, warmup: int, flush, attn_only=Fals
     torch.cuda.synchronize()
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
            torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    # hold the GPU (outside every timed interval) while the host queues all timed steps, so
+    # that no interval includes the GPU waiting for the host to enqueue the next graph
+    hold_gpu(torch, 1e-3 + 3e-4 * steps)
     for i in range(steps):
         flush.zero_()
         a, b, c = ev[i]

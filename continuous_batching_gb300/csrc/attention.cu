@@ -293,6 +293,49 @@ __device__ __forceinline__ float ex2(float x) {
     return y;
 }
 
+// Packed fp32 pairs (lo, hi) in one 64-bit register for the f32x2 instructions. They are used
+// where every row goes through the same instructions whatever its item (the softmax and the
+// rescale); the fold of split partials stays scalar like the combine kernel it must match.
+__device__ __forceinline__ uint64_t f2(float lo, float hi) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ void f2_split(uint64_t v, float& lo, float& hi) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t r;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+    return r;
+}
+__device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b) {
+    uint64_t r;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ uint64_t mul2(uint64_t a, uint64_t b) {
+    uint64_t r;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ float max3(float a, float b, float c) {
+    float r;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
+}
+
+// Maximum of 32 values (exact in any order).
+__device__ __forceinline__ float max32(const float (&v)[32]) {
+    float t[11];
+#pragma unroll
+    for (int k = 0; k < 10; ++k) t[k] = max3(v[3 * k], v[3 * k + 1], v[3 * k + 2]);
+    t[10] = fmaxf(v[30], v[31]);
+    const float u0 = max3(t[0], t[1], t[2]), u1 = max3(t[3], t[4], t[5]);
+    const float u2 = max3(t[6], t[7], t[8]), u3 = fmaxf(t[9], t[10]);
+    return fmaxf(max3(u0, u1, u2), u3);
+}
+
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
     __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<uint32_t*>(&v);
@@ -425,27 +468,21 @@ __device__ __forceinline__ void softmax_half(uint32_t tm_s, int r0, int q4, int 
         // this block
         const bool full = __all_sync(0xffffffffu, kb + kTileKeys - 1 <= pr);
         float sv[32];
-        float mx = -INFINITY;
         if (full) {
 #pragma unroll
             for (int cc = 0; cc < 16; ++cc)
 #pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    const float sc = __uint_as_float(r[4 * cc + 2 * sr + e]);
-                    sv[2 * cc + e] = sc;
-                    mx = fmaxf(mx, sc);
-                }
+                for (int e = 0; e < 2; ++e) sv[2 * cc + e] = __uint_as_float(r[4 * cc + 2 * sr + e]);
         } else {
 #pragma unroll
             for (int cc = 0; cc < 16; ++cc)
 #pragma unroll
                 for (int e = 0; e < 2; ++e) {
                     const int key = kb + 8 * cc + 2 * q4 + e;
-                    const float sc = key <= pr ? __uint_as_float(r[4 * cc + 2 * sr + e]) : -INFINITY;
-                    sv[2 * cc + e] = sc;
-                    mx = fmaxf(mx, sc);
+                    sv[2 * cc + e] = key <= pr ? __uint_as_float(r[4 * cc + 2 * sr + e]) : -INFINITY;
                 }
         }
+        float mx = max32(sv);
         mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
         mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
         // The reference maximum moves only when the row's maximum grows past it by more than
@@ -464,12 +501,28 @@ __device__ __forceinline__ void softmax_half(uint32_t tm_s, int r0, int q4, int 
                             ? 1.f
                             : ex2(__fmul_rn(__fsub_rn(m_old, m_use), c));
         const float nmc = __fmul_rn(-m_use, c);
-        float sum = 0.f;
+        // p = 2^(s c - m c) for the thread's 32 keys (pairs of adjacent columns packed), then
+        // their sum as a fixed tree: the pairs' lanes are added level by level and the two
+        // lanes last
+        const uint64_t c2 = f2(c, c), nmc2 = f2(nmc, nmc);
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-            sv[i] = ex2(__fmaf_rn(sv[i], c, nmc));
-            sum = __fadd_rn(sum, sv[i]);
+        for (int i = 0; i < 16; ++i) {
+            float x0, x1;
+            f2_split(fma2(f2(sv[2 * i], sv[2 * i + 1]), c2, nmc2), x0, x1);
+            sv[2 * i] = ex2(x0);
+            sv[2 * i + 1] = ex2(x1);
         }
+        uint64_t t8[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            t8[i] = add2(f2(sv[4 * i], sv[4 * i + 1]), f2(sv[4 * i + 2], sv[4 * i + 3]));
+#pragma unroll
+        for (int w = 4; w >= 1; w >>= 1)
+#pragma unroll
+            for (int i = 0; i < w; ++i) t8[i] = add2(t8[i], t8[i + w]);
+        float sum, sum_hi;
+        f2_split(t8[0], sum, sum_hi);
+        sum = __fadd_rn(sum, sum_hi);
         sum = __fadd_rn(sum, __shfl_xor_sync(0xffffffffu, sum, 1));
         sum = __fadd_rn(sum, __shfl_xor_sync(0xffffffffu, sum, 2));
         R.l[sr] = __fadd_rn(__fmul_rn(R.l[sr], a), sum);
@@ -490,15 +543,17 @@ __device__ __forceinline__ void rescale_half(uint32_t tm_o, const float alpha[2]
     if constexpr (D == 128) tmem_ld_16x256b_x16(tm_o, o);
     else tmem_ld_16x256b_x8(tm_o, o);
     tmem_wait_ld();
+    const uint64_t a2[2] = {f2(alpha[0], alpha[0]), f2(alpha[1], alpha[1])};
 #pragma unroll
     for (int cc = 0; cc < D / 8; ++cc)
 #pragma unroll
-        for (int sr = 0; sr < 2; ++sr)
-#pragma unroll
-            for (int e = 0; e < 2; ++e) {
-                const int k = 4 * cc + 2 * sr + e;
-                o[k] = __float_as_uint(__fmul_rn(__uint_as_float(o[k]), alpha[sr]));
-            }
+        for (int sr = 0; sr < 2; ++sr) {
+            const int k = 4 * cc + 2 * sr;
+            float x0, x1;
+            f2_split(mul2(f2(__uint_as_float(o[k]), __uint_as_float(o[k + 1])), a2[sr]), x0, x1);
+            o[k] = __float_as_uint(x0);
+            o[k + 1] = __float_as_uint(x1);
+        }
     if constexpr (D == 128) tmem_st_16x256b_x16(tm_o, o);
     else tmem_st_16x256b_x8(tm_o, o);
 }
@@ -586,15 +641,18 @@ __device__ __forceinline__ void fold_half(const Params& p, uint32_t tm_a, uint32
 #pragma unroll
         for (int cc = 0; cc < 8; ++cc)
 #pragma unroll
-            for (int sr = 0; sr < 2; ++sr)
+            for (int sr = 0; sr < 2; ++sr) {
+                if (!take[sr]) continue;
+                // scalar, like the combine kernel: packed multiplies feeding a packed add
+                // may be contracted into a fused multiply-add, which rounds once and can
+                // differ from the combine's result in the last bit
 #pragma unroll
                 for (int e = 0; e < 2; ++e) {
                     const int k = 4 * cc + 2 * sr + e;
-                    if (take[sr])
-                        a[k] = __float_as_uint(
-                            __fadd_rn(__fmul_rn(__uint_as_float(a[k]), fa[sr]),
-                                      __fmul_rn(__uint_as_float(o[k]), fb[sr])));
+                    a[k] = __float_as_uint(__fadd_rn(__fmul_rn(__uint_as_float(a[k]), fa[sr]),
+                                                     __fmul_rn(__uint_as_float(o[k]), fb[sr])));
                 }
+            }
         if (!fin) {
             tmem_st_16x256b_x8(tm_p + 64 * h, a);
             continue;
