@@ -21,7 +21,7 @@ LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libpagedatt
 PA_OK, PA_ERR_INVALID, PA_ERR_SHAPE, PA_ERR_BOUNDS, PA_ERR_OOM, PA_ERR_READONLY, \
     PA_ERR_DOUBLE_FREE, PA_ERR_INCONSISTENT, PA_ERR_WORKSPACE, PA_ERR_CUDA, PA_ERR_STATE = range(11)
 PA_DEVERR_BLOCK, PA_DEVERR_SLOT, PA_DEVERR_TIMEOUT, PA_DEVERR_META = 1, 2, 4, 8
-PA_SPLIT_TOKENS = 1024
+PA_SPLIT_TOKENS = 2048
 PA_TILE_KEYS = 128
 
 

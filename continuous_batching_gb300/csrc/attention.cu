@@ -23,7 +23,8 @@
 //                 into its tile's S buffer in TMEM (A operand from TMEM)
 // A tensor-core output element depends only on its own row of A and column of B, so a row's
 // bits do not depend on the other rows of the tile; the fixed splits
-// [s*1024, (s+1)*1024) and the ascending-order combine make them independent of the batch.
+// [s*PA_SPLIT_TOKENS, (s+1)*PA_SPLIT_TOKENS) and the ascending-order combine make them
+// independent of the batch.
 //
 // Persistent schedule: one CTA per SM walks the items blockIdx.x, blockIdx.x + gridDim.x, ...
 // (the host orders items longest first). Warp roles (384 threads): warps 0-7 softmax /
@@ -115,7 +116,10 @@ constexpr int kHolderOff = 8 * kNumBars;          // TMEM address written by tcg
 constexpr int kAbortOff = kHolderOff + 4;
 constexpr int kRingOff = 512;                     // 4 item slots of 64 bytes
 constexpr int kTableOff = 768;                    // per loader warp: the item's table entries
-constexpr int kMaxTableEntries = 128;             // 1024 keys / 8-token blocks
+constexpr int kTableKeys = 1024;                  // keys whose table entries a loader holds
+constexpr int kTableTiles = kTableKeys / kTileKeys;
+constexpr int kMaxTableEntries = kTableKeys / 8;  // at the smallest block size, 8 tokens
+static_assert(kSplit % kTableKeys == 0, "a split starts a table window");
 static_assert(kAbortOff + 4 <= kRingOff, "control area");
 
 struct Params {
@@ -985,10 +989,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (last) break;
             const int key_end = min(I.k_begin + I.n_tiles * kTileKeys, I.ctx);
             for (int jt = 0; jt < I.n_tiles; ++jt, ++tc) {
-                // the table entries of one split at a time (the split of tile jt starts at sk)
-                const int sk = I.k_begin + (jt & ~(kSplitTiles - 1)) * kTileKeys;
-                if ((jt & (kSplitTiles - 1)) == 0) {
-                    const int n_ent = min((min(sk + kSplit, key_end) - sk + p.bs - 1) >> log2bs,
+                // the table entries of kTableKeys keys at a time (the window of tile jt starts
+                // at key sk)
+                const int sk = I.k_begin + (jt & ~(kTableTiles - 1)) * kTileKeys;
+                if ((jt & (kTableTiles - 1)) == 0) {
+                    const int n_ent = min((min(sk + kTableKeys, key_end) - sk + p.bs - 1) >> log2bs,
                                           kMaxTableEntries);
                     const int32_t* trow =
                         p.block_table + int64_t(I.seq) * p.max_blocks + (sk >> log2bs);

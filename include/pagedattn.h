@@ -62,8 +62,11 @@ typedef enum pa_status {
 
 /* Fixed KV split: keys [s * PA_SPLIT_TOKENS, (s + 1) * PA_SPLIT_TOKENS) form split s of every
  * sequence. It depends on nothing but the key position, which keeps the numerics of a row
- * independent of the batch ("fixed KV split per context length", P3 page Design / paged.py). */
-#define PA_SPLIT_TOKENS 1024
+ * independent of the batch ("fixed KV split per context length", P3 page Design / paged.py).
+ * The size was tuned once on GB300 (2048 beat 1024 on every measured workload: fewer split
+ * folds per prefill tile and fewer, longer decode items) and is frozen: changing it changes
+ * the bits of every row longer than one split. */
+#define PA_SPLIT_TOKENS 2048
 /* Keys per tile of the shared tile routine; tiles are aligned to multiples of this. */
 #define PA_TILE_KEYS 128
 

@@ -74,7 +74,7 @@ def test_slot_mapping_rejects_bad_metadata():
 
 @pytest.mark.parametrize("name", wl.CONFIG_NAMES)
 def test_plan_covers_every_row_head_split_once(name):
-    """Each (query row, KV head, split s <= pos // 1024) appears in exactly one item. A decode
+    """Each (query row, KV head, split s <= pos // PA_SPLIT_TOKENS) appears in exactly one item. A decode
     row's splits are items of one split each; a prefill tile's item starts at split 0 and
     covers every split its last row reaches."""
     st = wl.make_config(name, with_pool=False)
@@ -112,7 +112,8 @@ def test_plan_covers_every_row_head_split_once(name):
 
 def test_workspace_bytes_cover_partials():
     shape = bd.Shape.make(32, 8, 128, 16, 100)
-    assert bd.pa_workspace_bytes(shape, 10, 3000) == 10 * 3 * 32 * 130 * 4
+    assert bd.pa_workspace_bytes(shape, 10, 3000) == 10 * 2 * 32 * 130 * 4
+    assert bd.pa_workspace_bytes(shape, 10, 4097) == 10 * 3 * 32 * 130 * 4
     assert bd.pa_workspace_bytes(shape, 0, 0) == 256
 
 

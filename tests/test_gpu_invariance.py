@@ -30,7 +30,7 @@ def sub_step(st: wl.Step, idx, k_pool, v_pool):
 
 def test_alone_vs_among_others():
     """Each sequence alone, and among 1, 3 and 7 others in shuffled orders: equal bits."""
-    ctx = [3000, 17, 1500, 2049, 128, 700, 4100, 64, 1024, 999]
+    ctx = [3000, 17, 2070, 2049, 128, 700, 4100, 64, 2048, 999]
     nq = [1, 1, 40, 1, 128, 1, 1, 64, 1, 300]
     st = wl.make_step(32, 8, 128, 16, ctx, nq, seed=21)
     full, kp, vp, _ = run_step(st, torch)

@@ -39,8 +39,8 @@ def test_tiny_config_all_rows():
 
 # ragged mix: decode rows at tile and split boundaries plus prefill segments that start at 0,
 # straddle the first split boundary, end on a tile boundary and have ragged tails
-MID_CTX = [1, 17, 127, 128, 129, 1023, 1024, 1025, 2049, 3000, 200, 1100, 2100, 5, 384]
-MID_NQ = [1, 1, 1, 1, 1, 1, 1, 1, 1, 1, 200, 77, 33, 5, 129]
+MID_CTX = [1, 17, 127, 128, 129, 1023, 1024, 1025, 2047, 2048, 2049, 4097, 200, 2100, 4200, 5, 384]
+MID_NQ = [1] * 12 + [200, 77, 33, 5, 129]
 
 
 @pytest.mark.parametrize("Hq,Hkv,D,bs", [(32, 8, 128, 16), (8, 8, 128, 32), (16, 2, 64, 8),
@@ -166,7 +166,7 @@ def test_items_that_break_the_split_rule_are_flagged_and_skipped():
     """A prefill tile's item must cover all of its splits from split 0 and a decode row's item
     exactly one: forged items that do otherwise are skipped with PA_DEVERR_META, and the rows
     of the other items are still right."""
-    st = wl.make_step(16, 4, 128, 16, [3000, 2500, 700], [40, 1, 1], seed=91)
+    st = wl.make_step(16, 4, 128, 16, [5000, 4500, 700], [40, 1, 1], seed=91)
     shape = shape_of(st)
     import tests.gpu_util as gu
     kp, vp = gu.bf16_dev(st.k_pool, torch), gu.bf16_dev(st.v_pool, torch)
@@ -176,7 +176,7 @@ def test_items_that_break_the_split_rule_are_flagged_and_skipped():
     items = bd.pa_plan_step(shape, st.cu_seqlens_q, st.ctx_lens)
     pre = np.flatnonzero(items["seq"] == 0)
     dec = np.flatnonzero((items["seq"] == 1) & (items["split"] == 0))
-    assert np.all(items["n_splits"][pre] == 3)
+    assert np.all(items["n_splits"][pre] == (5000 - 1) // bd.PA_SPLIT_TOKENS + 1) and len(dec) == 4
     for forge in ("prefill_one_split", "prefill_late_start", "decode_two_splits"):
         bad = items.copy()
         if forge == "prefill_one_split":

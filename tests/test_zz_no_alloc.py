@@ -76,7 +76,7 @@ def test_static_scratch_matches_workspace_entry_point_twice(lib):
 
 
 def test_static_scratch_refuses_steps_beyond_its_size(lib):
-    # 2048 decode rows of 16k context need 2048 * 16 * 32 * 130 * 4 B of partials > 32 MiB
+    # 2048 decode rows of 16k context need 2048 * 8 * 32 * 130 * 4 B of partials > 32 MiB
     st = wl.make_step(32, 8, 128, 16, [16384] * 2, [1, 1], seed=43, with_pool=False)
     shape = bd.Shape.make(st.Hq, st.Hkv, st.D, st.block_size, st.num_blocks)
     dummy = torch.zeros(16, dtype=torch.int32, device="cuda")
