@@ -448,93 +448,136 @@ __device__ __forceinline__ void rows_init(Rows2& R, int r0, int rs, int rows_val
     }
 }
 
-// Online softmax of one 128-key tile (keys kb .. kb + 127) for the half at TMEM address tm_s
-// (lane offset included): S is read, the rows' state is updated and P, rounded to bf16, is
-// stored over the first 64 columns. alpha[sr] is the factor the row's O must be scaled by.
-__device__ __forceinline__ void softmax_half(uint32_t tm_s, int r0, int q4, int rows_valid,
+// Online softmax step of one 128-key tile (keys kb .. kb + 127) for the thread's first NR rows
+// (sr = 0 .. NR-1), taken in lockstep so that the two rows' dependency chains interleave: the
+// rows' state is updated, their P, rounded to bf16, goes to pk (packed column 4 cc + q4 of row
+// sr is pk[2 cc + sr]) and alpha[sr] is the factor the row's O must be scaled by. The
+// arithmetic of a row depends on its own scores only.
+template <int NR>
+__device__ __forceinline__ void softmax_rows(const uint32_t (&r)[64], uint32_t (&pk)[32], int q4,
                                              int kb, float c, Rows2& R, float alpha[2]) {
-    uint32_t r[64];
-    tmem_ld_16x256b_x16(tm_s, r);
-    tmem_wait_ld();
-    uint32_t pk[32];                 // P rounded to bf16, packed in pairs
+    float sv[NR][32];
+    float mx[NR];
 #pragma unroll
-    for (int sr = 0; sr < 2; ++sr) {
-        alpha[sr] = 1.f;
-        // an 8-row block with no valid row (the tail of a decode or a ragged tile) needs no
-        // softmax: its P is never used for a written output
-        if (r0 + 8 * sr >= rows_valid) {
-#pragma unroll
-            for (int cc = 0; cc < 16; ++cc) pk[2 * cc + sr] = 0u;
-            continue;
-        }
+    for (int sr = 0; sr < NR; ++sr) {
         const int pr = R.pos[sr];
         // the causal / ctx mask matters only when some key of the tile lies past some row of
-        // this block
-        const bool full = __all_sync(0xffffffffu, kb + kTileKeys - 1 <= pr);
-        float sv[32];
-        if (full) {
+        // this 8-row block
+        if (__all_sync(0xffffffffu, kb + kTileKeys - 1 <= pr)) {
 #pragma unroll
             for (int cc = 0; cc < 16; ++cc)
 #pragma unroll
-                for (int e = 0; e < 2; ++e) sv[2 * cc + e] = __uint_as_float(r[4 * cc + 2 * sr + e]);
+                for (int e = 0; e < 2; ++e)
+                    sv[sr][2 * cc + e] = __uint_as_float(r[4 * cc + 2 * sr + e]);
         } else {
 #pragma unroll
             for (int cc = 0; cc < 16; ++cc)
 #pragma unroll
                 for (int e = 0; e < 2; ++e) {
                     const int key = kb + 8 * cc + 2 * q4 + e;
-                    sv[2 * cc + e] = key <= pr ? __uint_as_float(r[4 * cc + 2 * sr + e]) : -INFINITY;
+                    sv[sr][2 * cc + e] =
+                        key <= pr ? __uint_as_float(r[4 * cc + 2 * sr + e]) : -INFINITY;
                 }
         }
-        float mx = max32(sv);
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+        mx[sr] = max32(sv[sr]);
+    }
+#pragma unroll
+    for (int sr = 0; sr < NR; ++sr) mx[sr] = fmaxf(mx[sr], __shfl_xor_sync(0xffffffffu, mx[sr], 1));
+#pragma unroll
+    for (int sr = 0; sr < NR; ++sr) mx[sr] = fmaxf(mx[sr], __shfl_xor_sync(0xffffffffu, mx[sr], 2));
+    float a[NR], m_ref[NR];
+    uint64_t nmc2[NR];
+#pragma unroll
+    for (int sr = 0; sr < NR; ++sr) {
         // The reference maximum moves only when the row's maximum grows past it by more than
         // 8 in base-2 units, so P <= 2^8 and O needs rescaling rarely; the decision depends on
         // the row's own scores alone.
         const float m_old = R.m[sr];
-        const float m_new = fmaxf(m_old, mx);
+        const float m_new = fmaxf(m_old, mx[sr]);
         const bool move = m_old == -INFINITY ? m_new != -INFINITY
                                              : __fmul_rn(__fsub_rn(m_new, m_old), c) > kLazyLog2;
-        const float m_ref = move ? m_new : m_old;
-        const float m_use = m_ref == -INFINITY ? 0.f : m_ref;
+        m_ref[sr] = move ? m_new : m_old;
+        const float m_use = m_ref[sr] == -INFINITY ? 0.f : m_ref[sr];
         // A row that has not seen a key yet (a padding row of the block, or a row whose
         // position precedes this split) has O = 0 and l = 0: its factor stays 1 so that it
         // never asks for a rescale of O.
-        const float a = (m_old == m_use || m_ref == -INFINITY)
-                            ? 1.f
-                            : ex2(__fmul_rn(__fsub_rn(m_old, m_use), c));
+        a[sr] = (m_old == m_use || m_ref[sr] == -INFINITY)
+                    ? 1.f
+                    : ex2(__fmul_rn(__fsub_rn(m_old, m_use), c));
         const float nmc = __fmul_rn(-m_use, c);
-        // p = 2^(s c - m c) for the thread's 32 keys (pairs of adjacent columns packed), then
-        // their sum as a fixed tree: the pairs' lanes are added level by level and the two
-        // lanes last
-        const uint64_t c2 = f2(c, c), nmc2 = f2(nmc, nmc);
+        nmc2[sr] = f2(nmc, nmc);
+    }
+    // p = 2^(s c - m c) for the thread's 32 keys of each row (pairs of adjacent columns
+    // packed), then their sum as a fixed tree: the pairs' lanes are added level by level and
+    // the two lanes last
+    const uint64_t c2 = f2(c, c);
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
+    for (int i = 0; i < 16; ++i)
+#pragma unroll
+        for (int sr = 0; sr < NR; ++sr) {
             float x0, x1;
-            f2_split(fma2(f2(sv[2 * i], sv[2 * i + 1]), c2, nmc2), x0, x1);
-            sv[2 * i] = ex2(x0);
-            sv[2 * i + 1] = ex2(x1);
+            f2_split(fma2(f2(sv[sr][2 * i], sv[sr][2 * i + 1]), c2, nmc2[sr]), x0, x1);
+            sv[sr][2 * i] = ex2(x0);
+            sv[sr][2 * i + 1] = ex2(x1);
         }
-        uint64_t t8[8];
+    uint64_t t8[NR][8];
 #pragma unroll
-        for (int i = 0; i < 8; ++i)
-            t8[i] = add2(f2(sv[4 * i], sv[4 * i + 1]), f2(sv[4 * i + 2], sv[4 * i + 3]));
+    for (int i = 0; i < 8; ++i)
 #pragma unroll
-        for (int w = 4; w >= 1; w >>= 1)
+        for (int sr = 0; sr < NR; ++sr)
+            t8[sr][i] = add2(f2(sv[sr][4 * i], sv[sr][4 * i + 1]),
+                             f2(sv[sr][4 * i + 2], sv[sr][4 * i + 3]));
 #pragma unroll
-            for (int i = 0; i < w; ++i) t8[i] = add2(t8[i], t8[i + w]);
-        float sum, sum_hi;
-        f2_split(t8[0], sum, sum_hi);
-        sum = __fadd_rn(sum, sum_hi);
-        sum = __fadd_rn(sum, __shfl_xor_sync(0xffffffffu, sum, 1));
-        sum = __fadd_rn(sum, __shfl_xor_sync(0xffffffffu, sum, 2));
-        R.l[sr] = __fadd_rn(__fmul_rn(R.l[sr], a), sum);
-        R.m[sr] = m_ref;
-        alpha[sr] = a;
-        // keys 8cc + 2q4 + {0, 1} -> packed column 4cc + q4 (16x128b layout)
+    for (int w = 4; w >= 1; w >>= 1)
 #pragma unroll
-        for (int cc = 0; cc < 16; ++cc) pk[2 * cc + sr] = pack_bf16(sv[2 * cc], sv[2 * cc + 1]);
+        for (int i = 0; i < w; ++i)
+#pragma unroll
+            for (int sr = 0; sr < NR; ++sr) t8[sr][i] = add2(t8[sr][i], t8[sr][i + w]);
+    float sum[NR];
+#pragma unroll
+    for (int sr = 0; sr < NR; ++sr) {
+        float lo, hi;
+        f2_split(t8[sr][0], lo, hi);
+        sum[sr] = __fadd_rn(lo, hi);
+    }
+#pragma unroll
+    for (int sr = 0; sr < NR; ++sr)
+        sum[sr] = __fadd_rn(sum[sr], __shfl_xor_sync(0xffffffffu, sum[sr], 1));
+#pragma unroll
+    for (int sr = 0; sr < NR; ++sr)
+        sum[sr] = __fadd_rn(sum[sr], __shfl_xor_sync(0xffffffffu, sum[sr], 2));
+#pragma unroll
+    for (int sr = 0; sr < NR; ++sr) {
+        R.l[sr] = __fadd_rn(__fmul_rn(R.l[sr], a[sr]), sum[sr]);
+        R.m[sr] = m_ref[sr];
+        alpha[sr] = a[sr];
+    }
+    // keys 8cc + 2q4 + {0, 1} -> packed column 4cc + q4 (16x128b layout)
+#pragma unroll
+    for (int cc = 0; cc < 16; ++cc)
+#pragma unroll
+        for (int sr = 0; sr < NR; ++sr)
+            pk[2 * cc + sr] = pack_bf16(sv[sr][2 * cc], sv[sr][2 * cc + 1]);
+}
+
+// Online softmax of one 128-key tile for the half at TMEM address tm_s (lane offset
+// included): S is read, the rows' state is updated and P, rounded to bf16, is stored over the
+// first 64 columns. alpha[sr] is the factor the row's O must be scaled by. A second 8-row
+// block with no valid row (the tail of a decode or of a ragged tile) needs no softmax: its P
+// is never used for a written output.
+__device__ __forceinline__ void softmax_half(uint32_t tm_s, int r0, int q4, int rows_valid,
+                                             int kb, float c, Rows2& R, float alpha[2]) {
+    uint32_t r[64];
+    tmem_ld_16x256b_x16(tm_s, r);
+    tmem_wait_ld();
+    uint32_t pk[32];                 // P rounded to bf16, packed in pairs
+    if (r0 + 8 >= rows_valid) {
+        softmax_rows<1>(r, pk, q4, kb, c, R, alpha);
+        alpha[1] = 1.f;
+#pragma unroll
+        for (int cc = 0; cc < 16; ++cc) pk[2 * cc + 1] = 0u;
+    } else {
+        softmax_rows<2>(r, pk, q4, kb, c, R, alpha);
     }
     // P replaces S in the first 64 columns of this tile's S buffer
     tmem_st_16x128b_x16(tm_s, pk);
