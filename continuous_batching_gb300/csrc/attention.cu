@@ -103,14 +103,14 @@ enum Bar {
     kPFull = 26,     // + S buffer: softmax (256 arrivals) -> MMA: P stored, O rescaled,
                      //   V tail zeroed (the softmax may finish tile t before the MMA has
                      //   seen tile t-1)
-    kPVDone = 28,    // + S buffer: MMA -> softmax: the PV of a tile of that parity finished
-                     //   (the softmax waits only when it rescales O, and at the epilogue)
+    kPVDone = 28,    // + S buffer: MMA -> softmax, MMA: the PV of a tile of that parity
+                     //   finished (the softmax waits only when it rescales O and at a split's
+                     //   end; the MMA before it writes the next S into the buffer P was in)
     kOFree = 30,     // + buffer: epilogue (256 arrivals) -> MMA
     kDrain = 32,
     kItemFull = 33,  // + slot (4): producer -> everyone: the slot holds the next item
     kItemEmpty = 37, // + slot: consumers (MMA 2, softmax 256, loaders 64 arrivals) -> producer
-    kPFree = 41,     // + S buffer: MMA (after PV) -> MMA: the P in that buffer has been read
-    kNumBars = 43
+    kNumBars = 41
 };
 constexpr int kHolderOff = 8 * kNumBars;          // TMEM address written by tcgen05.alloc
 constexpr int kAbortOff = kHolderOff + 4;
@@ -876,41 +876,46 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
             constexpr uint32_t idesc_s = make_idesc(kRows, kTileKeys, false);
             constexpr uint32_t idesc_o = make_idesc(kRows, D, true);
-            const auto issue_s = [&](int qb, int st, uint32_t d) {
-                const uint32_t qbase = sb + L::kQ + qb * L::kQBuf;
-                const uint32_t kbase = sb + L::kK + st * L::kKVTile;   // K ring slot
+            static_assert(L::kQHalf == L::kKVHalf, "Q and K chunks share the step offsets");
+            // This thread shares its scheduler with two softmax warps, and tcgen05.mma issue
+            // takes about as long as the tensor work, so every instruction of this loop costs
+            // tensor-pipe time: descriptors are built once per buffer, and a 16-wide step k
+            // only adds its byte offset / 16 to the start-address field (bits 0-13; shared
+            // addresses stay below 2^18, so the add never carries out of the field).
+            const uint64_t qd0 = make_sdesc(sb + L::kQ, 16, 1024);
+            const uint64_t kd0 = make_sdesc(sb + L::kK, 16, 1024);
+            constexpr uint32_t kBufStep = uint32_t(L::kKVTile) >> 4;
+            static_assert(L::kQBuf == L::kKVTile, "Q buffers and K/V slots have one size");
+            const auto issue_s = [&](uint64_t qdesc, uint64_t kdesc, uint32_t d) {
 #pragma unroll
                 for (int k = 0; k < D / 16; ++k) {
-                    const uint32_t qa = qbase + (k >> 2) * L::kQHalf + (k & 3) * 32;
-                    const uint32_t ka = kbase + (k >> 2) * L::kKVHalf + (k & 3) * 32;
-                    umma_bf16(d, make_sdesc(qa, 16, 1024), make_sdesc(ka, 16, 1024), idesc_s,
-                              k > 0);
+                    const uint32_t off = uint32_t((k >> 2) * L::kQHalf + (k & 3) * 32) >> 4;
+                    umma_bf16(d, qdesc + off, kdesc + off, idesc_s, k > 0);
                 }
             };
             // V tile: block b of the tile at b * bs * 128 * chunks bytes, its 64-column halves
             // bs * 128 bytes apart (MN-major B operand: LBO = half stride, SBO = 8-key stride)
             const uint32_t v_lbo = uint32_t(p.bs) * 128;
             const uint32_t v_sbo = p.bs >= 16 ? 1024u : uint32_t(p.bs) * 128 * L::kChunks;
-            // offset of the 16-key step k inside a V slot (block of the step, row in the
-            // block), computed once: the issuing thread shares its scheduler with the softmax
-            // warps, and a division per MMA would throttle the tensor pipe
+            const uint64_t vd0 = make_sdesc(sb + L::kV, v_lbo, v_sbo);
+            // offset / 16 of the 16-key step k inside a V slot (block of the step, row in the
+            // block), computed once
             uint32_t v_off[kTileKeys / 16];
             {
                 const int log2bs = __ffs(p.bs) - 1;
 #pragma unroll
                 for (int k = 0; k < kTileKeys / 16; ++k) {
                     const int key = 16 * k;
-                    v_off[k] = uint32_t(key >> log2bs) * (uint32_t(p.bs) * 128 * L::kChunks) +
-                               uint32_t(key & (p.bs - 1)) * 128;
+                    v_off[k] = (uint32_t(key >> log2bs) * (uint32_t(p.bs) * 128 * L::kChunks) +
+                                uint32_t(key & (p.bs - 1)) * 128) >> 4;
                 }
             }
-            const auto issue_pv = [&](int st, uint32_t p_tmem, uint32_t d, bool acc) {
-                const uint32_t vbase = sb + L::kV + st * L::kKVTile;   // V ring slot
+            const auto issue_pv = [&](uint64_t vdesc, uint32_t p_tmem, uint32_t d, bool acc) {
 #pragma unroll
                 for (int k = 0; k < kTileKeys / 16; ++k) {
                     // P of keys 16k .. 16k+15 is 8 packed columns of the S buffer
-                    umma_bf16_tmem_a(d, p_tmem + 8 * k, make_sdesc(vbase + v_off[k], v_lbo, v_sbo),
-                                     idesc_o, (acc || k > 0) ? 1u : 0u);
+                    umma_bf16_tmem_a(d, p_tmem + 8 * k, vdesc + v_off[k], idesc_o,
+                                     (acc || k > 0) ? 1u : 0u);
                 }
             };
             // Two cursors walk the same item sequence: one issues S = Q K^T for the next tile
@@ -918,9 +923,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             // as soon as the softmax has produced P. Neither waits for the other, so the
             // stage of a finished tile is released without waiting for the next tile's data.
             // Each split of an item (its tiles from a multiple of kSplitTiles on) accumulates
-            // in an O buffer of its own, alternating with the split counter sg.
+            // in an O buffer of its own, alternating with the split counter sg. vs / vph follow
+            // tc % SV and (tc / SV) & 1 (the V ring's slot and phase).
             struct Cursor {
-                int ic, jt, tc, sg;
+                int ic, jt, tc, sg, vs, vph;
                 bool have, done;
                 Item I;
             };
@@ -939,6 +945,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             };
             const auto advance = [&](Cursor& c) {
                 ++c.tc;
+                if (++c.vs == SV) {
+                    c.vs = 0;
+                    c.vph ^= 1;
+                }
                 if (++c.jt == c.I.n_tiles) {
                     c.jt = 0;
                     ++c.ic;
@@ -948,7 +958,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ++c.sg;
                 }
             };
-            Cursor cs{0, 0, 0, 0, false, false, Item{}}, cv{0, 0, 0, 0, false, false, Item{}};
+            static_assert((SK & (SK - 1)) == 0, "K ring slots: a power of two");
+            constexpr int kLog2SK = SK == 2 ? 1 : SK == 4 ? 2 : 3;
+            Cursor cs{0, 0, 0, 0, 0, 0, false, false, Item{}};
+            Cursor cv{0, 0, 0, 0, 0, 0, false, false, Item{}};
+            unsigned idle = 0;
             unsigned long long idle_since = 0;
             while (!(cs.done && cv.done)) {
                 bool progress = false;
@@ -959,40 +973,42 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const bool cont = (cv.jt & (kSplitTiles - 1)) != 0;
                 if (cv.have && cv.tc < cs.tc &&
                     mbar_test_wait(bar(kPFull + (cv.tc & 1)), (cv.tc >> 1) & 1) &&
-                    mbar_test_wait(bar(kVFull + cv.tc % SV), (cv.tc / SV) & 1) &&
+                    mbar_test_wait(bar(kVFull + cv.vs), cv.vph) &&
                     (cont || cv.sg < 2 ||
                      mbar_test_wait(bar(kOFree + (cv.sg & 1)), ((cv.sg >> 1) - 1) & 1))) {
                     tc_fence_after();
-                    const int st = cv.tc % SV;
-                    issue_pv(st, tmem + (cv.tc & 1) * 128, tmem + kTmemO + (cv.sg & 1) * 128,
-                             cont);
-                    tc_commit(bar(kPFree + (cv.tc & 1)));
-                    tc_commit(bar(kVEmpty + st));
+                    issue_pv(vd0 + uint32_t(cv.vs) * kBufStep, tmem + (cv.tc & 1) * 128,
+                             tmem + kTmemO + (cv.sg & 1) * 128, cont);
+                    tc_commit(bar(kVEmpty + cv.vs));
                     tc_commit(bar(kPVDone + (cv.tc & 1)));
                     advance(cv);
                     progress = true;
                 }
                 // S = Q K^T for the next tile: its S buffer last held the P of tile cs.tc - 2,
                 // which must have been read by that tile's PV (finished, not just issued)
+                const int ks = cs.tc & (SK - 1);
                 if (cs.have && cs.tc <= cv.tc + 1 &&
-                    (cs.tc < 2 || mbar_test_wait(bar(kPFree + (cs.tc & 1)), ((cs.tc >> 1) - 1) & 1)) &&
+                    (cs.tc < 2 || mbar_test_wait(bar(kPVDone + (cs.tc & 1)), ((cs.tc >> 1) - 1) & 1)) &&
                     (cs.jt > 0 || mbar_test_wait(bar(kQFull + (cs.ic & 1)), (cs.ic >> 1) & 1)) &&
-                    mbar_test_wait(bar(kKFull + cs.tc % SK), (cs.tc / SK) & 1)) {
+                    mbar_test_wait(bar(kKFull + ks), (cs.tc >> kLog2SK) & 1)) {
                     tc_fence_after();
-                    issue_s(cs.ic & 1, cs.tc % SK, tmem + (cs.tc & 1) * 128);
-                    tc_commit(bar(kKEmpty + cs.tc % SK));
+                    issue_s(qd0 + uint32_t(cs.ic & 1) * kBufStep, kd0 + uint32_t(ks) * kBufStep,
+                            tmem + (cs.tc & 1) * 128);
+                    tc_commit(bar(kKEmpty + ks));
                     tc_commit(bar(kSFull + (cs.tc & 1)));
                     if (cs.jt == cs.I.n_tiles - 1) tc_commit(bar(kQEmpty + (cs.ic & 1)));
                     advance(cs);
                     progress = true;
                 }
+                // the clock is read every 64 idle polls only
                 if (progress) {
-                    idle_since = 0;
-                } else {
-                    const unsigned long long now = global_ns();
-                    if (!idle_since) idle_since = now;
+                    idle = 0;
+                } else if ((++idle & 63) == 0) {
                     if (*abort_word) break;
-                    if (now - idle_since > kWaitLimitNs) {
+                    const unsigned long long now = global_ns();
+                    if (idle == 64) {
+                        idle_since = now;
+                    } else if (now - idle_since > kWaitLimitNs) {
                         *abort_word = 1;
                         break;
                     }
