@@ -152,6 +152,15 @@ __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
                  : "memory");
 }
 
+// The MMA warp runs its whole loop with all 32 lanes, so that its control flow never
+// diverges; the instructions that one thread must issue take the issuing lane as a predicate.
+__device__ __forceinline__ void mbar_arrive_if(uint32_t issue, uint32_t bar) {
+    asm volatile(
+        "{\n\t.reg .pred q;\n\t.reg .b64 st;\n\tsetp.ne.b32 q, %1, 0;\n\t"
+        "@q mbarrier.arrive.shared::cta.b64 st, [%0];\n\t}" ::"r"(bar), "r"(issue)
+        : "memory");
+}
+
 __device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
     asm volatile(
         "{\n\t.reg .b64 st;\n\tmbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1;\n\t}" ::"r"(bar),
@@ -241,9 +250,12 @@ __device__ __forceinline__ void tc_fence_before() {
 __device__ __forceinline__ void tc_fence_after() {
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
-__device__ __forceinline__ void tc_commit(uint32_t bar) {
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
-                 : "memory");
+__device__ __forceinline__ void tc_commit_if(uint32_t issue, uint32_t bar) {
+    asm volatile(
+        "{\n\t.reg .pred q;\n\tsetp.ne.b32 q, %1, 0;\n\t"
+        "@q tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(bar),
+        "r"(issue)
+        : "memory");
 }
 __device__ __forceinline__ void tmem_wait_ld() {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
@@ -253,22 +265,23 @@ __device__ __forceinline__ void tmem_wait_st() {
 }
 
 // D[tmem] (+)= A[smem] * B[smem]^T, kind::f16 (bf16 inputs, fp32 accumulator).
-__device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                          uint32_t idesc, uint32_t accumulate) {
+__device__ __forceinline__ void umma_bf16(uint32_t issue, uint32_t d_tmem, uint64_t a_desc,
+                                          uint64_t b_desc, uint32_t idesc, uint32_t accumulate) {
     asm volatile(
-        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        "{\n\t.reg .pred p;\n\t.reg .pred q;\n\tsetp.ne.b32 p, %4, 0;\n\tsetp.ne.b32 q, %5, 0;\n\t"
+        "@q tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate), "r"(issue)
         : "memory");
 }
 
 // D[tmem] (+)= A[tmem] * B[smem]^T, kind::f16; A is 128 lanes (rows) x packed bf16 pairs.
-__device__ __forceinline__ void umma_bf16_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
-                                                 uint32_t idesc, uint32_t accumulate) {
+__device__ __forceinline__ void umma_bf16_tmem_a(uint32_t issue, uint32_t d_tmem,
+                                                 uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                                 uint32_t accumulate) {
     asm volatile(
-        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        "{\n\t.reg .pred p;\n\t.reg .pred q;\n\tsetp.ne.b32 p, %4, 0;\n\tsetp.ne.b32 q, %5, 0;\n\t"
+        "@q tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate), "r"(issue)
         : "memory");
 }
 
@@ -873,11 +886,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else if (warp == 9) {
         // ------------------------------------------------------------ MMA issuer
-        if (lane == 0) {
+        // All 32 lanes run the loop (uniform control flow, no divergence on any branch); lane
+        // 0 alone issues the MMAs, commits and arrivals, through predicates.
+        {
+            const uint32_t leader = lane == 0 ? 1u : 0u;
             constexpr uint32_t idesc_s = make_idesc(kRows, kTileKeys, false);
             constexpr uint32_t idesc_o = make_idesc(kRows, D, true);
             static_assert(L::kQHalf == L::kKVHalf, "Q and K chunks share the step offsets");
-            // This thread shares its scheduler with two softmax warps, and tcgen05.mma issue
+            // This warp shares its scheduler with two softmax warps, and tcgen05.mma issue
             // takes about as long as the tensor work, so every instruction of this loop costs
             // tensor-pipe time: descriptors are built once per buffer, and a 16-wide step k
             // only adds its byte offset / 16 to the start-address field (bits 0-13; shared
@@ -890,7 +906,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int k = 0; k < D / 16; ++k) {
                     const uint32_t off = uint32_t((k >> 2) * L::kQHalf + (k & 3) * 32) >> 4;
-                    umma_bf16(d, qdesc + off, kdesc + off, idesc_s, k > 0);
+                    umma_bf16(leader, d, qdesc + off, kdesc + off, idesc_s, k > 0);
                 }
             };
             // V tile: block b of the tile at b * bs * 128 * chunks bytes, its 64-column halves
@@ -914,7 +930,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int k = 0; k < kTileKeys / 16; ++k) {
                     // P of keys 16k .. 16k+15 is 8 packed columns of the S buffer
-                    umma_bf16_tmem_a(d, p_tmem + 8 * k, vdesc + v_off[k], idesc_o,
+                    umma_bf16_tmem_a(leader, d, p_tmem + 8 * k, vdesc + v_off[k], idesc_o,
                                      (acc || k > 0) ? 1u : 0u);
                 }
             };
@@ -939,7 +955,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!mbar_test_wait(bar(kItemFull + slot), (c.ic >> 2) & 1)) return;
                 bool last;
                 c.I = slot_item(ring + slot, &last);
-                mbar_arrive(bar(kItemEmpty + slot));
+                mbar_arrive_if(leader, bar(kItemEmpty + slot));
                 c.have = !last;
                 c.done = last;
             };
@@ -979,8 +995,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tc_fence_after();
                     issue_pv(vd0 + uint32_t(cv.vs) * kBufStep, tmem + (cv.tc & 1) * 128,
                              tmem + kTmemO + (cv.sg & 1) * 128, cont);
-                    tc_commit(bar(kVEmpty + cv.vs));
-                    tc_commit(bar(kPVDone + (cv.tc & 1)));
+                    tc_commit_if(leader, bar(kVEmpty + cv.vs));
+                    tc_commit_if(leader, bar(kPVDone + (cv.tc & 1)));
                     advance(cv);
                     progress = true;
                 }
@@ -994,9 +1010,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tc_fence_after();
                     issue_s(qd0 + uint32_t(cs.ic & 1) * kBufStep, kd0 + uint32_t(ks) * kBufStep,
                             tmem + (cs.tc & 1) * 128);
-                    tc_commit(bar(kKEmpty + ks));
-                    tc_commit(bar(kSFull + (cs.tc & 1)));
-                    if (cs.jt == cs.I.n_tiles - 1) tc_commit(bar(kQEmpty + (cs.ic & 1)));
+                    tc_commit_if(leader, bar(kKEmpty + ks));
+                    tc_commit_if(leader, bar(kSFull + (cs.tc & 1)));
+                    tc_commit_if(leader && cs.jt == cs.I.n_tiles - 1, bar(kQEmpty + (cs.ic & 1)));
                     advance(cs);
                     progress = true;
                 }
@@ -1014,8 +1030,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
             }
-            // drain: every MMA this thread issued has finished before TMEM is released
-            tc_commit(bar(kDrain));
+            // drain: every MMA lane 0 issued has finished before TMEM is released
+            tc_commit_if(leader, bar(kDrain));
             wait_drain(bar(kDrain), 0);
         }
     } else if (warp >= 10) {
