@@ -93,24 +93,24 @@ struct Layout {
 // not be able to complete before the test. Barriers that a role waits on only sometimes (or
 // that another role can race ahead on) are therefore split by tile or item parity.
 enum Bar {
-    kKFull = 0,      // + slot (up to 4): TMA -> MMA (K of the tile landed)
-    kKEmpty = 4,     // + slot: MMA (after S) -> K loader
-    kVFull = 8,      // + slot (up to 6): TMA -> MMA, softmax (V of the tile landed)
-    kVEmpty = 14,    // + slot: MMA (after PV) -> V loader
-    kQFull = 20,     // + buffer: TMA -> MMA
-    kQEmpty = 22,    // + buffer: MMA (after the item's last S) -> producer
-    kSFull = 24,     // + S buffer: MMA -> softmax
-    kPFull = 26,     // + S buffer: softmax (256 arrivals) -> MMA: P stored, O rescaled,
-                     //   V tail zeroed (the softmax may finish tile t before the MMA has
-                     //   seen tile t-1)
-    kPVDone = 28,    // + S buffer: MMA -> softmax, MMA: the PV of a tile of that parity
-                     //   finished (the softmax waits only when it rescales O and at a split's
-                     //   end; the MMA before it writes the next S into the buffer P was in)
-    kOFree = 30,     // + buffer: epilogue (256 arrivals) -> MMA
-    kDrain = 32,
-    kItemFull = 33,  // + slot (4): producer -> everyone: the slot holds the next item
-    kItemEmpty = 37, // + slot: consumers (MMA 2, softmax 256, loaders 64 arrivals) -> producer
-    kNumBars = 41
+    kKFull = 0,      // + K slot (up to 4): TMA -> MMA (K of the tile landed)
+    kVFull = 4,      // + V slot (up to 6): TMA -> softmax (V of the tile landed)
+    kQFull = 10,     // + buffer: TMA -> MMA
+    kQEmpty = 12,    // + buffer: MMA (after the item's last S) -> producer
+    kSFull = 14,     // + K slot of the tile (tile % SK): MMA -> softmax, K loader: S of the
+                     //   tile finished, so its K slot is free as well
+    kPFull = 18,     // + tile parity: softmax (256 arrivals) -> MMA: P stored, O rescaled, V
+                     //   landed and its tail zeroed (the softmax may finish tile t before the
+                     //   MMA has seen tile t-1)
+    kPVDone = 20,    // + V slot of the tile (tile % SV): MMA -> softmax, MMA, V loader: the PV
+                     //   of the tile finished, so its V slot and the S buffer that held its P
+                     //   are free (the softmax waits only when it rescales O and at a split's
+                     //   end)
+    kOFree = 26,     // + buffer: epilogue (256 arrivals) -> MMA
+    kDrain = 28,
+    kItemFull = 29,  // + slot (4): producer -> everyone: the slot holds the next item
+    kItemEmpty = 33, // + slot: consumers (MMA 2, softmax 256, loaders 64 arrivals) -> producer
+    kNumBars = 37
 };
 constexpr int kHolderOff = 8 * kNumBars;          // TMEM address written by tcgen05.alloc
 constexpr int kAbortOff = kHolderOff + 4;
@@ -761,6 +761,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                       const __grid_constant__ CUtensorMap tm_qn, const Params p) {
     using L = Layout<D>;
     constexpr int SK = L::kStagesK;
+    static_assert(SK == 2 || SK == 4, "K ring slots: 2 or 4");
+    constexpr int kLog2SK = SK == 2 ? 1 : 2;
     constexpr int SV = L::kStagesV;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -974,8 +976,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ++c.sg;
                 }
             };
-            static_assert((SK & (SK - 1)) == 0, "K ring slots: a power of two");
-            constexpr int kLog2SK = SK == 2 ? 1 : SK == 4 ? 2 : 3;
             Cursor cs{0, 0, 0, 0, 0, 0, false, false, Item{}};
             Cursor cv{0, 0, 0, 0, 0, 0, false, false, Item{}};
             unsigned idle = 0;
@@ -984,34 +984,35 @@ __global__ void __launch_bounds__(kThreads, 1)
                 bool progress = false;
                 fetch(cv);
                 fetch(cs);
-                // O += P V for the oldest tile whose P is ready (the first tile of a split
-                // starts its O buffer once the epilogue has released it)
+                // O += P V for the oldest tile whose P is ready (P published implies that V
+                // has landed; the first tile of a split starts its O buffer once the epilogue
+                // has released it)
                 const bool cont = (cv.jt & (kSplitTiles - 1)) != 0;
                 if (cv.have && cv.tc < cs.tc &&
                     mbar_test_wait(bar(kPFull + (cv.tc & 1)), (cv.tc >> 1) & 1) &&
-                    mbar_test_wait(bar(kVFull + cv.vs), cv.vph) &&
                     (cont || cv.sg < 2 ||
                      mbar_test_wait(bar(kOFree + (cv.sg & 1)), ((cv.sg >> 1) - 1) & 1))) {
                     tc_fence_after();
                     issue_pv(vd0 + uint32_t(cv.vs) * kBufStep, tmem + (cv.tc & 1) * 128,
                              tmem + kTmemO + (cv.sg & 1) * 128, cont);
-                    tc_commit_if(leader, bar(kVEmpty + cv.vs));
-                    tc_commit_if(leader, bar(kPVDone + (cv.tc & 1)));
+                    tc_commit_if(leader, bar(kPVDone + cv.vs));
                     advance(cv);
                     progress = true;
                 }
                 // S = Q K^T for the next tile: its S buffer last held the P of tile cs.tc - 2,
-                // which must have been read by that tile's PV (finished, not just issued)
+                // which must have been read by that tile's PV (finished, not just issued);
+                // that PV's barrier is V slot (tc - 2) % SV, phase ((tc - 2) / SV) & 1
                 const int ks = cs.tc & (SK - 1);
+                const int pv2 = cs.vs >= 2 ? cs.vs - 2 : cs.vs - 2 + SV;
+                const int pv2ph = cs.vs >= 2 ? cs.vph : cs.vph ^ 1;
                 if (cs.have && cs.tc <= cv.tc + 1 &&
-                    (cs.tc < 2 || mbar_test_wait(bar(kPVDone + (cs.tc & 1)), ((cs.tc >> 1) - 1) & 1)) &&
+                    (cs.tc < 2 || mbar_test_wait(bar(kPVDone + pv2), pv2ph)) &&
                     (cs.jt > 0 || mbar_test_wait(bar(kQFull + (cs.ic & 1)), (cs.ic >> 1) & 1)) &&
                     mbar_test_wait(bar(kKFull + ks), (cs.tc >> kLog2SK) & 1)) {
                     tc_fence_after();
                     issue_s(qd0 + uint32_t(cs.ic & 1) * kBufStep, kd0 + uint32_t(ks) * kBufStep,
                             tmem + (cs.tc & 1) * 128);
-                    tc_commit_if(leader, bar(kKEmpty + ks));
-                    tc_commit_if(leader, bar(kSFull + (cs.tc & 1)));
+                    tc_commit_if(leader, bar(kSFull + ks));
                     tc_commit_if(leader && cs.jt == cs.I.n_tiles - 1, bar(kQEmpty + (cs.ic & 1)));
                     advance(cs);
                     progress = true;
@@ -1048,7 +1049,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         // boxes per block: K one per 64-column half; V one (both halves) when D = 128
         const int boxes_per_block = is_v ? 1 : L::kChunks;
         const int full_b = is_v ? kVFull : kKFull;
-        const int empty_b = is_v ? kVEmpty : kKEmpty;
+        // a K slot is free once S of its tile has finished, a V slot once PV has
+        const int empty_b = is_v ? kPVDone : kSFull;
         const int S = is_v ? SV : SK;                    // slots in this tensor's ring
         const uint32_t slots = sb + (is_v ? L::kV : L::kK);
         int tc = 0, ic = 0;
@@ -1151,7 +1153,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (jin == 0) rows_init(R, r0, rs, I.rows_valid, I.pos0, p.g);
                 const int ob = sg & 1;
                 const uint32_t tm_o = tmem + kTmemO + ob * 128 + lanes;
-                if (!(ok = wait_bounded(bar(kSFull + (tc & 1)), (tc >> 1) & 1, abort_word)))
+                if (!(ok = wait_bounded(bar(kSFull + (tc & (SK - 1))), (tc >> kLog2SK) & 1,
+                                        abort_word)))
                     break;
                 tc_fence_after();
                 const int kb = I.k_begin + jt * kTileKeys;
@@ -1161,18 +1164,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // and only in warps where some row's running maximum moved
                 const bool need = alpha[0] != 1.f || alpha[1] != 1.f;
                 if (jin > 0 && __any_sync(0xffffffffu, need)) {
-                    if (!(ok = wait_bounded(bar(kPVDone + ((tc - 1) & 1)), ((tc - 1) >> 1) & 1,
+                    if (!(ok = wait_bounded(bar(kPVDone + (tc - 1) % SV), ((tc - 1) / SV) & 1,
                                             abort_word)))
                         break;
                     tc_fence_after();
                     rescale_half<D>(tm_o, alpha);
                 }
                 tmem_wait_st();
+                // V of the tile has landed before P is published (the PV issue relies on it);
                 // keys at or beyond ctx are stale or were never loaded: give them zero values
                 // so that their (zero) probabilities contribute exact zeros
+                if (!(ok = wait_bounded(bar(kVFull + tc % SV), (tc / SV) & 1, abort_word))) break;
                 if (kb + kTileKeys > I.ctx) {
-                    if (!(ok = wait_bounded(bar(kVFull + tc % SV), (tc / SV) & 1, abort_word)))
-                        break;
                     zero_v_tail<D>(sb + L::kV + (tc % SV) * L::kKVTile, kb, I.ctx, p.bs, tid, 256);
                     // the zeros were written through the generic proxy and the PV MMA reads
                     // them through the async proxy: only these tiles need the proxy fence
@@ -1193,7 +1196,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     continue;
                 }
-                if (!(ok = wait_bounded(bar(kPVDone + (tc & 1)), (tc >> 1) & 1, abort_word)))
+                if (!(ok = wait_bounded(bar(kPVDone + tc % SV), (tc / SV) & 1, abort_word)))
                     break;
                 tc_fence_after();
                 if (I.n_splits > 1) {
