@@ -15,11 +15,16 @@ What it computes (plain definitions, numpy, fp64 for all floating point):
   row over its own keys, GQA map q_head // (Hq/Hkv), scale 1/sqrt(D)
   (same page, Design / paged.py "'row' = one SDPA per query row over exactly
   its own keys"; Tensor parallelism / Design "Blocked map q_head // group").
+* ``fp8``: the float8_e4m3fn KV cache with per-tensor scales: write codes =
+  e4m3(x / s) rounded to nearest (ties to even code), saturating at +-448; read
+  value = code * s ("P3: native paged-KV continuous-batching sampler", Review,
+  kv_dtype item; "Finish RL Training Faster: Bitwise-Consistent, ...", 4.2).
 * ``allocator``: LIFO block allocator with refcounts, all-or-nothing capacity
   growth, read-only shared prefix blocks and the layout check
   (same page, Design / paged.py; Evidence item 4).
 
-Pins (tests marked ``not gpu``): storage-layout equivalence with a plain
+Pins (tests marked ``not gpu``): the e4m3 format's fixed points, exhaustive round
+trips and ties, and torch's float8_e4m3fn cast as a library cross-check; storage-layout equivalence with a plain
 contiguous cache ("Optional paged KV cache (vLLM-style) — v1 design",
 Implementation order step 1 and step 3), brute force on tiny inputs, closed
 forms, a library cross-check (torch scaled_dot_product_attention in fp64), the
