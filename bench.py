@@ -57,8 +57,8 @@ MIXED = ("mixed ragged step: 48 decode rows (ctx lognormal median 3000, cap 1638
          "prefill segments of 512 rows at prior offsets {0,512,4096,9000}, T=2096, seed 2")
 
 
-def kv_bytes(st: wl.Step) -> int:
-    return int(st.ctx_lens.astype(np.int64).sum()) * 2 * st.Hkv * st.D * 2
+def kv_bytes(st: wl.Step, elem_bytes: int = 2) -> int:
+    return int(st.ctx_lens.astype(np.int64).sum()) * 2 * st.Hkv * st.D * elem_bytes
 
 
 def prefill_flops(st: wl.Step) -> float:
@@ -199,20 +199,36 @@ class ClockSampler:
 class GpuStep:
     """Device-resident inputs for one workload plus the public-API runner."""
 
-    def __init__(self, st: wl.Step, torch, bd):
+    def __init__(self, st: wl.Step, torch, bd, kv: str = "bf16"):
         self.st, self.torch, self.bd = st, torch, bd
         dev = lambda a: torch.from_numpy(a.view(np.int16)).cuda().view(torch.bfloat16)
         self.shape = bd.Shape.make(st.Hq, st.Hkv, st.D, st.block_size, st.num_blocks)
         self.kp, self.vp = dev(st.k_pool), dev(st.v_pool)
+        self.kv_scales = None
+        if kv == "fp8":
+            # the cache holds float8_e4m3fn codes with per-tensor scales (amax / 448); the
+            # synthetic bf16 pool is quantised once, before timing, by the library's own write
+            ks = float(self.kp.abs().max().float().item()) / 448.0
+            vs = float(self.vp.abs().max().float().item()) / 448.0
+            self.kv_scales = (float(np.float32(ks)), float(np.float32(vs)))
+            n = st.num_blocks * st.block_size
+            kp8 = torch.empty(self.kp.shape, dtype=torch.uint8, device="cuda")
+            vp8 = torch.empty(self.vp.shape, dtype=torch.uint8, device="cuda")
+            all_slots = torch.arange(n, dtype=torch.int32, device="cuda")
+            bd.paged_kv_write_fp8(self.kp.view(n, st.Hkv, st.D), self.vp.view(n, st.Hkv, st.D),
+                                  all_slots, kp8, vp8, *self.kv_scales, self.shape)
+            torch.cuda.synchronize()
+            self.kp, self.vp = kp8, vp8
         self.q, self.kn, self.vn = dev(st.q), dev(st.k_new), dev(st.v_new)
         self.out = torch.empty((st.T, st.Hq, st.D), dtype=torch.bfloat16, device="cuda")
-        self.runner = bd.StepRunner(self.shape).prepare(st.cu_seqlens_q, st.ctx_lens,
-                                                        st.block_table)
+        self.runner = bd.StepRunner(self.shape, kv_scales=self.kv_scales).prepare(
+            st.cu_seqlens_q, st.ctx_lens, st.block_table)
         # the timed steps replay CUDA graphs of the same calls (fixed buffers, padded plan):
         # one graph for the KV write, one for the attention kernels
         lim = bd.StepLimits(B=st.B, T=st.T, max_blocks=st.block_table.shape[1],
                             max_ctx=int(st.ctx_lens.max()))
-        self.graph_runner = bd.StepRunner(self.shape, limits=lim).prepare(
+        self.graph_runner = bd.StepRunner(self.shape, limits=lim,
+                                          kv_scales=self.kv_scales).prepare(
             st.cu_seqlens_q, st.ctx_lens, st.block_table)
         self.g_write = self.graph_runner.capture(self.q, self.kn, self.vn, self.kp, self.vp,
                                                  self.out, attend=False)
@@ -326,7 +342,8 @@ def run_ours(args) -> dict:
 
     name = args.workload
     st = make_workload(name, rank)
-    g = GpuStep(st, torch, bd)
+    fp8_kv = args.kv == "fp8"
+    g = GpuStep(st, torch, bd, args.kv)
     flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
 
     def barrier():
@@ -349,7 +366,7 @@ def run_ours(args) -> dict:
         if not args.no_clocks:
             load_for(g, torch, 1.0)
     tokens = name in TOKEN_WORKLOADS
-    bytes_step = kv_bytes(st)
+    bytes_step = kv_bytes(st, 1 if fp8_kv else 2)
     units_step = float(st.T) if tokens else float(bytes_step)
     unit = "tokens/s" if tokens else UNIT
     scale = 1.0 if tokens else 1e-9
@@ -375,16 +392,17 @@ def run_ours(args) -> dict:
         achieved = prefill_flops(st) / (attn_avg * 1e-3) / 1e12
         roof = {"bound": "tensor", "achieved": round(achieved, 1), "peak": peaks["bf16_tflops"],
                 "unit": "TFLOP/s", "frac": round(achieved / peaks["bf16_tflops"], 4),
-                "traffic": measured_traffic(name),
+                "traffic": measured_traffic(name + ("_fp8" if fp8_kv else "")),
                 "kernel": "paged_attention_step (tile routine), causal algorithmic FLOPs "
                           "4*D*Hq*(n*o + n(n+1)/2)",
                 "peak_src": peaks["src"] + " (burst)"}
     else:
-        roof_bytes = unique_kv_bytes(st) if name == "prefix" else bytes_step
+        roof_bytes = (unique_kv_bytes(st) // (2 if fp8_kv else 1) if name == "prefix"
+                      else bytes_step)
         achieved = roof_bytes / (attn_avg * 1e-3) / 1e9
         roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
                 "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
-                "traffic": measured_traffic(name),
+                "traffic": measured_traffic(name + ("_fp8" if fp8_kv else "")),
                 "kernel": "paged_attention_step (attention kernels + split combine)",
                 "peak_src": peaks["src"]}
         if name == "prefix":
@@ -395,7 +413,7 @@ def run_ours(args) -> dict:
     mixed = None
     if name == "decode" and not args.no_mixed:
         sm = wl.make_config("mixed", seed=rank_seed("mixed", rank))
-        gm = GpuStep(sm, torch, bd)
+        gm = GpuStep(sm, torch, bd, args.kv)
         m_step, m_attn = time_steps(gm, torch, args.steps, args.warmup, flush)
         mm = statistics.mean(m_step)
         pf = prefill_flops(sm)
@@ -408,9 +426,12 @@ def run_ours(args) -> dict:
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": unit, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16 (K/V as fp8 e4m3 codes, f16 MMA operands)" if fp8_kv else "bf16",
         "data": "synthetic",
         "config": {"workload": WORKLOADS[name], "kv_bytes_per_step": bytes_step, "T": st.T,
+                   "kv_cache": ("float8_e4m3fn codes, per-tensor scales "
+                                f"{g.kv_scales[0]:.6g} / {g.kv_scales[1]:.6g}") if fp8_kv else "bf16",
                    "l2": f"inputs larger than L2 ({bytes_step / 1e9:.2f} GB K/V) and L2 flushed "
                          "by a 256 MiB write between timed steps",
                    "parallelism": f"replicas{world}"},
@@ -424,7 +445,7 @@ def run_ours(args) -> dict:
     }
     if mixed:
         line["ragged_step"] = mixed
-    if rank == 0 and not args.no_cpu_baseline:
+    if rank == 0 and not args.no_cpu_baseline and not fp8_kv:
         line["cpu_baseline"] = cpu_baseline(st, budget_s=args.cpu_budget, tokens=tokens)
     if world > 1:
         import torch.distributed as dist
@@ -511,6 +532,9 @@ def main(argv=None):
     ap.add_argument("--workload", default="decode", choices=sorted(WORKLOADS),
                     help="synthetic workload of the timed step (decode is the headline)")
     ap.add_argument("--no-mixed", action="store_true")
+    ap.add_argument("--kv", default="bf16", choices=["bf16", "fp8"],
+                    help="KV cache type: bf16, or float8_e4m3fn codes with per-tensor scales "
+                         "(head_dim 128 workloads)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--no-clocks", action="store_true",

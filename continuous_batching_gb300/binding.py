@@ -137,6 +137,11 @@ def load() -> C.CDLL:
         _sig(lib, "paged_attention_step", C.c_int32,
              [_vp, _vp, _vp, _vp, C.c_int32, _vp, _vp, C.c_int32, C.c_int32, C.c_int32,
               _vp, C.c_int32, _vp, C.c_size_t, _vp, sp, _vp, _vp])
+        _sig(lib, "paged_kv_write_fp8", C.c_int32,
+             [_vp, _vp, _vp, C.c_int32, _vp, _vp, C.c_float, C.c_float, sp, _vp, _vp])
+        _sig(lib, "paged_attention_step_fp8", C.c_int32,
+             [_vp, _vp, _vp, _vp, C.c_int32, _vp, _vp, C.c_int32, C.c_int32, C.c_int32,
+              _vp, C.c_int32, C.c_float, C.c_float, _vp, C.c_size_t, _vp, sp, _vp, _vp])
         _lib = lib
         return lib
 
@@ -430,6 +435,33 @@ def paged_attention_step(q, k_pool, v_pool, block_table, cu_seqlens_q, ctx_lens,
         "paged_attention_step")
 
 
+def paged_kv_write_fp8(k_new, v_new, slot_mapping, k_pool, v_pool, k_scale: float,
+                       v_scale: float, shape: Shape, err=None, stream=None) -> None:
+    """bf16 k_new / v_new [T, Hkv, D] quantised into uint8 float8_e4m3fn pools with per-tensor
+    scales (code = e4m3(x / scale))."""
+    T = int(slot_mapping.shape[0])
+    _check(load().paged_kv_write_fp8(_dev(k_new), _dev(v_new), _dev(slot_mapping), T,
+                                     _dev(k_pool), _dev(v_pool), float(k_scale), float(v_scale),
+                                     C.byref(shape), _dev(err), _stream(stream)),
+           "paged_kv_write_fp8")
+
+
+def paged_attention_step_fp8(q, k_pool, v_pool, block_table, cu_seqlens_q, ctx_lens,
+                             max_ctx: int, items, k_scale: float, v_scale: float, workspace,
+                             out, shape: Shape, err=None, stream=None) -> None:
+    """paged_attention_step over uint8 float8_e4m3fn pools with per-tensor scales."""
+    B = int(ctx_lens.shape[0])
+    T = int(q.shape[0])
+    n_items = int(items.numel() // 8)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(load().paged_attention_step_fp8(
+        _dev(q), _dev(k_pool), _dev(v_pool), _dev(block_table), int(block_table.shape[1]),
+        _dev(cu_seqlens_q), _dev(ctx_lens), B, T, int(max_ctx), _dev(items), n_items,
+        float(k_scale), float(v_scale), _dev(workspace), ws_bytes, _dev(out), C.byref(shape),
+        _dev(err), _stream(stream)),
+        "paged_attention_step_fp8")
+
+
 class StepLimits:
     """Fixed sizes of a step that is captured in a CUDA graph: B sequences, T query rows,
     block-table width max_blocks and a context bound max_ctx. Every step prepared under these
@@ -448,12 +480,16 @@ class StepRunner:
     With limits (StepLimits), prepare() writes the metadata into fixed device buffers in place
     (the plan padded to a fixed item count with n_q == 0 items, the table padded with -1), so
     capture() can record run() once in a CUDA graph and replay() runs any later prepared step.
+    With kv_scales = (k_scale, v_scale) the pools are uint8 float8_e4m3fn caches and the fp8
+    write and read entry points run instead.
     """
 
-    def __init__(self, shape: Shape, device="cuda", limits: Optional[StepLimits] = None):
+    def __init__(self, shape: Shape, device="cuda", limits: Optional[StepLimits] = None,
+                 kv_scales: Optional[tuple] = None):
         import torch
         self.torch = torch
         self.shape = shape
+        self.kv_scales = None if kv_scales is None else (float(kv_scales[0]), float(kv_scales[1]))
         self.device = torch.device(device)
         self.limits = limits
         self.ws = None
@@ -543,9 +579,18 @@ class StepRunner:
         self.graph.replay()
 
     def write(self, k_new, v_new, k_pool, v_pool, stream=None):
+        if self.kv_scales is not None:
+            paged_kv_write_fp8(k_new, v_new, self.slots, k_pool, v_pool, *self.kv_scales,
+                               self.shape, self.err, stream)
+            return
         paged_kv_write(k_new, v_new, self.slots, k_pool, v_pool, self.shape, self.err, stream)
 
     def attend(self, q, k_pool, v_pool, out, stream=None):
+        if self.kv_scales is not None:
+            paged_attention_step_fp8(q, k_pool, v_pool, self.table, self.cu, self.ctx,
+                                     self.max_ctx, self.items, *self.kv_scales, self.ws, out,
+                                     self.shape, self.err, stream)
+            return
         paged_attention_step(q, k_pool, v_pool, self.table, self.cu, self.ctx, self.max_ctx,
                              self.items, self.ws, out, self.shape, self.err, stream)
 

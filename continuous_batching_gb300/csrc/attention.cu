@@ -110,7 +110,12 @@ enum Bar {
     kDrain = 28,
     kItemFull = 29,  // + slot (4): producer -> everyone: the slot holds the next item
     kItemEmpty = 33, // + slot: consumers (MMA 2, softmax 256, loaders 64 arrivals) -> producer
-    kNumBars = 37
+    // fp8 cache only: the tile's codes have been expanded to f16 in place (32 arrivals: the
+    // loader or producer warp), which the MMA and softmax wait for instead of the TMA barrier
+    kKReady = 37,    // + K slot
+    kVReady = 41,    // + V slot
+    kQReady = 47,    // + Q buffer
+    kNumBars = 49
 };
 constexpr int kHolderOff = 8 * kNumBars;          // TMEM address written by tcgen05.alloc
 constexpr int kAbortOff = kHolderOff + 4;
@@ -134,7 +139,9 @@ struct Params {
     __nv_bfloat16* out;
     int32_t* err;
     int32_t n_items, B, T, max_blocks, max_splits, Hq, Hkv, g, bs, num_blocks;
-    float c;            // log2(e) / sqrt(D): softmax works in base 2 on raw scores
+    float c;            // log2(e) / sqrt(D) (times the K scale of an fp8 cache): softmax
+                        // works in base 2 on raw scores
+    float v_scale;      // V scale of an fp8 cache (1 for bf16): out = O * (rcp(l) * v_scale)
 };
 
 // ----------------------------------------------------------------- PTX wrappers
@@ -286,11 +293,11 @@ __device__ __forceinline__ void umma_bf16_tmem_a(uint32_t issue, uint32_t d_tmem
 }
 
 // Instruction descriptor, kind::f16: fp32 accumulator (bits 4-5 = 1), A and B bf16 (bits 7-9,
-// 10-12 = 1), A K-major, B K-major or MN-major (bit 16), N >> 3 at bits 17-22, M >> 4 at
-// bits 24-28.
-__host__ __device__ constexpr uint32_t make_idesc(int M, int N, bool b_mn_major) {
-    return (1u << 4) | (1u << 7) | (1u << 10) | ((b_mn_major ? 1u : 0u) << 16) |
-           (uint32_t(N >> 3) << 17) | (uint32_t(M >> 4) << 24);
+// 10-12 = 1) or both f16 (0), A K-major, B K-major or MN-major (bit 16), N >> 3 at bits
+// 17-22, M >> 4 at bits 24-28.
+__host__ __device__ constexpr uint32_t make_idesc(int M, int N, bool b_mn_major, bool f16) {
+    return (1u << 4) | ((f16 ? 0u : 1u) << 7) | ((f16 ? 0u : 1u) << 10) |
+           ((b_mn_major ? 1u : 0u) << 16) | (uint32_t(N >> 3) << 17) | (uint32_t(M >> 4) << 24);
 }
 
 // Shared-memory matrix descriptor: start address >> 4 (bits 0-13), leading-dimension byte
@@ -358,16 +365,53 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
     return *reinterpret_cast<uint32_t*>(&v);
 }
 
-__device__ __forceinline__ void st_shared_u32(uint32_t addr, uint32_t v) {
-    asm volatile("st.shared.b32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+__device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
+    uint32_t r;
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+__device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
+    uint4 v;
+    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "r"(addr)
+                 : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
+                                             uint32_t d) {
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
+                 "r"(d)
+                 : "memory");
+}
+
+// Two e4m3 codes (lower byte first) -> two f16 (exact: every e4m3 value is an f16 value).
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_codes) {
+    uint32_t r;
+    asm("{\n\t.reg .b16 h;\n\tcvt.u16.u32 h, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, h;\n\t}"
+        : "=r"(r)
+        : "r"(two_codes));
+    return r;
+}
+
+// Two bf16 (lower half first) -> two f16, rounded to nearest and saturated at +-65504.
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t w) {
+    uint32_t r;
+    asm("cvt.rn.satfinite.f16x2.f32 %0, %1, %2;"
+        : "=r"(r)
+        : "f"(__uint_as_float(w & 0xFFFF0000u)), "f"(__uint_as_float(w << 16)));
+    return r;
 }
 __device__ __forceinline__ void st_shared_zero16(uint32_t addr) {
     asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};" ::"r"(addr), "r"(0) : "memory");
 }
 
-// Offset of 16-byte chunk `chunk` (0..7) of row `row` in a 128-byte-swizzled tile.
-__device__ __forceinline__ uint32_t swz(int row, int chunk) {
-    return uint32_t(row * 128 + ((chunk ^ (row & 7)) << 4));
+// Address of 16-byte chunk j of the 128-byte row at shared address row_addr, in the 128-byte
+// swizzle TMA and the MMA use (the chunk index XOR address bits 7-9).
+__device__ __forceinline__ uint32_t swz128(uint32_t row_addr, int j) {
+    return row_addr + (uint32_t(j ^ int((row_addr >> 7) & 7)) << 4);
 }
 
 
@@ -466,7 +510,7 @@ __device__ __forceinline__ void rows_init(Rows2& R, int r0, int rs, int rows_val
 // rows' state is updated, their P, rounded to bf16, goes to pk (packed column 4 cc + q4 of row
 // sr is pk[2 cc + sr]) and alpha[sr] is the factor the row's O must be scaled by. The
 // arithmetic of a row depends on its own scores only.
-template <int NR>
+template <int NR, bool H16>
 __device__ __forceinline__ void softmax_rows(const uint32_t (&r)[64], uint32_t (&pk)[32], int q4,
                                              int kb, float c, Rows2& R, float alpha[2]) {
     float sv[NR][32];
@@ -570,14 +614,17 @@ __device__ __forceinline__ void softmax_rows(const uint32_t (&r)[64], uint32_t (
     for (int cc = 0; cc < 16; ++cc)
 #pragma unroll
         for (int sr = 0; sr < NR; ++sr)
-            pk[2 * cc + sr] = pack_bf16(sv[sr][2 * cc], sv[sr][2 * cc + 1]);
+            pk[2 * cc + sr] = H16 ? pack_f16(sv[sr][2 * cc], sv[sr][2 * cc + 1])
+                                  : pack_bf16(sv[sr][2 * cc], sv[sr][2 * cc + 1]);
 }
 
 // Online softmax of one 128-key tile for the half at TMEM address tm_s (lane offset
 // included): S is read, the rows' state is updated and P, rounded to bf16, is stored over the
-// first 64 columns. alpha[sr] is the factor the row's O must be scaled by. A second 8-row
-// block with no valid row (the tail of a decode or of a ragged tile) needs no softmax: its P
-// is never used for a written output.
+// first 64 columns (as f16 when H16, the operand type of an fp8 cache's MMAs, else bf16).
+// alpha[sr] is the factor the row's O must be scaled by. A second 8-row block with no valid
+// row (the tail of a decode or of a ragged tile) needs no softmax: its P is never used for a
+// written output.
+template <bool H16>
 __device__ __forceinline__ void softmax_half(uint32_t tm_s, int r0, int q4, int rows_valid,
                                              int kb, float c, Rows2& R, float alpha[2]) {
     uint32_t r[64];
@@ -585,12 +632,12 @@ __device__ __forceinline__ void softmax_half(uint32_t tm_s, int r0, int q4, int 
     tmem_wait_ld();
     uint32_t pk[32];                 // P rounded to bf16, packed in pairs
     if (r0 + 8 >= rows_valid) {
-        softmax_rows<1>(r, pk, q4, kb, c, R, alpha);
+        softmax_rows<1, H16>(r, pk, q4, kb, c, R, alpha);
         alpha[1] = 1.f;
 #pragma unroll
         for (int cc = 0; cc < 16; ++cc) pk[2 * cc + 1] = 0u;
     } else {
-        softmax_rows<2>(r, pk, q4, kb, c, R, alpha);
+        softmax_rows<2, H16>(r, pk, q4, kb, c, R, alpha);
     }
     // P replaces S in the first 64 columns of this tile's S buffer
     tmem_st_16x128b_x16(tm_s, pk);
@@ -619,7 +666,7 @@ __device__ __forceinline__ void rescale_half(uint32_t tm_o, const float alpha[2]
 }
 
 // Epilogue of the half, O already in registers: a row whose position lies in one split is
-// finished here (out = bf16(O * rcp(l))); a row spanning several splits stores this split's
+// finished here (out = bf16(O * (rcp(l) * v_scale))); a row spanning several splits stores this split's
 // partial (acc = O, m, l) for the fixed-order combine. Rows are those of a tile whose first
 // row is token q_start at position pos0 (rows_valid rows, g heads per token).
 template <int D>
@@ -636,7 +683,7 @@ __device__ __forceinline__ void store_half(const Params& p, const uint32_t* o, i
         const int tok = q_start + row / p.g;
         const int head = kvh * p.g + row % p.g;
         if (nsp == 1) {
-            const float inv = __frcp_rn(R.l[sr]);
+            const float inv = __fmul_rn(__frcp_rn(R.l[sr]), p.v_scale);
             __nv_bfloat16* dst = p.out + (int64_t(tok) * p.Hq + head) * D;
 #pragma unroll
             for (int cc = 0; cc < D / 8; ++cc) {
@@ -671,7 +718,7 @@ struct Fold2 {
 // ACC = ACC a + O b. A row whose position precedes the split has no keys in it and keeps its
 // running result unchanged, as the combine would not fold it. Unless fin, the result goes to
 // tm_p, whose buffer holds the running result from here on; with fin the rows are finished,
-// out = bf16(ACC * rcp(L)), like every other row of the step.
+// out = bf16(ACC * (rcp(L) * v_scale)), like every other row of the step.
 template <int D>
 __device__ __forceinline__ void fold_half(const Params& p, uint32_t tm_a, uint32_t tm_p, int r0,
                                           int rs, int q4, int rows_valid, int q_start, int kvh,
@@ -690,7 +737,7 @@ __device__ __forceinline__ void fold_half(const Params& p, uint32_t tm_a, uint32
             F.L[sr] = __fadd_rn(__fmul_rn(F.L[sr], fa[sr]), __fmul_rn(R.l[sr], fb[sr]));
             F.M[sr] = mn;
         }
-        inv[sr] = fin ? __frcp_rn(F.L[sr]) : 0.f;
+        inv[sr] = fin ? __fmul_rn(__frcp_rn(F.L[sr]), p.v_scale) : 0.f;
     }
 #pragma unroll
     for (int h = 0; h < D / 64; ++h) {
@@ -753,16 +800,23 @@ __device__ __forceinline__ void zero_v_tail(uint32_t vb, int kb, int ctx, int bs
     }
 }
 
-template <int D>
+// F8: the pools hold float8_e4m3fn codes (head_dim 128 only); the loaders expand each tile
+// to f16 in shared memory, Q is rounded to f16, and the MMAs take f16 operands.
+template <int D, bool F8>
 __global__ void __launch_bounds__(kThreads, 1)
     paged_attn_kernel(const __grid_constant__ CUtensorMap tm_k,
                       const __grid_constant__ CUtensorMap tm_v,
                       const __grid_constant__ CUtensorMap tm_q1,
                       const __grid_constant__ CUtensorMap tm_qn, const Params p) {
     using L = Layout<D>;
+    static_assert(!F8 || D == 128, "the fp8 cache is supported at head_dim 128");
     constexpr int SK = L::kStagesK;
     static_assert(SK == 2 || SK == 4, "K ring slots: 2 or 4");
     constexpr int kLog2SK = SK == 2 ? 1 : 2;
+    // what the MMA and softmax wait for: the TMA landing, or (fp8 cache) the f16 expansion
+    constexpr int kKUse = F8 ? kKReady : kKFull;
+    constexpr int kVUse = F8 ? kVReady : kVFull;
+    constexpr int kQUse = F8 ? kQReady : kQFull;
     constexpr int SV = L::kStagesV;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -779,6 +833,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(bars + 8 * b,
                       (b == kPFull || b == kPFull + 1 || b == kOFree || b == kOFree + 1) ? 256
                       : (b >= kItemEmpty && b < kItemEmpty + 4)       ? 2 + 256 + 64
+                      : b >= kKReady                                  ? 32
                                                                       : 1);
         *abort_word = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -878,6 +933,26 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             ok = __shfl_sync(0xffffffffu, ok, 0);
             if (!ok) break;
+            if constexpr (F8) {
+                // the MMAs of an fp8 cache take f16 operands: once Q has landed, round it to
+                // f16 in place (every 16-byte chunk keeps its position, so the swizzle holds)
+                if (lane == 0) ok = wait_bounded(bar(kQFull + qb), (ic >> 1) & 1, abort_word);
+                ok = __shfl_sync(0xffffffffu, ok, 0);
+                if (!ok) break;
+                const int rows = I.n_q == 1 ? p.g : kRows;
+                const uint32_t qbase = sb + L::kQ + qb * L::kQBuf;
+                for (int i = lane; i < rows * 8 * L::kChunks; i += 32) {
+                    const int r = i / (8 * L::kChunks);
+                    const int rem = i - r * 8 * L::kChunks;
+                    const uint32_t a = qbase + (rem >> 3) * L::kQHalf + r * 128 + (rem & 7) * 16;
+                    const uint4 v = ld_shared_v4(a);
+                    st_shared_v4(a, bf16x2_to_f16x2(v.x), bf16x2_to_f16x2(v.y),
+                                 bf16x2_to_f16x2(v.z), bf16x2_to_f16x2(v.w));
+                }
+                fence_proxy_async();
+                __syncwarp();
+                mbar_arrive(bar(kQReady + qb));          // all 32 lanes arrive
+            }
             ++round;
             ++ic;
         }
@@ -892,8 +967,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         // 0 alone issues the MMAs, commits and arrivals, through predicates.
         {
             const uint32_t leader = lane == 0 ? 1u : 0u;
-            constexpr uint32_t idesc_s = make_idesc(kRows, kTileKeys, false);
-            constexpr uint32_t idesc_o = make_idesc(kRows, D, true);
+            constexpr uint32_t idesc_s = make_idesc(kRows, kTileKeys, false, F8);
+            constexpr uint32_t idesc_o = make_idesc(kRows, D, true, F8);
             static_assert(L::kQHalf == L::kKVHalf, "Q and K chunks share the step offsets");
             // This warp shares its scheduler with two softmax warps, and tcgen05.mma issue
             // takes about as long as the tensor work, so every instruction of this loop costs
@@ -1007,8 +1082,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int pv2ph = cs.vs >= 2 ? cs.vph : cs.vph ^ 1;
                 if (cs.have && cs.tc <= cv.tc + 1 &&
                     (cs.tc < 2 || mbar_test_wait(bar(kPVDone + pv2), pv2ph)) &&
-                    (cs.jt > 0 || mbar_test_wait(bar(kQFull + (cs.ic & 1)), (cs.ic >> 1) & 1)) &&
-                    mbar_test_wait(bar(kKFull + ks), (cs.tc >> kLog2SK) & 1)) {
+                    (cs.jt > 0 || mbar_test_wait(bar(kQUse + (cs.ic & 1)), (cs.ic >> 1) & 1)) &&
+                    mbar_test_wait(bar(kKUse + ks), (cs.tc >> kLog2SK) & 1)) {
                     tc_fence_after();
                     issue_s(qd0 + uint32_t(cs.ic & 1) * kBufStep, kd0 + uint32_t(ks) * kBufStep,
                             tmem + (cs.tc & 1) * 128);
@@ -1055,6 +1130,47 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t slots = sb + (is_v ? L::kV : L::kK);
         int tc = 0, ic = 0;
         int ok = 1;
+        // fp8 cache: shared address of 16-byte-chunk row R of a slot's 64-column half h (K:
+        // [half][key row]; V: [block][half][row]). The codes of row R land unswizzled at
+        // row_base(R, 1), exactly where the row's second f16 half goes, so a row can be
+        // expanded in place once its 128 code bytes have been read.
+        const auto row_base = [&](uint32_t slot, int R, int h) -> uint32_t {
+            return is_v ? slot + uint32_t(R >> log2bs) * uint32_t(p.bs * 256) +
+                              uint32_t(h * p.bs * 128) + uint32_t(R & (p.bs - 1)) * 128
+                        : slot + uint32_t(h * L::kKVHalf) + uint32_t(R) * 128;
+        };
+        int pend_tc = -1, pend_rows = 0;       // fp8: the tile whose codes still need expanding
+        // waits for tile t's codes, expands its first `rows` rows to f16 (8 lanes per row,
+        // 4 rows per pass) and publishes it on the ready barrier
+        const auto expand = [&](int t, int rows) {
+            const int st = t % S;
+            if (lane == 0) ok = wait_bounded(bar(full_b + st), (t / S) & 1, abort_word);
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (!ok) return;
+            const uint32_t slot = slots + st * L::kKVTile;
+            const int c = lane & 7;             // code chunk: columns 16 c .. 16 c + 15
+            for (int R0 = 0; R0 < rows; R0 += 4) {
+                const int R = R0 + (lane >> 3);
+                const bool act = R < rows;
+                uint4 v = make_uint4(0u, 0u, 0u, 0u);
+                if (act) v = ld_shared_v4(row_base(slot, R, 1) + c * 16);
+                __syncwarp();                   // the row is read before its staging is reused
+                if (act) {
+                    const uint32_t rb = row_base(slot, R, c >> 2);
+                    const int j0 = (2 * c) & 7;
+                    st_shared_v4(swz128(rb, j0), e4m3x2_to_f16x2(v.x & 0xFFFFu),
+                                 e4m3x2_to_f16x2(v.x >> 16), e4m3x2_to_f16x2(v.y & 0xFFFFu),
+                                 e4m3x2_to_f16x2(v.y >> 16));
+                    st_shared_v4(swz128(rb, j0 + 1), e4m3x2_to_f16x2(v.z & 0xFFFFu),
+                                 e4m3x2_to_f16x2(v.z >> 16), e4m3x2_to_f16x2(v.w & 0xFFFFu),
+                                 e4m3x2_to_f16x2(v.w >> 16));
+                }
+            }
+            // generic-proxy writes, read by the MMA through the async proxy
+            fence_proxy_async();
+            __syncwarp();
+            mbar_arrive(bar((is_v ? kVReady : kKReady) + st));     // all 32 lanes arrive
+        };
         for (;;) {
             if (lane == 0)
                 ok = wait_bounded(bar(kItemFull + (ic & 3)), (ic >> 2) & 1, abort_word);
@@ -1094,11 +1210,27 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int kb = I.k_begin + jt * kTileKeys;
                 const int key_hi = min(kb + kTileKeys, I.ctx);   // real keys end at ctx
                 const int nblk = (key_hi - kb + p.bs - 1) >> log2bs;
+                const uint32_t dst = slots + st * L::kKVTile;
+                const int e0 = (kb - sk) >> log2bs;
+                if constexpr (F8) {
+                    // one box of bs rows x 128 code bytes per block, into the second halves
+                    if (lane == 0) mbar_expect_tx(bar(full_b + st), uint32_t(nblk) * p.bs * 128);
+                    __syncwarp();
+                    for (int b = lane; b < nblk; b += 32)
+                        tma_load_3d(row_base(dst, b * p.bs, 1), tmap, bar(full_b + st), 0, I.kvh,
+                                    tbl[e0 + b] * p.bs);
+                    // the tile before this one has had time to land: expand it now
+                    if (pend_tc >= 0) {
+                        expand(pend_tc, pend_rows);
+                        if (!ok) break;
+                    }
+                    pend_tc = tc;
+                    pend_rows = nblk * p.bs;
+                    continue;
+                }
                 if (lane == 0)
                     mbar_expect_tx(bar(full_b + st), uint32_t(nblk) * p.bs * 128 * L::kChunks);
                 __syncwarp();
-                const uint32_t dst = slots + st * L::kKVTile;
-                const int e0 = (kb - sk) >> log2bs;
                 for (int j = lane; j < nblk * boxes_per_block; j += 32) {
                     const int b = j / boxes_per_block;
                     const int r = j - b * boxes_per_block;
@@ -1118,6 +1250,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = __shfl_sync(0xffffffffu, ok, 0);
             if (!ok) break;
             ++ic;
+        }
+        if constexpr (F8) {
+            if (ok && pend_tc >= 0) expand(pend_tc, pend_rows);      // the CTA's last tile
         }
         if (lane == 0) {
             // never leave with copies in flight into this CTA's shared memory
@@ -1159,7 +1294,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_after();
                 const int kb = I.k_begin + jt * kTileKeys;
                 float alpha[2] = {1.f, 1.f};
-                if (on) softmax_half(tmem + (tc & 1) * 128 + lanes, r0, q4, I.rows_valid, kb, c, R, alpha);
+                if (on)
+                    softmax_half<F8>(tmem + (tc & 1) * 128 + lanes, r0, q4, I.rows_valid, kb, c, R,
+                                     alpha);
                 // O belongs to the previous tile's PV until it has finished: rescale only then,
                 // and only in warps where some row's running maximum moved
                 const bool need = alpha[0] != 1.f || alpha[1] != 1.f;
@@ -1174,7 +1311,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // V of the tile has landed before P is published (the PV issue relies on it);
                 // keys at or beyond ctx are stale or were never loaded: give them zero values
                 // so that their (zero) probabilities contribute exact zeros
-                if (!(ok = wait_bounded(bar(kVFull + tc % SV), (tc / SV) & 1, abort_word))) break;
+                if (!(ok = wait_bounded(bar(kVUse + tc % SV), (tc / SV) & 1, abort_word))) break;
                 if (kb + kTileKeys > I.ctx) {
                     zero_v_tail<D>(sb + L::kV + (tc % SV) * L::kKVTile, kb, I.ctx, p.bs, tid, 256);
                     // the zeros were written through the generic proxy and the PV MMA reads
@@ -1241,7 +1378,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 // For every (decode row, q head) whose row spans more than one split: fold the partials of
 // splits 0, 1, ... in ascending order, starting from split 0's (m, l, acc) as they are:
 //   M' = max(M, m_s), a = 2^((M - M') c), b = 2^((m_s - M') c),
-//   L = L a + l_s b, ACC = ACC a + acc_s b;  out = bf16_rne(ACC * rcp_rn(L)).
+//   L = L a + l_s b, ACC = ACC a + acc_s b;  out = bf16_rne(ACC * (rcp_rn(L) * v_scale))
+// (v_scale is 1 for a bf16 cache, so that product is rcp_rn(L) exactly).
 // A row with one split is finished by the attention kernel with the same two roundings, and
 // so is every row of a sequence with several query rows, whose item folds its own splits in
 // this order (fold_half). One thread per (sequence, q head, 4 columns); sequences with other
@@ -1254,7 +1392,7 @@ template <int D>
 __global__ void __launch_bounds__(256)
     combine_kernel(const float* __restrict__ ws_acc, const float* __restrict__ ws_ml,
                    const int32_t* __restrict__ cu, const int32_t* __restrict__ ctx, int32_t B,
-                   int32_t T, int32_t Hq, int32_t max_splits, float c,
+                   int32_t T, int32_t Hq, int32_t max_splits, float c, float v_scale,
                    __nv_bfloat16* __restrict__ out) {
     constexpr int kCols = 4;                  // columns per thread (one float4)
     constexpr int kUnits = D / kCols;         // threads per (row, q head)
@@ -1312,7 +1450,7 @@ __global__ void __launch_bounds__(256)
             M = mn;
         }
     }
-    const float inv = __frcp_rn(Lsum);
+    const float inv = __fmul_rn(__frcp_rn(Lsum), v_scale);
     __nv_bfloat16* dst = out + (tok * Hq + head) * D + col;
     *reinterpret_cast<uint2*>(dst) =
         make_uint2(pack_bf16(__fmul_rn(acc[0], inv), __fmul_rn(acc[1], inv)),
@@ -1350,6 +1488,23 @@ int32_t make_map(CUtensorMap* m, const void* base, int D, int heads, int64_t row
     return r == CUDA_SUCCESS ? PA_OK : PA_ERR_CUDA;
 }
 
+// An fp8 pool as {D, heads, rows} bytes: one box is one block of one KV head, bs rows of D
+// code bytes, unswizzled (the loader expands it in shared memory).
+int32_t make_map_codes(CUtensorMap* m, const void* base, int D, int heads, int64_t rows,
+                       int box_rows) {
+    auto fn = encode_fn();
+    if (!fn) return PA_ERR_CUDA;
+    const cuuint64_t dims[3] = {cuuint64_t(D), cuuint64_t(heads), cuuint64_t(rows)};
+    const cuuint64_t strides[2] = {cuuint64_t(D), cuuint64_t(heads) * D};
+    const cuuint32_t box[3] = {cuuint32_t(D), 1, cuuint32_t(box_rows)};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    const CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims,
+                          strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? PA_OK : PA_ERR_CUDA;
+}
+
 struct Maps {
     CUtensorMap k, v, q1, qn;
 };
@@ -1358,13 +1513,22 @@ struct Maps {
 // 64-column chunk. q as {D, Hq, T}: a decode item's box is its g heads of one token, a prefill
 // item's box is g heads of 128/g tokens (rows past the item are not used; past T they read 0).
 int32_t make_maps(Maps* m, const void* q, const void* k_pool, const void* v_pool, int32_t T,
-                  const pa_shape* s) {
+                  const pa_shape* s, bool fp8) {
     const int D = s->head_dim;
     const int g = s->num_q_heads / s->num_kv_heads;
     const int64_t rows = int64_t(s->num_blocks) * s->block_size;
     int32_t st;
-    if ((st = make_map(&m->k, k_pool, D, s->num_kv_heads, rows, 1, s->block_size))) return st;
-    if (D == 128) {
+    if (fp8) {
+        if ((st = make_map_codes(&m->k, k_pool, D, s->num_kv_heads, rows, s->block_size)))
+            return st;
+        if ((st = make_map_codes(&m->v, v_pool, D, s->num_kv_heads, rows, s->block_size)))
+            return st;
+    } else if ((st = make_map(&m->k, k_pool, D, s->num_kv_heads, rows, 1, s->block_size))) {
+        return st;
+    }
+    if (fp8) {
+        // both code maps are built above
+    } else if (D == 128) {
         // {64, rows, half, head}: one box holds both 64-column halves of one block, halves
         // outermost, so that each half's rows are contiguous in shared memory
         auto fn = encode_fn();
@@ -1401,14 +1565,14 @@ int32_t sm_count_for_current_device(int* n) {
     return PA_OK;
 }
 
-template <int D>
+template <int D, bool F8>
 int32_t launch(const Maps& maps, const Params& prm, int32_t max_ctx, cudaStream_t stream) {
     static int attr_device = -1;          // device the shared-memory limit was raised on
     int dev = 0;
     int32_t st = note_cuda(cudaGetDevice(&dev));
     if (st) return st;
     if (attr_device != dev) {
-        st = note_cuda(cudaFuncSetAttribute(paged_attn_kernel<D>,
+        st = note_cuda(cudaFuncSetAttribute(paged_attn_kernel<D, F8>,
                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
                                             Layout<D>::kAlloc));
         if (st) return st;
@@ -1430,7 +1594,7 @@ int32_t launch(const Maps& maps, const Params& prm, int32_t max_ctx, cudaStream_
     cfg.stream = stream;
     cfg.attrs = pdl;
     cfg.numAttrs = 1;
-    st = note_cuda(cudaLaunchKernelEx(&cfg, paged_attn_kernel<D>, maps.k, maps.v, maps.q1,
+    st = note_cuda(cudaLaunchKernelEx(&cfg, paged_attn_kernel<D, F8>, maps.k, maps.v, maps.q1,
                                       maps.qn, prm));
     if (st) return st;
     if (max_ctx > kSplit) {
@@ -1440,7 +1604,7 @@ int32_t launch(const Maps& maps, const Params& prm, int32_t max_ctx, cudaStream_
         cfg.dynamicSmemBytes = 0;
         st = note_cuda(cudaLaunchKernelEx(&cfg, combine_kernel<D>, (const float*)prm.ws_acc,
                                           (const float*)prm.ws_ml, prm.cu, prm.ctx, prm.B, prm.T,
-                                          prm.Hq, prm.max_splits, prm.c, prm.out));
+                                          prm.Hq, prm.max_splits, prm.c, prm.v_scale, prm.out));
     }
     return st;
 }
@@ -1450,7 +1614,8 @@ int32_t prepare_step(const void* q, const void* k_pool, const void* v_pool,
                      const int32_t* block_table, int32_t max_blocks, const int32_t* cu_seqlens_q,
                      const int32_t* ctx_lens, int32_t B, int32_t T, int32_t max_ctx,
                      const pa_work_item* items, int32_t n_items, void* out,
-                     const pa_shape* shape, int32_t* err_flag, Maps* maps, Params* prm) {
+                     const pa_shape* shape, int32_t* err_flag, Maps* maps, Params* prm,
+                     bool fp8 = false) {
     int32_t st = check_shape(shape);
     if (st) return st;
     if (B < 0 || T < 0 || n_items < 0 || max_ctx < 0 || max_blocks < 0) return PA_ERR_INVALID;
@@ -1460,7 +1625,7 @@ int32_t prepare_step(const void* q, const void* k_pool, const void* v_pool,
     if ((reinterpret_cast<uintptr_t>(k_pool) | reinterpret_cast<uintptr_t>(v_pool) |
          reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(out)) & 15)
         return PA_ERR_INVALID;
-    if ((st = make_maps(maps, q, k_pool, v_pool, T, shape))) return st;
+    if ((st = make_maps(maps, q, k_pool, v_pool, T, shape, fp8))) return st;
     const int D = shape->head_dim;
     prm->k_pool = static_cast<const __nv_bfloat16*>(k_pool);
     prm->v_pool = static_cast<const __nv_bfloat16*>(v_pool);
@@ -1483,6 +1648,7 @@ int32_t prepare_step(const void* q, const void* k_pool, const void* v_pool,
     prm->bs = shape->block_size;
     prm->num_blocks = shape->num_blocks;
     prm->c = float(1.4426950408889634 / std::sqrt(double(D)));
+    prm->v_scale = 1.f;
     return PA_OK;
 }
 
@@ -1514,8 +1680,39 @@ extern "C" int32_t paged_attention_step(const void* q, const void* k_pool, const
                            T, max_ctx, items, n_items, out, shape, err_flag, &maps, &prm)))
         return st;
     point_workspace(&prm, static_cast<float*>(workspace), T, shape->num_q_heads, shape->head_dim);
-    if (shape->head_dim == 128) return launch<128>(maps, prm, max_ctx, stream);
-    return launch<64>(maps, prm, max_ctx, stream);
+    if (shape->head_dim == 128) return launch<128, false>(maps, prm, max_ctx, stream);
+    return launch<64, false>(maps, prm, max_ctx, stream);
+}
+
+// FP8 KV cache: the same step over float8_e4m3fn pools with per-tensor scales. The K scale
+// joins the softmax constant (scores are taken on the codes' values), the V scale the final
+// factor of every row: out = bf16(O * (rcp(l) * v_scale)).
+extern "C" int32_t paged_attention_step_fp8(const void* q, const void* k_pool, const void* v_pool,
+                                            const int32_t* block_table, int32_t max_blocks,
+                                            const int32_t* cu_seqlens_q, const int32_t* ctx_lens,
+                                            int32_t B, int32_t T, int32_t max_ctx,
+                                            const pa_work_item* items, int32_t n_items,
+                                            float k_scale, float v_scale, void* workspace,
+                                            size_t ws_bytes, void* out, const pa_shape* shape,
+                                            int32_t* err_flag, pa_stream_t stream) {
+    int32_t st = check_shape(shape);
+    if (st) return st;
+    if (shape->head_dim != 128) return PA_ERR_SHAPE;
+    if (B < 0 || T < 0 || n_items < 0 || max_ctx < 0 || max_blocks < 0) return PA_ERR_INVALID;
+    if (!(k_scale > 0.f) || !(v_scale > 0.f) || !(k_scale < INFINITY) || !(v_scale < INFINITY))
+        return PA_ERR_INVALID;
+    if (T == 0 || n_items == 0) return PA_OK;
+    if (max_ctx > kSplit && (!workspace || ws_bytes < pa_workspace_bytes(shape, T, max_ctx)))
+        return PA_ERR_WORKSPACE;
+    Maps maps;
+    Params prm;
+    if ((st = prepare_step(q, k_pool, v_pool, block_table, max_blocks, cu_seqlens_q, ctx_lens, B,
+                           T, max_ctx, items, n_items, out, shape, err_flag, &maps, &prm, true)))
+        return st;
+    prm.c = prm.c * k_scale;
+    prm.v_scale = v_scale;
+    point_workspace(&prm, static_cast<float*>(workspace), T, shape->num_q_heads, shape->head_dim);
+    return launch<128, true>(maps, prm, max_ctx, stream);
 }
 
 // ------------------------------------------- allocation-free variant of the attention step
@@ -1574,6 +1771,6 @@ extern "C" int32_t paged_attention_step_static_scratch(
     float* scratch = nullptr;
     if ((st = static_scratch_for_current_device(&scratch))) return st;
     point_workspace(&prm, scratch, T, shape->num_q_heads, shape->head_dim);
-    if (shape->head_dim == 128) return launch<128>(maps, prm, max_ctx, stream);
-    return launch<64>(maps, prm, max_ctx, stream);
+    if (shape->head_dim == 128) return launch<128, false>(maps, prm, max_ctx, stream);
+    return launch<64, false>(maps, prm, max_ctx, stream);
 }

@@ -327,6 +327,37 @@ int32_t paged_attention_step(const void* q, const void* k_pool, const void* v_po
                              void* workspace, size_t ws_bytes, void* out,
                              const pa_shape* shape, int32_t* err_flag, pa_stream_t stream);
 
+/* ------------------------------------------------------------------ FP8 KV cache
+ * K and V stored as float8_e4m3fn codes (1 byte each) with one scale per tensor ("P3: native
+ * paged-KV continuous-batching sampler", Review, kv_dtype item: dequantised on read; unscaled
+ * e4m3 is lossy, so per-tensor scales. "Finish RL Training Faster: Bitwise-Consistent, ...",
+ * 4.2: FP8 storage, one shared write path, one read path for prefill and decode).
+ * Pools: uint8 [num_blocks, block_size, Hkv, D], the same geometry as the bf16 pools. The
+ * value a code stands for is code_value * scale; the caller chooses the scales (for example
+ * amax / 448 of what it writes) and passes the same ones to every write and read of a pool.
+ *
+ * Write: code = e4m3(x / scale) for each element, the division in fp32 with IEEE rounding,
+ * then rounding to the nearest e4m3 value (ties to even) with finite values beyond 448
+ * saturating to +-448. Arguments as paged_kv_write, plus k_scale, v_scale (finite, > 0; else
+ * PA_ERR_INVALID). Hkv * D must be a multiple of 16. */
+int32_t paged_kv_write_fp8(const void* k_new, const void* v_new, const int32_t* slot_mapping,
+                           int32_t T, void* k_pool, void* v_pool, float k_scale, float v_scale,
+                           const pa_shape* shape, int32_t* err_flag, pa_stream_t stream);
+
+/* Read: paged_attention_step over fp8 pools (head_dim 128 only, else PA_ERR_SHAPE). Every row
+ * runs the same tile routine as on a bf16 cache, with f16 operands: the codes are expanded to
+ * f16 exactly in shared memory, Q is rounded to f16 (saturating at +-65504) and P is rounded
+ * to f16. The K scale multiplies the softmax constant; out = bf16(O * (rcp(l) * v_scale)).
+ * Bit identity across batch mixes and between prefill and decode holds within the fp8 path.
+ * Arguments, items, workspace and errors as paged_attention_step, plus k_scale, v_scale. */
+int32_t paged_attention_step_fp8(const void* q, const void* k_pool, const void* v_pool,
+                                 const int32_t* block_table, int32_t max_blocks,
+                                 const int32_t* cu_seqlens_q, const int32_t* ctx_lens,
+                                 int32_t B, int32_t T, int32_t max_ctx,
+                                 const pa_work_item* items, int32_t n_items, float k_scale,
+                                 float v_scale, void* workspace, size_t ws_bytes, void* out,
+                                 const pa_shape* shape, int32_t* err_flag, pa_stream_t stream);
+
 /* Allocation-free variant of paged_attention_step (no counterpart on the pages: it is a
  * deployment convenience of this library). Same arguments, meaning and result as
  * paged_attention_step, minus the workspace: the split partials go to a fixed device array of

@@ -137,3 +137,10 @@ def test_dequantised_attention_reduces_to_the_bf16_oracle_on_exact_values():
     got = pa.attention(q, kf, vf, table, cu, ctx, 4)
     want = pa.attention(q, kb, vb, table, cu, ctx, 4)
     assert np.array_equal(got, want)
+
+
+def test_table_quantiser_equals_the_per_element_definition():
+    rng = np.random.default_rng(14)
+    bits = rng.integers(0, 65536, size=200000).astype(np.uint16)
+    for s in (0.011, 1.0, 3.0, 1e-30, 7e30):
+        assert np.array_equal(fp8.quantize(bits, s), fp8._quantize_values(bits, s))
