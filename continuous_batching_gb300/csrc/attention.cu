@@ -60,6 +60,9 @@ constexpr int kRows = PA_ROWS;
 constexpr int kTileKeys = PA_TILE_KEYS;
 constexpr int kSplit = PA_SPLIT_TOKENS;
 constexpr int kThreads = 384;
+// an fp8 cache adds two warps (12: K, 13: V) that expand the codes the loaders bring in
+template <bool F8>
+constexpr int kThreadsFor = F8 ? kThreads + 64 : kThreads;
 constexpr uint32_t kTmemCols = 512;     // S0 [0,128) S1 [128,256) O0 [256,384) O1 [384,512)
 constexpr uint32_t kTmemO = 256;
 constexpr unsigned long long kWaitLimitNs = 1000000000ull;   // one second per wait
@@ -387,13 +390,45 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
                  : "memory");
 }
 
-// Two e4m3 codes (lower byte first) -> two f16 (exact: every e4m3 value is an f16 value).
-__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_codes) {
-    uint32_t r;
-    asm("{\n\t.reg .b16 h;\n\tcvt.u16.u32 h, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, h;\n\t}"
-        : "=r"(r)
-        : "r"(two_codes));
-    return r;
+// Four e4m3 codes (lowest byte first) -> two f16x2 words (exact: every e4m3 value is an f16
+// value).
+__device__ __forceinline__ void e4m3x4_to_f16x4(uint32_t w, uint32_t& lo, uint32_t& hi) {
+    asm("{\n\t.reg .b16 a, b;\n\tmov.b32 {a, b}, %2;\n\t"
+        "cvt.rn.f16x2.e4m3x2 %0, a;\n\tcvt.rn.f16x2.e4m3x2 %1, b;\n\t}"
+        : "=r"(lo), "=r"(hi)
+        : "r"(w));
+}
+
+// Expands the first `rows` 128-byte code rows of a K or V ring slot to f16 in place (8 lanes
+// per row, 4 rows per pass). Row R's codes sit unswizzled where the row's second 64-column
+// f16 half goes (K slots: [half][key row]; V slots: [block][half][row]); its f16 halves go
+// to the 128-byte swizzled rows TMA would have written. A row is read by its 8 lanes before
+// any lane writes over it.
+__device__ __forceinline__ void expand_codes(uint32_t slot, int rows, bool is_v, int bs,
+                                             int log2bs, int lane) {
+    const int c = lane & 7;                    // code chunk: columns 16 c .. 16 c + 15
+    const int j0 = 2 * (c & 3);                // its first f16 chunk within the half
+    for (int R = lane >> 3; R - (lane >> 3) < rows; R += 4) {
+        const bool act = R < rows;
+        const uint32_t b0 = is_v ? slot + uint32_t(R >> log2bs) * uint32_t(bs * 256) +
+                                       uint32_t(R & (bs - 1)) * 128
+                                 : slot + uint32_t(R) * 128;
+        const uint32_t b1 = b0 + (is_v ? uint32_t(bs * 128) : uint32_t(kTileKeys * 128));
+        uint4 v = make_uint4(0u, 0u, 0u, 0u);
+        if (act) v = ld_shared_v4(b1 + c * 16);
+        __syncwarp();
+        if (act) {
+            uint32_t f[8];
+            e4m3x4_to_f16x4(v.x, f[0], f[1]);
+            e4m3x4_to_f16x4(v.y, f[2], f[3]);
+            e4m3x4_to_f16x4(v.z, f[4], f[5]);
+            e4m3x4_to_f16x4(v.w, f[6], f[7]);
+            const uint32_t rb = (c >> 2) ? b1 : b0;
+            const int x = R & 7;               // 128-byte swizzle: chunk ^ (row & 7)
+            st_shared_v4(rb + (uint32_t(j0 ^ x) << 4), f[0], f[1], f[2], f[3]);
+            st_shared_v4(rb + (uint32_t((j0 + 1) ^ x) << 4), f[4], f[5], f[6], f[7]);
+        }
+    }
 }
 
 // Two bf16 (lower half first) -> two f16, rounded to nearest and saturated at +-65504.
@@ -407,13 +442,6 @@ __device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t w) {
 __device__ __forceinline__ void st_shared_zero16(uint32_t addr) {
     asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};" ::"r"(addr), "r"(0) : "memory");
 }
-
-// Address of 16-byte chunk j of the 128-byte row at shared address row_addr, in the 128-byte
-// swizzle TMA and the MMA use (the chunk index XOR address bits 7-9).
-__device__ __forceinline__ uint32_t swz128(uint32_t row_addr, int j) {
-    return row_addr + (uint32_t(j ^ int((row_addr >> 7) & 7)) << 4);
-}
-
 
 // One work item, checked against the metadata it points at (device data). A bad item does
 // no work in any role and raises PA_DEVERR_META (reported by the softmax warps).
@@ -803,7 +831,7 @@ __device__ __forceinline__ void zero_v_tail(uint32_t vb, int kb, int ctx, int bs
 // F8: the pools hold float8_e4m3fn codes (head_dim 128 only); the loaders expand each tile
 // to f16 in shared memory, Q is rounded to f16, and the MMAs take f16 operands.
 template <int D, bool F8>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreadsFor<F8>, 1)
     paged_attn_kernel(const __grid_constant__ CUtensorMap tm_k,
                       const __grid_constant__ CUtensorMap tm_v,
                       const __grid_constant__ CUtensorMap tm_q1,
@@ -832,7 +860,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int b = 0; b < kNumBars; ++b)
             mbar_init(bars + 8 * b,
                       (b == kPFull || b == kPFull + 1 || b == kOFree || b == kOFree + 1) ? 256
-                      : (b >= kItemEmpty && b < kItemEmpty + 4)       ? 2 + 256 + 64
+                      : (b >= kItemEmpty && b < kItemEmpty + 4)       ? 2 + 256 + 64 + (F8 ? 64 : 0)
                       : b >= kKReady                                  ? 32
                                                                       : 1);
         *abort_word = 0;
@@ -1110,7 +1138,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_commit_if(leader, bar(kDrain));
             wait_drain(bar(kDrain), 0);
         }
-    } else if (warp >= 10) {
+    } else if (warp == 10 || warp == 11) {
         // ------------------------------------------------------------ K (warp 6) / V (warp 7)
         const bool is_v = warp == 11;
         int32_t* tbl = reinterpret_cast<int32_t*>(smem + L::kBar + kTableOff) +
@@ -1130,46 +1158,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t slots = sb + (is_v ? L::kV : L::kK);
         int tc = 0, ic = 0;
         int ok = 1;
-        // fp8 cache: shared address of 16-byte-chunk row R of a slot's 64-column half h (K:
-        // [half][key row]; V: [block][half][row]). The codes of row R land unswizzled at
-        // row_base(R, 1), exactly where the row's second f16 half goes, so a row can be
-        // expanded in place once its 128 code bytes have been read.
+        // fp8 cache: shared address of row R of a slot's 64-column half h (K: [half][key row];
+        // V: [block][half][row]). The codes of row R land unswizzled at row_base(R, 1), where
+        // the row's second f16 half goes, and are expanded there (expand_codes).
         const auto row_base = [&](uint32_t slot, int R, int h) -> uint32_t {
             return is_v ? slot + uint32_t(R >> log2bs) * uint32_t(p.bs * 256) +
                               uint32_t(h * p.bs * 128) + uint32_t(R & (p.bs - 1)) * 128
                         : slot + uint32_t(h * L::kKVHalf) + uint32_t(R) * 128;
-        };
-        int pend_tc = -1, pend_rows = 0;       // fp8: the tile whose codes still need expanding
-        // waits for tile t's codes, expands its first `rows` rows to f16 (8 lanes per row,
-        // 4 rows per pass) and publishes it on the ready barrier
-        const auto expand = [&](int t, int rows) {
-            const int st = t % S;
-            if (lane == 0) ok = wait_bounded(bar(full_b + st), (t / S) & 1, abort_word);
-            ok = __shfl_sync(0xffffffffu, ok, 0);
-            if (!ok) return;
-            const uint32_t slot = slots + st * L::kKVTile;
-            const int c = lane & 7;             // code chunk: columns 16 c .. 16 c + 15
-            for (int R0 = 0; R0 < rows; R0 += 4) {
-                const int R = R0 + (lane >> 3);
-                const bool act = R < rows;
-                uint4 v = make_uint4(0u, 0u, 0u, 0u);
-                if (act) v = ld_shared_v4(row_base(slot, R, 1) + c * 16);
-                __syncwarp();                   // the row is read before its staging is reused
-                if (act) {
-                    const uint32_t rb = row_base(slot, R, c >> 2);
-                    const int j0 = (2 * c) & 7;
-                    st_shared_v4(swz128(rb, j0), e4m3x2_to_f16x2(v.x & 0xFFFFu),
-                                 e4m3x2_to_f16x2(v.x >> 16), e4m3x2_to_f16x2(v.y & 0xFFFFu),
-                                 e4m3x2_to_f16x2(v.y >> 16));
-                    st_shared_v4(swz128(rb, j0 + 1), e4m3x2_to_f16x2(v.z & 0xFFFFu),
-                                 e4m3x2_to_f16x2(v.z >> 16), e4m3x2_to_f16x2(v.w & 0xFFFFu),
-                                 e4m3x2_to_f16x2(v.w >> 16));
-                }
-            }
-            // generic-proxy writes, read by the MMA through the async proxy
-            fence_proxy_async();
-            __syncwarp();
-            mbar_arrive(bar((is_v ? kVReady : kKReady) + st));     // all 32 lanes arrive
         };
         for (;;) {
             if (lane == 0)
@@ -1219,14 +1214,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int b = lane; b < nblk; b += 32)
                         tma_load_3d(row_base(dst, b * p.bs, 1), tmap, bar(full_b + st), 0, I.kvh,
                                     tbl[e0 + b] * p.bs);
-                    // the tile before this one has had time to land: expand it now
-                    if (pend_tc >= 0) {
-                        expand(pend_tc, pend_rows);
-                        if (!ok) break;
-                    }
-                    pend_tc = tc;
-                    pend_rows = nblk * p.bs;
-                    continue;
+                    continue;                   // the expander warp takes it from here
                 }
                 if (lane == 0)
                     mbar_expect_tx(bar(full_b + st), uint32_t(nblk) * p.bs * 128 * L::kChunks);
@@ -1251,13 +1239,53 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!ok) break;
             ++ic;
         }
-        if constexpr (F8) {
-            if (ok && pend_tc >= 0) expand(pend_tc, pend_rows);      // the CTA's last tile
-        }
         if (lane == 0) {
             // never leave with copies in flight into this CTA's shared memory
             for (int t = max(0, tc - S); t < tc; ++t)
                 wait_drain(bar(full_b + t % S), (t / S) & 1);
+        }
+    } else if (warp >= 12) {
+        // ------------------------------------------------------------ fp8 expanders (12: K, 13: V)
+        // Walk the same tiles as the loaders: wait for a tile's codes to land, expand them to
+        // f16 in place and publish the tile on its ready barrier (which the MMA, for K, or
+        // the softmax, for V, waits for instead of the TMA barrier).
+        if constexpr (F8) {
+            const bool is_v = warp == 13;
+            const volatile ItemSlot* ring =
+                reinterpret_cast<const volatile ItemSlot*>(smem + L::kBar + kRingOff);
+            const int log2bs = __ffs(p.bs) - 1;
+            const int full_b = is_v ? kVFull : kKFull;
+            const int ready_b = is_v ? kVReady : kKReady;
+            const int S = is_v ? SV : SK;
+            const uint32_t slots = sb + (is_v ? L::kV : L::kK);
+            int tc = 0, ic = 0;
+            int ok = 1;
+            for (;;) {
+                if (lane == 0)
+                    ok = wait_bounded(bar(kItemFull + (ic & 3)), (ic >> 2) & 1, abort_word);
+                ok = __shfl_sync(0xffffffffu, ok, 0);
+                if (!ok) break;
+                bool last;
+                const Item I = slot_item(ring + (ic & 3), &last);
+                mbar_arrive(bar(kItemEmpty + (ic & 3)));     // all 32 lanes arrive
+                if (last) break;
+                for (int jt = 0; jt < I.n_tiles; ++jt, ++tc) {
+                    const int st = tc % S;
+                    if (lane == 0) ok = wait_bounded(bar(full_b + st), (tc / S) & 1, abort_word);
+                    ok = __shfl_sync(0xffffffffu, ok, 0);
+                    if (!ok) break;
+                    const int kb = I.k_begin + jt * kTileKeys;
+                    const int key_hi = min(kb + kTileKeys, I.ctx);
+                    const int rows = ((key_hi - kb + p.bs - 1) >> log2bs) * p.bs;
+                    expand_codes(slots + st * L::kKVTile, rows, is_v, p.bs, log2bs, lane);
+                    // generic-proxy writes, read by the MMA through the async proxy
+                    fence_proxy_async();
+                    __syncwarp();
+                    mbar_arrive(bar(ready_b + st));             // all 32 lanes arrive
+                }
+                if (!ok) break;
+                ++ic;
+            }
         }
     } else {
         // ------------------------------------------------------------ softmax warps 0-7
@@ -1589,7 +1617,7 @@ int32_t launch(const Maps& maps, const Params& prm, int32_t max_ctx, cudaStream_
     pdl[0].val.programmaticStreamSerializationAllowed = 1;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(unsigned(grid));
-    cfg.blockDim = dim3(kThreads);
+    cfg.blockDim = dim3(kThreadsFor<F8>);
     cfg.dynamicSmemBytes = Layout<D>::kAlloc;
     cfg.stream = stream;
     cfg.attrs = pdl;
