@@ -60,9 +60,10 @@ constexpr int kRows = PA_ROWS;
 constexpr int kTileKeys = PA_TILE_KEYS;
 constexpr int kSplit = PA_SPLIT_TOKENS;
 constexpr int kThreads = 384;
-// an fp8 cache adds two warps (12: K, 13: V) that expand the codes the loaders bring in
+// an fp8 cache adds four warps (12, 14: K; 13, 15: V) that expand the codes the loaders bring
+// in, each pair taking half of every tile's rows
 template <bool F8>
-constexpr int kThreadsFor = F8 ? kThreads + 64 : kThreads;
+constexpr int kThreadsFor = F8 ? kThreads + 128 : kThreads;
 constexpr uint32_t kTmemCols = 512;     // S0 [0,128) S1 [128,256) O0 [256,384) O1 [384,512)
 constexpr uint32_t kTmemO = 256;
 constexpr unsigned long long kWaitLimitNs = 1000000000ull;   // one second per wait
@@ -113,8 +114,9 @@ enum Bar {
     kDrain = 28,
     kItemFull = 29,  // + slot (4): producer -> everyone: the slot holds the next item
     kItemEmpty = 33, // + slot: consumers (MMA 2, softmax 256, loaders 64 arrivals) -> producer
-    // fp8 cache only: the tile's codes have been expanded to f16 in place (32 arrivals: the
-    // loader or producer warp), which the MMA and softmax wait for instead of the TMA barrier
+    // fp8 cache only: the tile's codes have been expanded to f16 in place (K, V: 64 arrivals from
+    // the two expander warps; Q: 32 from the producer), which the MMA and softmax wait for
+    // instead of the TMA barrier
     kKReady = 37,    // + K slot
     kVReady = 41,    // + V slot
     kQReady = 47,    // + Q buffer
@@ -399,16 +401,16 @@ __device__ __forceinline__ void e4m3x4_to_f16x4(uint32_t w, uint32_t& lo, uint32
         : "r"(w));
 }
 
-// Expands the first `rows` 128-byte code rows of a K or V ring slot to f16 in place (8 lanes
+// Expands the 128-byte code rows r_begin .. rows - 1 of a K or V ring slot to f16 in place (8 lanes
 // per row, 4 rows per pass). Row R's codes sit unswizzled where the row's second 64-column
 // f16 half goes (K slots: [half][key row]; V slots: [block][half][row]); its f16 halves go
 // to the 128-byte swizzled rows TMA would have written. A row is read by its 8 lanes before
 // any lane writes over it.
-__device__ __forceinline__ void expand_codes(uint32_t slot, int rows, bool is_v, int bs,
-                                             int log2bs, int lane) {
+__device__ __forceinline__ void expand_codes(uint32_t slot, int r_begin, int rows, bool is_v,
+                                             int bs, int log2bs, int lane) {
     const int c = lane & 7;                    // code chunk: columns 16 c .. 16 c + 15
     const int j0 = 2 * (c & 3);                // its first f16 chunk within the half
-    for (int R = lane >> 3; R - (lane >> 3) < rows; R += 4) {
+    for (int R = r_begin + (lane >> 3); R - (lane >> 3) < rows; R += 4) {
         const bool act = R < rows;
         const uint32_t b0 = is_v ? slot + uint32_t(R >> log2bs) * uint32_t(bs * 256) +
                                        uint32_t(R & (bs - 1)) * 128
@@ -860,8 +862,9 @@ __global__ void __launch_bounds__(kThreadsFor<F8>, 1)
         for (int b = 0; b < kNumBars; ++b)
             mbar_init(bars + 8 * b,
                       (b == kPFull || b == kPFull + 1 || b == kOFree || b == kOFree + 1) ? 256
-                      : (b >= kItemEmpty && b < kItemEmpty + 4)       ? 2 + 256 + 64 + (F8 ? 64 : 0)
-                      : b >= kKReady                                  ? 32
+                      : (b >= kItemEmpty && b < kItemEmpty + 4)       ? 2 + 256 + 64 + (F8 ? 128 : 0)
+                      : (b >= kKReady && b < kQReady)                 ? 64
+                      : b >= kQReady                                  ? 32
                                                                       : 1);
         *abort_word = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -1245,12 +1248,13 @@ __global__ void __launch_bounds__(kThreadsFor<F8>, 1)
                 wait_drain(bar(full_b + t % S), (t / S) & 1);
         }
     } else if (warp >= 12) {
-        // ------------------------------------------------------------ fp8 expanders (12: K, 13: V)
+        // ------------------------------------------------------------ fp8 expanders (12, 14: K; 13, 15: V)
         // Walk the same tiles as the loaders: wait for a tile's codes to land, expand them to
         // f16 in place and publish the tile on its ready barrier (which the MMA, for K, or
         // the softmax, for V, waits for instead of the TMA barrier).
         if constexpr (F8) {
-            const bool is_v = warp == 13;
+            const bool is_v = (warp & 1) != 0;
+            const int half = (warp - 12) >> 1;           // rows 64 half .. 64 half + 63
             const volatile ItemSlot* ring =
                 reinterpret_cast<const volatile ItemSlot*>(smem + L::kBar + kRingOff);
             const int log2bs = __ffs(p.bs) - 1;
@@ -1277,7 +1281,8 @@ __global__ void __launch_bounds__(kThreadsFor<F8>, 1)
                     const int kb = I.k_begin + jt * kTileKeys;
                     const int key_hi = min(kb + kTileKeys, I.ctx);
                     const int rows = ((key_hi - kb + p.bs - 1) >> log2bs) * p.bs;
-                    expand_codes(slots + st * L::kKVTile, rows, is_v, p.bs, log2bs, lane);
+                    expand_codes(slots + st * L::kKVTile, 64 * half, min(rows, 64 * half + 64),
+                                 is_v, p.bs, log2bs, lane);
                     // generic-proxy writes, read by the MMA through the async proxy
                     fence_proxy_async();
                     __syncwarp();
