@@ -89,6 +89,32 @@ def test_captured_mixed_step_equals_direct_launch():
     assert np.array_equal(got, _eager(st, kp, vp, q, kn, vn))
 
 
+def test_captured_fp8_mixed_step_equals_direct_launch():
+    """The same over an fp8 cache (float8_e4m3fn codes, per-tensor scales)."""
+    from oracle import fp8
+    st = wl.make_step(32, 8, 128, 16, [300, 1800, 2500, 640], [1, 1, 200, 37], seed=23)
+    scales = (0.0125, 0.0117)
+    k8 = torch.from_numpy(fp8.quantize(st.k_pool, scales[0])).cuda()
+    v8 = torch.from_numpy(fp8.quantize(st.v_pool, scales[1])).cuda()
+    lim = bd.StepLimits(B=st.B, T=st.T, max_blocks=st.block_table.shape[1] + 3, max_ctx=4096)
+    runner = bd.StepRunner(shape_of(st), limits=lim, kv_scales=scales)
+    q, kn, vn = bf16_dev(st.q, torch), bf16_dev(st.k_new, torch), bf16_dev(st.v_new, torch)
+    out = torch.empty((st.T, st.Hq, st.D), dtype=torch.bfloat16, device="cuda")
+    runner.prepare(st.cu_seqlens_q, st.ctx_lens, st.block_table)
+    runner.capture(q, kn, vn, k8, v8, out)
+    runner.replay()
+    torch.cuda.synchronize()
+    got = out.view(torch.int16).cpu().numpy()
+    assert runner.device_error() == 0
+    eager = bd.StepRunner(shape_of(st), kv_scales=scales).prepare(st.cu_seqlens_q, st.ctx_lens,
+                                                                  st.block_table)
+    out2 = torch.empty_like(out)
+    eager.run(q, kn, vn, k8, v8, out2)
+    torch.cuda.synchronize()
+    assert eager.device_error() == 0
+    assert np.array_equal(got, out2.view(torch.int16).cpu().numpy())
+
+
 def test_limits_are_enforced_on_the_host():
     st = wl.make_step(8, 2, 64, 16, [40, 50], [1, 1], seed=23)
     lim = bd.StepLimits(B=2, T=2, max_blocks=st.block_table.shape[1], max_ctx=45)
