@@ -23,6 +23,7 @@ PA_OK, PA_ERR_INVALID, PA_ERR_SHAPE, PA_ERR_BOUNDS, PA_ERR_OOM, PA_ERR_READONLY,
 PA_DEVERR_BLOCK, PA_DEVERR_SLOT, PA_DEVERR_TIMEOUT, PA_DEVERR_META = 1, 2, 4, 8
 PA_SPLIT_TOKENS = 2048
 PA_TILE_KEYS = 128
+PA_PLAN_CTAS = 152
 
 
 class PagedAttnError(RuntimeError):
@@ -59,7 +60,7 @@ class Shape(C.Structure):
 class WorkItem(C.Structure):
     _fields_ = [("seq", C.c_int32), ("q_start", C.c_int32), ("n_q", C.c_int32),
                 ("kv_head", C.c_int32), ("split", C.c_int32), ("n_tiles", C.c_int32),
-                ("n_splits", C.c_int32), ("reserved1", C.c_int32)]
+                ("n_splits", C.c_int32), ("next", C.c_int32)]
 
 
 WORK_ITEM_DTYPE = np.dtype([(n, np.int32) for n, _ in WorkItem._fields_])

@@ -26,8 +26,8 @@
 // [s*PA_SPLIT_TOKENS, (s+1)*PA_SPLIT_TOKENS) and the ascending-order combine make them
 // independent of the batch.
 //
-// Persistent schedule: one CTA per SM walks the items blockIdx.x, blockIdx.x + gridDim.x, ...
-// (the host orders items longest first). Warp roles (384 threads): warps 0-7 softmax /
+// Persistent schedule: CTA c (one per SM) walks list c of the plan, which the host deals
+// longest item first to the least-loaded list. Warp roles (384 threads): warps 0-7 softmax /
 // rescale / epilogue (two warps per TMEM sub-partition, one per 16-lane half), warp 8
 // producer (reads the work items, publishes them in a ring, loads each item's Q tile by TMA
 // into one of two Q buffers), warp 9 MMA issuer and TMEM owner, warp 10 K loader, warp 11 V
@@ -895,27 +895,26 @@ __global__ void __launch_bounds__(kThreadsFor<F8>, 1)
         }
         int ic = 0;
         int ok = 1;
-        // Snake order over the (longest-first) item list: round r gives CTA c the item
-        // r G + c when r is even and r G + (G - 1 - c) when r is odd, which evens out the
-        // CTAs' totals (a plain stride would hand CTA 0 the longest item of every round).
-        int round = 0;
-        const int G = int(gridDim.x);
+        // The plan's list blockIdx.x: it starts at that item and follows `next`, which only
+        // moves forward, so the walk ends. Padding (n_q == 0) ends it too.
+        int idx = int(blockIdx.x);
         for (;;) {
             Item I;
             I.good = false;
             bool have = false;
-            for (; int64_t(round) * G < p.n_items; ++round) {
-                const int x = (round & 1) ? G - 1 - int(blockIdx.x) : int(blockIdx.x);
-                const int64_t idx = int64_t(round) * G + x;
-                if (idx >= p.n_items) continue;           // a hole in the last, partial round
+            while (idx >= 0 && idx < p.n_items) {
+                const int cur = idx;
                 // an item with n_q == 0 is padding (a plan padded to a fixed item count, so
-                // that a captured step can be replayed with new metadata); padding follows all
-                // real items, so every later round of this CTA is padding too
-                if (p.items[idx].n_q == 0) {
-                    round = int((int64_t(p.n_items) + G - 1) / G);
-                    break;
+                // that a captured step can be replayed with new metadata): no more work
+                if (p.items[cur].n_q == 0) break;
+                const int nxt = p.items[cur].next;
+                if (nxt > 0 && (nxt <= cur || nxt >= p.n_items)) {
+                    if (lane == 0 && p.err) atomicOr(p.err, PA_DEVERR_META);
+                    idx = -1;                             // a link that does not move forward
+                } else {
+                    idx = nxt > 0 ? nxt : -1;
                 }
-                I = load_item(p, int(idx));
+                I = load_item(p, cur);
                 if (I.good) {
                     have = true;
                     break;
@@ -984,7 +983,6 @@ __global__ void __launch_bounds__(kThreadsFor<F8>, 1)
                 __syncwarp();
                 mbar_arrive(bar(kQReady + qb));          // all 32 lanes arrive
             }
-            ++round;
             ++ic;
         }
         if (lane == 0) {
@@ -1581,23 +1579,6 @@ int32_t make_maps(Maps* m, const void* q, const void* k_pool, const void* v_pool
     return make_map(&m->qn, q, D, s->num_q_heads, T, g, kRows / g);
 }
 
-int32_t sm_count_for_current_device(int* n) {
-    static int cached[64] = {};
-    int dev = 0;
-    int32_t st = note_cuda(cudaGetDevice(&dev));
-    if (st) return st;
-    if (dev >= 0 && dev < 64 && cached[dev]) {
-        *n = cached[dev];
-        return PA_OK;
-    }
-    int v = 0;
-    st = note_cuda(cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev));
-    if (st) return st;
-    if (dev >= 0 && dev < 64) cached[dev] = v;
-    *n = v;
-    return PA_OK;
-}
-
 template <int D, bool F8>
 int32_t launch(const Maps& maps, const Params& prm, int32_t max_ctx, cudaStream_t stream) {
     static int attr_device = -1;          // device the shared-memory limit was raised on
@@ -1611,9 +1592,7 @@ int32_t launch(const Maps& maps, const Params& prm, int32_t max_ctx, cudaStream_
         if (st) return st;
         attr_device = dev;
     }
-    int sms = 0;
-    if ((st = sm_count_for_current_device(&sms))) return st;
-    const int grid = std::min(prm.n_items, sms);
+    const int grid = std::min(prm.n_items, PA_PLAN_CTAS);      // one CTA per list of the plan
     // Both kernels are programmatic dependents of what precedes them on the stream: each
     // launches while its predecessor drains and waits (griddepcontrol.wait) before it reads
     // anything.

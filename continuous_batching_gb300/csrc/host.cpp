@@ -9,6 +9,7 @@
 #include <cstdint>
 #include <cstring>
 #include <unordered_map>
+#include <queue>
 #include <vector>
 
 #include <cuda_runtime.h>
@@ -73,7 +74,7 @@ struct pa_allocator {
 
 extern "C" {
 
-int32_t pa_abi_version(void) { return 1; }
+int32_t pa_abi_version(void) { return 2; }
 
 const char* pa_status_string(int32_t st) {
     switch (st) {
@@ -451,8 +452,38 @@ int32_t pa_plan_step(const pa_shape* shape, int32_t B, const int32_t* cu, const 
     std::stable_sort(out.begin(), out.end(), [](const pa_work_item& x, const pa_work_item& y) {
         return x.n_tiles > y.n_tiles;
     });
-    if (!out.empty()) std::memcpy(items, out.data(), out.size() * sizeof(pa_work_item));
-    *n_items = int32_t(out.size());
+    // Longest processing time first: each item, longest first, joins the list (one per CTA)
+    // with the least cost so far, the lower list on a tie.
+    const int32_t n = int32_t(out.size());
+    const int32_t G = std::min<int32_t>(n, PA_PLAN_CTAS);
+    std::vector<std::vector<int32_t>> lists(size_t(std::max(G, 1)));
+    using Load = std::pair<int64_t, int32_t>;        // (cost so far, list)
+    std::priority_queue<Load, std::vector<Load>, std::greater<Load>> least;
+    for (int32_t c = 0; c < G; ++c) least.push({0, c});
+    for (int32_t i = 0; i < n; ++i) {
+        const Load l = least.top();
+        least.pop();
+        lists[size_t(l.second)].push_back(i);
+        least.push({l.first + out[size_t(i)].n_tiles + 1, l.second});
+    }
+    // Stored position by position: the k-th item of every list that has one, lists in order,
+    // for k = 0, 1, ...; so list c starts at index c and a successor has a higher index.
+    std::vector<int32_t> at(size_t(n), 0);           // output index of sorted item i
+    std::vector<int32_t> order;
+    order.reserve(size_t(n));
+    for (size_t k = 0; order.size() < size_t(n); ++k)
+        for (int32_t c = 0; c < G; ++c)
+            if (k < lists[size_t(c)].size()) {
+                at[size_t(lists[size_t(c)][k])] = int32_t(order.size());
+                order.push_back(lists[size_t(c)][k]);
+            }
+    for (int32_t c = 0; c < G; ++c) {
+        const std::vector<int32_t>& L = lists[size_t(c)];
+        for (size_t k = 0; k < L.size(); ++k)
+            out[size_t(L[k])].next = k + 1 < L.size() ? at[size_t(L[k + 1])] : -1;
+    }
+    for (int32_t j = 0; j < n; ++j) items[j] = out[size_t(order[size_t(j)])];
+    *n_items = n;
     return PA_OK;
 }
 

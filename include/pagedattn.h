@@ -69,6 +69,10 @@ typedef enum pa_status {
 #define PA_SPLIT_TOKENS 2048
 /* Keys per tile of the shared tile routine; tiles are aligned to multiples of this. */
 #define PA_TILE_KEYS 128
+/* Persistent attention grid: min(n_items, PA_PLAN_CTAS) CTAs, one per SM of a GB300, and the
+ * same number of item lists in a plan (CTA c walks list c). A device with fewer SMs runs the
+ * surplus CTAs as SMs free up: the same results, later. */
+#define PA_PLAN_CTAS 152
 
 /* Geometry of one layer's pool. Supported: head_dim in {64, 128}; group = Hq / Hkv in
  * {1, 2, 4, 8, 16}; block_size a power of two in [8, 128]. */
@@ -82,11 +86,13 @@ typedef struct pa_shape {
 
 /* One unit of attention work: query rows [q_start, q_start + n_q) of sequence `seq`, one KV
  * head, one KV split. Produced by pa_plan_step on the host; copied to the device by the
- * caller and passed to paged_attention_step. An item with n_q == 0 is padding and is skipped
- * without error; padding must follow every real item (the kernel stops at the first one). A
- * caller that captures a step in a CUDA graph pads every plan at its end to one fixed item
- * count (pa_plan_max_items for its limits) and rewrites the device buffers in place before
- * each replay. */
+ * caller and passed to paged_attention_step. The items form min(n, PA_PLAN_CTAS) lists, n the
+ * real items: list c starts at item c and continues through `next`, and CTA c of the kernel
+ * walks it. An item with n_q == 0 is padding: a CTA that meets one (as its first item, or
+ * through `next`) has no more work, without error. Padding follows every real item. A caller
+ * that captures a step in a CUDA graph pads every plan at its end to one fixed item count
+ * (pa_plan_max_items for its limits) and rewrites the device buffers in place before each
+ * replay: the CTAs past the real plan's lists then start at padding. */
 typedef struct pa_work_item {
     int32_t seq;        /* index into cu_seqlens_q / ctx_lens / block_table rows */
     int32_t q_start;    /* first query row (token index into q and out) */
@@ -95,7 +101,9 @@ typedef struct pa_work_item {
     int32_t split;      /* first KV split index */
     int32_t n_tiles;    /* key tiles of PA_TILE_KEYS the item reads (a cost estimate) */
     int32_t n_splits;   /* consecutive splits from `split` the item covers (0 counts as 1) */
-    int32_t reserved1;
+    int32_t next;       /* index of the next item of this item's list; <= 0 ends the list. A
+                         * successor has a higher index (an item that breaks this, or points
+                         * past n_items, ends its list and raises PA_DEVERR_META) */
 } pa_work_item;
 
 /* ---------------------------------------------------------------- library ---------- */
@@ -258,8 +266,12 @@ int64_t pa_plan_max_items(const pa_shape* shape, int32_t B, int32_t T, int32_t m
  * chunk) gives one item per (tile, KV head) that covers every split the tile's last row
  * reaches; the kernel folds those splits itself, in the same ascending order and arithmetic,
  * so a row's bits are the same either way. paged_attention_step relies on this rule (an item
- * that breaks it is flagged PA_DEVERR_META and skipped). Items are ordered by decreasing
- * n_tiles (ties keep the generation order), so the order is a pure function of the metadata.
+ * that breaks it is flagged PA_DEVERR_META and skipped). Balance: the items, taken by
+ * decreasing n_tiles (ties in generation order), are dealt longest-processing-time first to
+ * G = min(n, PA_PLAN_CTAS) lists, each to the list of least total cost so far (cost of an
+ * item: n_tiles + 1; ties go to the lower list). The output holds the first item of every
+ * list (list c at index c), then the second item of every list that has one, in list order,
+ * and so on, with `next` linking each list. Everything is a pure function of the metadata.
  * Validates the metadata like pa_compute_slots (minus the table). PA_ERR_INVALID if
  * max_items is too small. */
 int32_t pa_plan_step(const pa_shape* shape, int32_t B, const int32_t* cu_seqlens_q,

@@ -38,7 +38,7 @@ def test_every_declared_symbol_is_exported(built_library):
 
 
 def test_abi_version_and_status_strings():
-    assert bd.pa_abi_version() == 1
+    assert bd.pa_abi_version() == 2
     assert bd.status_string(bd.PA_ERR_OOM) == "PA_ERR_OOM"
     assert bd.status_string(999) == "PA_ERR_UNKNOWN"
 
@@ -104,10 +104,89 @@ def test_plan_covers_every_row_head_split_once(name):
                     count[key] = count.get(key, 0) + 1
     want = {(t, h, s) for t in range(st.T) for h in range(st.Hkv) for s in range(nsplit[t])}
     assert set(count) == want and all(v == 1 for v in count.values())
-    # longest items first, deterministic
-    assert np.all(np.diff(items["n_tiles"]) <= 0)
-    again = bd.pa_plan_step(shape, st.cu_seqlens_q, st.ctx_lens)
+    check_lists(items, len(items))
+    again = bd.pa_plan_step(shape, st.cu_seqlens_q, st.ctx_lens)     # deterministic
     assert np.array_equal(items, again)
+
+
+def walk(items, n_items):
+    """The kernel's walk: CTA c of min(n_items, PA_PLAN_CTAS) starts at item c and follows
+    `next` (<= 0 ends) while it moves forward; padding (n_q == 0) ends a list."""
+    lists = []
+    for c in range(min(n_items, bd.PA_PLAN_CTAS)):
+        got, idx = [], c
+        while 0 <= idx < n_items and items[idx]["n_q"] != 0:
+            got.append(idx)
+            nxt = int(items[idx]["next"])
+            assert nxt <= 0 or idx < nxt < n_items, "a link must move forward"
+            idx = nxt if nxt > 0 else -1
+        lists.append(got)
+    return lists
+
+
+def check_lists(items, n_items):
+    """Every real item is on exactly one list; the layout and the longest-processing-time
+    deal the planner documents."""
+    n = int(np.sum(items["n_q"][:n_items] != 0))
+    G = min(n, bd.PA_PLAN_CTAS)
+    lists = walk(items, n_items)
+    seen = [i for L in lists for i in L]
+    assert sorted(seen) == list(range(n)), "each real item once, padding never"
+    assert all(len(L) > 0 for L in lists[:G]) and all(not L for L in lists[G:])
+    # stored position by position: the k-th items of all lists, lists in order
+    order = [L[k] for k in range(max(map(len, lists), default=0)) for L in lists if k < len(L)]
+    assert order == list(range(n))
+    tiles = items["n_tiles"][:n].astype(np.int64)
+    cost = [int(np.sum(tiles[L] + 1)) for L in lists[:G]]
+    for L in lists[:G]:
+        assert np.all(np.diff(tiles[L]) <= 0), "a list takes its items longest first"
+    if G:
+        # the greedy deal: when a list took its last item it was the cheapest list, so it
+        # exceeds the cheapest final list by at most that item's cost
+        for L, c in zip(lists[:G], cost):
+            assert c - (tiles[L[-1]] + 1) <= min(cost)
+        # the longest G items open the G lists, longest first
+        assert np.all(np.diff(tiles[:G]) <= 0)
+        assert tiles[:G].min() >= (tiles[G:].max() if n > G else 0)
+
+
+def test_plan_lists_balance_a_skewed_step():
+    """One long prefill segment among many short decodes: the deal puts the long items on
+    lists of their own and keeps the busiest list near the average."""
+    ctx = [9000 + 512] + [300] * 400
+    nq = [512] + [1] * 400
+    cu = np.concatenate([[0], np.cumsum(nq)]).astype(np.int32)
+    shape = bd.Shape.make(32, 8, 128, 16, 4096)
+    items = bd.pa_plan_step(shape, cu, np.array(ctx, np.int32))
+    check_lists(items, len(items))
+    lists = walk(items, len(items))
+    cost = [int(np.sum(items["n_tiles"][L].astype(np.int64) + 1)) for L in lists]
+    longest = int(items["n_tiles"].max()) + 1
+    assert max(cost) <= max(np.mean(cost), longest) + longest
+
+
+def test_padded_plan_walk_covers_the_real_items_once():
+    """A plan padded to a fixed count (a captured step): the CTAs past the real plan's lists
+    start at padding and do nothing."""
+    shape = bd.Shape.make(32, 8, 128, 16, 4096)
+    for ctx, nq in (([40, 3000], [1, 1]), ([5000] * 30, [1] * 30), ([700, 900], [300, 1])):
+        cu = np.concatenate([[0], np.cumsum(nq)]).astype(np.int32)
+        items = bd.pa_plan_step(shape, cu, np.array(ctx, np.int32))
+        cap = int(bd.load().pa_plan_max_items(ctypes.byref(shape), len(ctx), int(cu[-1]),
+                                              max(ctx)))
+        assert cap >= len(items)
+        padded = np.zeros(cap, dtype=bd.WORK_ITEM_DTYPE)
+        padded[:len(items)] = items
+        check_lists(padded, cap)
+
+
+def test_header_constants_match_the_binding():
+    import os, re
+    hdr = open(os.path.join(os.path.dirname(__file__), "..", "include", "pagedattn.h")).read()
+    defs = dict(re.findall(r"#define (PA_\w+)\s+(\d+)", hdr))
+    for name in ("PA_SPLIT_TOKENS", "PA_TILE_KEYS", "PA_PLAN_CTAS", "PA_DEVERR_BLOCK",
+                 "PA_DEVERR_SLOT", "PA_DEVERR_TIMEOUT", "PA_DEVERR_META"):
+        assert int(defs[name]) == getattr(bd, name), name
 
 
 def test_workspace_bytes_cover_partials():

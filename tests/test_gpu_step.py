@@ -196,6 +196,52 @@ def test_items_that_break_the_split_rule_are_flagged_and_skipped():
         assert_close(o[41:42], ref[41:42], forge)
 
 
+def test_plan_links_that_do_not_move_forward_end_the_list_and_are_flagged():
+    """A list link to the item itself, back to an earlier item or past the plan ends that list
+    with PA_DEVERR_META; the items of the other lists are still computed right."""
+    st = wl.make_step(16, 4, 128, 16, [700, 900, 40] + [300] * 200, [1] * 203, seed=93)
+    shape = shape_of(st)
+    g = st.Hq // st.Hkv
+    import tests.gpu_util as gu
+    kp, vp = gu.bf16_dev(st.k_pool, torch), gu.bf16_dev(st.v_pool, torch)
+    q = gu.bf16_dev(st.q, torch)
+    ref = pa.attention(st.q, st.k_pool, st.v_pool, st.block_table, st.cu_seqlens_q,
+                       st.ctx_lens, st.Hq)
+    items = bd.pa_plan_step(shape, st.cu_seqlens_q, st.ctx_lens)
+    second = int(items["next"][0])                 # list 0's second item
+    assert len(items) > bd.PA_PLAN_CTAS and second > 1
+    other = list_of(items, 1)                      # list 1 is never forged
+    for forge in ("self", "back", "past"):
+        bad = items.copy()
+        if forge == "self":
+            bad["next"][second] = second
+        elif forge == "back":
+            bad["next"][second] = 1
+        else:
+            bad["next"][0] = len(items)
+        runner = bd.StepRunner(shape).prepare(st.cu_seqlens_q, st.ctx_lens, st.block_table)
+        runner.items = torch.from_numpy(bad.view(np.int32).reshape(-1).copy()).cuda()
+        out = torch.zeros((st.T, st.Hq, st.D), dtype=torch.bfloat16, device="cuda")
+        runner.attend(q, kp, vp, out)
+        torch.cuda.synchronize()
+        assert runner.device_error() & bd.PA_DEVERR_META, forge
+        o = out.view(torch.int16).cpu().numpy().view(np.uint16)
+        got = np.stack([o[items["q_start"][j], items["kv_head"][j] * g:(items["kv_head"][j] + 1) * g]
+                        for j in other])
+        want = np.stack([ref[items["q_start"][j], items["kv_head"][j] * g:(items["kv_head"][j] + 1) * g]
+                         for j in other])
+        assert_close(got, want, forge)
+
+
+def list_of(items, c):
+    """Item indices of list c of a well-formed plan."""
+    got, idx = [], c
+    while idx >= 0:
+        got.append(idx)
+        idx = int(items["next"][idx]) if items["next"][idx] > 0 else -1
+    return got
+
+
 def test_host_rejects_bad_arguments_before_launch():
     st = wl.make_config("tiny")
     shape = shape_of(st)
