@@ -36,6 +36,7 @@ import argparse
 import hashlib
 import json
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -123,9 +124,14 @@ def load_peaks() -> dict:
 
 
 def kernel_source_hash() -> str:
+    """Hash of the attention kernel's code with comments and blank space removed, so that a
+    comment edit does not void the traffic records taken on the same code."""
     h = hashlib.sha256()
     for f in ("attention.cu", "tmem_ldst.h", "common.h"):
-        h.update(open(os.path.join(ROOT, "continuous_batching_gb300", "csrc", f), "rb").read())
+        src = open(os.path.join(ROOT, "continuous_batching_gb300", "csrc", f)).read()
+        src = re.sub(r"/\*.*?\*/", " ", src, flags=re.S)
+        src = re.sub(r"//[^\n]*", " ", src)
+        h.update(" ".join(src.split()).encode())
     return h.hexdigest()[:16]
 
 

@@ -31,12 +31,13 @@
 // rescale / epilogue (two warps per TMEM sub-partition, one per 16-lane half), warp 8
 // producer (reads the work items, publishes them in a ring, loads each item's Q tile by TMA
 // into one of two Q buffers), warp 9 MMA issuer and TMEM owner, warp 10 K loader, warp 11 V
-// loader. The loaders stream tiles by TMA through rings of
-// shared-memory slots across item boundaries; a K slot is free again as soon as S has read
-// it, a V slot once PV has. A paged tile is one box per block (K: one per 64-column half,
-// V: both halves in one box), issued from all 32 lanes of the loader warp. TMEM holds two S buffers (S of the
-// next tile is computed while the softmax works on the current one; P overwrites the S it came
-// from) and two O accumulators used by alternate splits (a split's epilogue or fold overlaps
+// loader; over an fp8 cache, 512 threads, warps 12-15 expanding the loaded codes to f16. The
+// loaders stream tiles by TMA through rings of shared-memory slots across item boundaries; a
+// K slot is free again as soon as S has read it, a V slot once PV has. A paged tile is one
+// box per block (K: one per 64-column half, V: both halves in one box), issued from all 32
+// lanes of the loader warp. TMEM holds two S buffers (S of the next tile is computed while
+// the softmax works on the current one; P overwrites the S it came from) and two O
+// accumulators used by alternate splits (a split's epilogue or fold overlaps
 // the next split's MMAs; the running result of a prefill tile's earlier splits sits in one of
 // them). Every wait on an mbarrier is bounded.
 #include <cuda.h>
@@ -1140,7 +1141,7 @@ __global__ void __launch_bounds__(kThreadsFor<F8>, 1)
             wait_drain(bar(kDrain), 0);
         }
     } else if (warp == 10 || warp == 11) {
-        // ------------------------------------------------------------ K (warp 6) / V (warp 7)
+        // ------------------------------------------------------------ K (warp 10) / V (warp 11)
         const bool is_v = warp == 11;
         int32_t* tbl = reinterpret_cast<int32_t*>(smem + L::kBar + kTableOff) +
                        (warp - 10) * kMaxTableEntries;
