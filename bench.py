@@ -259,21 +259,23 @@ class GpuStep:
         self.runner.run(self.q, self.kn, self.vn, self.kp, self.vp, self.out)
 
     def step_e2e(self):
-        """Public API from host buffers: plan + slots on the host, H2D of inputs and metadata,
-        kernels, D2H of the output."""
+        """Public API from host buffers, as a serving loop runs it: plan + slots on the host and
+        one pinned upload of the step's metadata (StepRunner with StepLimits), H2D of the new
+        tokens' q / k / v from pinned memory, the captured write and attention graphs, D2H of
+        the output, and a wait for it."""
         torch, st = self.torch, self.st
-        self.runner.prepare(st.cu_seqlens_q, st.ctx_lens, st.block_table)
+        self.graph_runner.prepare(st.cu_seqlens_q, st.ctx_lens, st.block_table)
         self.q.view(torch.int16).copy_(self.h_q, non_blocking=True)
         self.kn.view(torch.int16).copy_(self.h_kn, non_blocking=True)
         self.vn.view(torch.int16).copy_(self.h_vn, non_blocking=True)
-        self.step()
+        self.g_write.replay()
+        self.g_attend.replay()
         self.h_out.copy_(self.out.view(torch.int16), non_blocking=True)
         torch.cuda.current_stream().synchronize()
 
     def e2e_bytes(self):
         st = self.st
-        meta = 4 * (st.B + 1 + st.B + st.block_table.size + st.T) + self.runner.h_items.nbytes
-        h2d = st.q.nbytes + st.k_new.nbytes + st.v_new.nbytes + meta
+        h2d = st.q.nbytes + st.k_new.nbytes + st.v_new.nbytes + self.graph_runner.meta_bytes
         return h2d, st.T * st.Hq * st.D * 2
 
 

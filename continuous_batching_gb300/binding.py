@@ -481,6 +481,8 @@ class StepRunner:
     With limits (StepLimits), prepare() writes the metadata into fixed device buffers in place
     (the plan padded to a fixed item count with n_q == 0 items, the table padded with -1), so
     capture() can record run() once in a CUDA graph and replay() runs any later prepared step.
+    Those buffers are views of one device array, filled from one pinned host array by a single
+    asynchronous copy on the current stream; the next prepare() first waits for that copy.
     With kv_scales = (k_scale, v_scale) the pools are uint8 float8_e4m3fn caches and the fp8
     write and read entry points run instead.
     """
@@ -501,11 +503,26 @@ class StepRunner:
             d = self.device
             cap = int(load().pa_plan_max_items(C.byref(shape), L.B, L.T, L.max_ctx))
             self.n_items_cap = max(cap, 1)
-            self.items = torch.zeros(self.n_items_cap * 8, dtype=torch.int32, device=d)
-            self.cu = torch.zeros(L.B + 1, dtype=torch.int32, device=d)
-            self.ctx = torch.zeros(L.B, dtype=torch.int32, device=d)
-            self.table = torch.full((L.B, L.max_blocks), -1, dtype=torch.int32, device=d)
-            self.slots = torch.full((L.T,), -1, dtype=torch.int32, device=d)
+            parts = (("items", self.n_items_cap * 8), ("cu", L.B + 1), ("ctx", L.B),
+                     ("table", L.B * L.max_blocks), ("slots", L.T))
+            total = sum(n for _, n in parts)
+            self._meta = torch.empty(max(total, 1), dtype=torch.int32, device=d)
+            on_gpu = self.device.type == "cuda"
+            self._h_meta = torch.empty(max(total, 1), dtype=torch.int32, pin_memory=on_gpu)
+            h = self._h_meta.numpy()
+            self._h, dev, off = {}, {}, 0
+            for name, n in parts:
+                self._h[name], dev[name] = h[off:off + n], self._meta[off:off + n]
+                off += n
+            self._h["table"] = self._h["table"].reshape(L.B, L.max_blocks)
+            h[:] = 0                                      # items: n_q == 0, padding
+            self._h["table"].fill(-1)
+            self._h["slots"].fill(-1)
+            self._meta.copy_(self._h_meta)
+            self.items, self.cu, self.ctx = dev["items"], dev["cu"], dev["ctx"]
+            self.table = dev["table"].view(L.B, L.max_blocks)
+            self.slots = dev["slots"]
+            self._uploaded = None                         # event after the last upload
             self.max_ctx = L.max_ctx
             self.T = L.T
             need = pa_workspace_bytes(shape, L.T, L.max_ctx)
@@ -528,17 +545,21 @@ class StepRunner:
             if B != L.B or T != L.T or table.shape[1] > L.max_blocks or \
                     (B and int(ctx.max()) > L.max_ctx) or len(items) > self.n_items_cap:
                 raise ValueError("step exceeds the limits the runner was built for")
-            padded = np.zeros(self.n_items_cap, dtype=WORK_ITEM_DTYPE)   # n_q == 0: padding
-            padded[:len(items)] = items
-            tab = np.full((L.B, L.max_blocks), -1, dtype=np.int32)
-            tab[:, :table.shape[1]] = table
-            non_blocking = True
-            self.items.copy_(torch.from_numpy(padded.view(np.int32).reshape(-1)),
-                             non_blocking=non_blocking)
-            self.cu.copy_(torch.from_numpy(cu), non_blocking=non_blocking)
-            self.ctx.copy_(torch.from_numpy(ctx), non_blocking=non_blocking)
-            self.table.copy_(torch.from_numpy(tab), non_blocking=non_blocking)
-            self.slots.copy_(torch.from_numpy(_i32(slot_mapping)), non_blocking=non_blocking)
+            if self._uploaded is not None:
+                self._uploaded.synchronize()              # the pinned array is free again
+            hi = self._h["items"].view(WORK_ITEM_DTYPE)
+            hi[:len(items)] = items
+            hi[len(items):] = 0                           # n_q == 0: padding
+            self._h["cu"][:] = cu
+            self._h["ctx"][:] = ctx
+            ht = self._h["table"]
+            ht[:, :table.shape[1]] = table
+            ht[:, table.shape[1]:] = -1
+            self._h["slots"][:] = _i32(slot_mapping)
+            self._meta.copy_(self._h_meta, non_blocking=True)
+            if self._meta.is_cuda:
+                self._uploaded = torch.cuda.Event()
+                self._uploaded.record()
             return self
         self.max_ctx = int(ctx.max()) if len(ctx) else 0
         self.T = int(cu[-1]) if len(ctx) else 0
@@ -551,6 +572,14 @@ class StepRunner:
         if self.ws is None or self.ws.numel() * 4 < need:
             self.ws = torch.empty((need + 3) // 4, dtype=torch.float32, device=d)
         return self
+
+    @property
+    def meta_bytes(self) -> int:
+        """Bytes prepare() copies to the device per step (limits mode: the whole padded array)."""
+        if self.limits is not None:
+            return int(self._meta.numel()) * 4
+        return 4 * int(self.items.numel() + self.cu.numel() + self.ctx.numel() +
+                       self.table.numel() + self.slots.numel())
 
     def capture(self, q, k_new, v_new, k_pool, v_pool, out, write: bool = True,
                 attend: bool = True):

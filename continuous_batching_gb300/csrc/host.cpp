@@ -9,7 +9,6 @@
 #include <cstdint>
 #include <cstring>
 #include <unordered_map>
-#include <queue>
 #include <vector>
 
 #include <cuda_runtime.h>
@@ -422,6 +421,7 @@ int32_t pa_plan_step(const pa_shape* shape, int32_t B, const int32_t* cu, const 
     const int32_t g = shape->num_q_heads / shape->num_kv_heads;
     const int32_t rpt = PA_ROWS / g;
     std::vector<pa_work_item> out;
+    out.reserve(size_t(std::min<int64_t>(max_items, 1 << 16)));
     for (int32_t s = 0; s < B; ++s) {
         const int32_t n = cu[s + 1] - cu[s];
         for (int32_t t0 = 0; t0 < n; t0 += rpt) {
@@ -433,6 +433,7 @@ int32_t pa_plan_step(const pa_shape* shape, int32_t B, const int32_t* cu, const 
             const int32_t per_item = n > 1 ? nsplit : 1;
             for (int32_t h = 0; h < shape->num_kv_heads; ++h)
                 for (int32_t sp = 0; sp < nsplit; sp += per_item) {
+                    if (int64_t(out.size()) >= max_items) return PA_ERR_INVALID;
                     const int64_t k0 = int64_t(sp) * PA_SPLIT_TOKENS;
                     const int64_t k1 =
                         std::min<int64_t>(k0 + int64_t(per_item) * PA_SPLIT_TOKENS, p_max + 1);
@@ -448,41 +449,70 @@ int32_t pa_plan_step(const pa_shape* shape, int32_t B, const int32_t* cu, const 
                 }
         }
     }
-    if (int64_t(out.size()) > max_items) return PA_ERR_INVALID;
-    std::stable_sort(out.begin(), out.end(), [](const pa_work_item& x, const pa_work_item& y) {
-        return x.n_tiles > y.n_tiles;
-    });
-    // Longest processing time first: each item, longest first, joins the list (one per CTA)
-    // with the least cost so far, the lower list on a tie.
     const int32_t n = int32_t(out.size());
+    // by decreasing n_tiles, ties in generation order (a stable counting sort)
+    int32_t max_tiles = 0;
+    for (const pa_work_item& it : out) max_tiles = std::max(max_tiles, it.n_tiles);
+    std::vector<int32_t> by_cost(static_cast<size_t>(n));
+    if (max_tiles <= 4 * n + 4096) {
+        std::vector<int32_t> first(size_t(max_tiles) + 2, 0);
+        for (const pa_work_item& it : out) ++first[size_t(max_tiles - it.n_tiles) + 1];
+        for (size_t k = 1; k < first.size(); ++k) first[k] += first[k - 1];
+        for (int32_t i = 0; i < n; ++i)
+            by_cost[size_t(first[size_t(max_tiles - out[size_t(i)].n_tiles)]++)] = i;
+    } else {
+        for (int32_t i = 0; i < n; ++i) by_cost[size_t(i)] = i;
+        std::stable_sort(by_cost.begin(), by_cost.end(), [&](int32_t x, int32_t y) {
+            return out[size_t(x)].n_tiles > out[size_t(y)].n_tiles;
+        });
+    }
+    // Longest processing time first: each item, longest first, joins the list (one per CTA)
+    // with the least cost so far, the lower list on a tie. A binary min-heap of keys
+    // cost * 256 + list (G <= 256), so that equal costs order by list.
+    static_assert(PA_PLAN_CTAS <= 256, "list index must fit the heap key's low byte");
     const int32_t G = std::min<int32_t>(n, PA_PLAN_CTAS);
-    std::vector<std::vector<int32_t>> lists(size_t(std::max(G, 1)));
-    using Load = std::pair<int64_t, int32_t>;        // (cost so far, list)
-    std::priority_queue<Load, std::vector<Load>, std::greater<Load>> least;
-    for (int32_t c = 0; c < G; ++c) least.push({0, c});
-    for (int32_t i = 0; i < n; ++i) {
-        const Load l = least.top();
-        least.pop();
-        lists[size_t(l.second)].push_back(i);
-        least.push({l.first + out[size_t(i)].n_tiles + 1, l.second});
+    std::vector<uint64_t> heap(static_cast<size_t>(G));
+    for (int32_t c = 0; c < G; ++c) heap[size_t(c)] = uint64_t(c);   // ascending: a heap
+    std::vector<int32_t> owner(static_cast<size_t>(n)), rank(static_cast<size_t>(n));
+    std::vector<int32_t> len(static_cast<size_t>(G), 0);
+    for (int32_t j = 0; j < n; ++j) {
+        const int32_t i = by_cost[size_t(j)];
+        const int32_t c = int32_t(heap[0] & 255u);
+        owner[size_t(i)] = c;
+        rank[size_t(i)] = len[size_t(c)]++;
+        uint64_t key = heap[0] + (uint64_t(out[size_t(i)].n_tiles) + 1) * 256u;
+        size_t k = 0;                                                // sift the root down
+        for (;;) {
+            size_t m = 2 * k + 1;
+            if (m >= heap.size()) break;
+            if (m + 1 < heap.size() && heap[m + 1] < heap[m]) ++m;
+            if (heap[m] >= key) break;
+            heap[k] = heap[m];
+            k = m;
+        }
+        heap[k] = key;
     }
     // Stored position by position: the k-th item of every list that has one, lists in order,
     // for k = 0, 1, ...; so list c starts at index c and a successor has a higher index.
-    std::vector<int32_t> at(size_t(n), 0);           // output index of sorted item i
-    std::vector<int32_t> order;
-    order.reserve(size_t(n));
-    for (size_t k = 0; order.size() < size_t(n); ++k)
-        for (int32_t c = 0; c < G; ++c)
-            if (k < lists[size_t(c)].size()) {
-                at[size_t(lists[size_t(c)][k])] = int32_t(order.size());
-                order.push_back(lists[size_t(c)][k]);
-            }
+    std::vector<int32_t> off(size_t(G) + 1, 0);
+    int32_t longest = 0;
     for (int32_t c = 0; c < G; ++c) {
-        const std::vector<int32_t>& L = lists[size_t(c)];
-        for (size_t k = 0; k < L.size(); ++k)
-            out[size_t(L[k])].next = k + 1 < L.size() ? at[size_t(L[k + 1])] : -1;
+        off[size_t(c) + 1] = off[size_t(c)] + len[size_t(c)];
+        longest = std::max(longest, len[size_t(c)]);
     }
-    for (int32_t j = 0; j < n; ++j) items[j] = out[size_t(order[size_t(j)])];
+    std::vector<int32_t> member(static_cast<size_t>(n)), at(static_cast<size_t>(n));
+    for (int32_t i = 0; i < n; ++i)
+        member[size_t(off[size_t(owner[size_t(i)])] + rank[size_t(i)])] = i;
+    int32_t pos = 0;
+    for (int32_t k = 0; k < longest; ++k)
+        for (int32_t c = 0; c < G; ++c)
+            if (k < len[size_t(c)]) at[size_t(member[size_t(off[size_t(c)] + k)])] = pos++;
+    for (int32_t i = 0; i < n; ++i) {
+        const int32_t c = owner[size_t(i)], k = rank[size_t(i)];
+        pa_work_item it = out[size_t(i)];
+        it.next = k + 1 < len[size_t(c)] ? at[size_t(member[size_t(off[size_t(c)] + k + 1)])] : -1;
+        items[at[size_t(i)]] = it;
+    }
     *n_items = n;
     return PA_OK;
 }

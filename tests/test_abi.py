@@ -203,3 +203,34 @@ def test_upload_rejects_out_of_range_table_without_gpu():
     st = bd.load().pa_upload_block_table(ctypes.byref(shape), bad.ctypes.data_as(bd._i32p),
                                          None, 1, 2, None)
     assert st == bd.PA_ERR_BOUNDS
+
+
+def test_limits_runner_lays_out_padded_metadata_without_gpu():
+    """StepRunner with StepLimits: one metadata array whose views hold the plan padded with
+    n_q == 0 items, cu / ctx, the table padded with -1 and the slots; a second, smaller step
+    prepared into the same buffers leaves no stale entries. (Host logic: a CPU 'device'.)"""
+    torch = pytest.importorskip("torch")
+    shape = bd.Shape.make(8, 2, 64, 16, 64)
+    lim = bd.StepLimits(B=3, T=5, max_blocks=6, max_ctx=90)
+    r = bd.StepRunner(shape, device="cpu", limits=lim)
+    steps = [([40, 90, 17], [1, 3, 1],
+              [[0, 1, 2, -1, -1, -1], [3, 4, 5, 6, 7, 8], [9, 10, -1, -1, -1, -1]]),
+             ([16, 20, 33], [2, 2, 1], [[11, -1, -1], [12, 13, -1], [14, 15, 16]])]
+    for ctx, nq, tab in steps:
+        ctx = np.array(ctx, np.int32)
+        cu = np.concatenate([[0], np.cumsum(nq)]).astype(np.int32)
+        tab = np.array(tab, np.int32)
+        r.prepare(cu, ctx, tab)
+        items = bd.pa_plan_step(shape, cu, ctx)
+        dev_items = r.items.numpy().view(bd.WORK_ITEM_DTYPE)
+        assert len(dev_items) == r.n_items_cap >= len(items)
+        assert np.array_equal(dev_items[:len(items)], items)
+        assert np.all(dev_items["n_q"][len(items):] == 0) and np.all(dev_items[len(items):]["next"] == 0)
+        assert np.array_equal(r.cu.numpy(), cu) and np.array_equal(r.ctx.numpy(), ctx)
+        want = np.full((3, 6), -1, np.int32)
+        want[:, :tab.shape[1]] = tab
+        assert np.array_equal(r.table.numpy(), want)
+        assert np.array_equal(r.slots.numpy(), bd.pa_compute_slots(shape, tab, cu, ctx))
+        assert r.meta_bytes == 4 * (r.n_items_cap * 8 + 4 + 3 + 18 + 5)
+    with pytest.raises(ValueError):
+        r.prepare(np.array([0, 1, 2], np.int32), np.array([5, 5], np.int32), np.zeros((2, 1), np.int32))
