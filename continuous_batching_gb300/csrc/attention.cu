@@ -402,35 +402,40 @@ __device__ __forceinline__ void e4m3x4_to_f16x4(uint32_t w, uint32_t& lo, uint32
         : "r"(w));
 }
 
-// Expands the 128-byte code rows r_begin .. rows - 1 of a K or V ring slot to f16 in place (8 lanes
-// per row, 4 rows per pass). Row R's codes sit unswizzled where the row's second 64-column
-// f16 half goes (K slots: [half][key row]; V slots: [block][half][row]); its f16 halves go
-// to the 128-byte swizzled rows TMA would have written. A row is read by its 8 lanes before
-// any lane writes over it.
-__device__ __forceinline__ void expand_codes(uint32_t slot, int r_begin, int rows, bool is_v,
-                                             int bs, int log2bs, int lane) {
+// Expands the 128-byte code rows r_begin .. rows - 1 of a K (IS_V false) or V ring slot to f16
+// in place (8 lanes per row, 4 rows per pass). rows - r_begin is a multiple of 8 (whole blocks
+// of at least 8 rows), so every pass has 4 valid rows. Row R's codes sit unswizzled where the
+// row's second 64-column f16 half goes (K slots: [half][key row]; V slots: [block][half][row]);
+// its f16 halves go to the 128-byte swizzled rows TMA would have written. A row is read by its
+// 8 lanes before any lane writes over it.
+template <bool IS_V>
+__device__ __forceinline__ void expand_codes(uint32_t slot, int r_begin, int rows, int bs,
+                                             int log2bs, int lane) {
     const int c = lane & 7;                    // code chunk: columns 16 c .. 16 c + 15
-    const int j0 = 2 * (c & 3);                // its first f16 chunk within the half
-    for (int R = r_begin + (lane >> 3); R - (lane >> 3) < rows; R += 4) {
-        const bool act = R < rows;
-        const uint32_t b0 = is_v ? slot + uint32_t(R >> log2bs) * uint32_t(bs * 256) +
-                                       uint32_t(R & (bs - 1)) * 128
-                                 : slot + uint32_t(R) * 128;
-        const uint32_t b1 = b0 + (is_v ? uint32_t(bs * 128) : uint32_t(kTileKeys * 128));
-        uint4 v = make_uint4(0u, 0u, 0u, 0u);
-        if (act) v = ld_shared_v4(b1 + c * 16);
-        __syncwarp();
-        if (act) {
-            uint32_t f[8];
-            e4m3x4_to_f16x4(v.x, f[0], f[1]);
-            e4m3x4_to_f16x4(v.y, f[2], f[3]);
-            e4m3x4_to_f16x4(v.z, f[4], f[5]);
-            e4m3x4_to_f16x4(v.w, f[6], f[7]);
-            const uint32_t rb = (c >> 2) ? b1 : b0;
-            const int x = R & 7;               // 128-byte swizzle: chunk ^ (row & 7)
-            st_shared_v4(rb + (uint32_t(j0 ^ x) << 4), f[0], f[1], f[2], f[3]);
-            st_shared_v4(rb + (uint32_t((j0 + 1) ^ x) << 4), f[4], f[5], f[6], f[7]);
+    const uint32_t j0 = uint32_t(2 * (c & 3)); // its first f16 chunk within the half
+    const uint32_t hi = uint32_t(c >> 2);      // the half it goes to
+    for (int R0 = r_begin; R0 + 4 <= rows; R0 += 4) {        // warp-uniform: whole passes
+        const int R = R0 + (lane >> 3);
+        uint32_t b0, half_step;
+        if constexpr (IS_V) {
+            b0 = slot + uint32_t(R >> log2bs) * uint32_t(bs * 256) + uint32_t(R & (bs - 1)) * 128;
+            half_step = uint32_t(bs * 128);
+        } else {
+            b0 = slot + uint32_t(R) * 128;
+            half_step = uint32_t(kTileKeys * 128);
         }
+        const uint32_t b1 = b0 + half_step;
+        const uint4 v = ld_shared_v4(b1 + uint32_t(c) * 16);
+        __syncwarp();
+        uint32_t f[8];
+        e4m3x4_to_f16x4(v.x, f[0], f[1]);
+        e4m3x4_to_f16x4(v.y, f[2], f[3]);
+        e4m3x4_to_f16x4(v.z, f[4], f[5]);
+        e4m3x4_to_f16x4(v.w, f[6], f[7]);
+        const uint32_t rb = b0 + hi * half_step;
+        const uint32_t x = uint32_t(R & 7);    // 128-byte swizzle: chunk ^ (row & 7)
+        st_shared_v4(rb + ((j0 ^ x) << 4), f[0], f[1], f[2], f[3]);
+        st_shared_v4(rb + (((j0 + 1) ^ x) << 4), f[4], f[5], f[6], f[7]);
     }
 }
 
@@ -1280,8 +1285,12 @@ __global__ void __launch_bounds__(kThreadsFor<F8>, 1)
                     const int kb = I.k_begin + jt * kTileKeys;
                     const int key_hi = min(kb + kTileKeys, I.ctx);
                     const int rows = ((key_hi - kb + p.bs - 1) >> log2bs) * p.bs;
-                    expand_codes(slots + st * L::kKVTile, 64 * half, min(rows, 64 * half + 64),
-                                 is_v, p.bs, log2bs, lane);
+                    const uint32_t slot = slots + st * L::kKVTile;
+                    const int r_end = min(rows, 64 * half + 64);
+                    if (is_v)
+                        expand_codes<true>(slot, 64 * half, r_end, p.bs, log2bs, lane);
+                    else
+                        expand_codes<false>(slot, 64 * half, r_end, p.bs, log2bs, lane);
                     // generic-proxy writes, read by the MMA through the async proxy
                     fence_proxy_async();
                     __syncwarp();
