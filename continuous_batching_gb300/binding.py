@@ -523,6 +523,7 @@ class StepRunner:
             self.table = dev["table"].view(L.B, L.max_blocks)
             self.slots = dev["slots"]
             self._uploaded = None                         # event after the last upload
+            self._n_planned = 0                           # real items of the last plan
             self.max_ctx = L.max_ctx
             self.T = L.T
             need = pa_workspace_bytes(shape, L.T, L.max_ctx)
@@ -532,35 +533,12 @@ class StepRunner:
                 slot_mapping: Optional[np.ndarray] = None):
         torch = self.torch
         cu, ctx = _i32(cu_seqlens_q), _i32(ctx_lens)
+        if self.limits is not None:
+            return self._prepare_fixed(cu, ctx, _i32(block_table), slot_mapping)
         items = pa_plan_step(self.shape, cu, ctx)
         if slot_mapping is None:
             slot_mapping = pa_compute_slots(self.shape, block_table, cu, ctx)
-        self.h_items = items
         d = self.device
-        if self.limits is not None:
-            L = self.limits
-            B = len(ctx)
-            T = int(cu[-1]) if B else 0
-            table = _i32(block_table)
-            if B != L.B or T != L.T or table.shape[1] > L.max_blocks or \
-                    (B and int(ctx.max()) > L.max_ctx) or len(items) > self.n_items_cap:
-                raise ValueError("step exceeds the limits the runner was built for")
-            if self._uploaded is not None:
-                self._uploaded.synchronize()              # the pinned array is free again
-            hi = self._h["items"].view(WORK_ITEM_DTYPE)
-            hi[:len(items)] = items
-            hi[len(items):] = 0                           # n_q == 0: padding
-            self._h["cu"][:] = cu
-            self._h["ctx"][:] = ctx
-            ht = self._h["table"]
-            ht[:, :table.shape[1]] = table
-            ht[:, table.shape[1]:] = -1
-            self._h["slots"][:] = _i32(slot_mapping)
-            self._meta.copy_(self._h_meta, non_blocking=True)
-            if self._meta.is_cuda:
-                self._uploaded = torch.cuda.Event()
-                self._uploaded.record()
-            return self
         self.max_ctx = int(ctx.max()) if len(ctx) else 0
         self.T = int(cu[-1]) if len(ctx) else 0
         self.items = torch.from_numpy(items.view(np.int32).reshape(-1).copy()).to(d)
@@ -571,6 +549,45 @@ class StepRunner:
         need = pa_workspace_bytes(self.shape, self.T, self.max_ctx)
         if self.ws is None or self.ws.numel() * 4 < need:
             self.ws = torch.empty((need + 3) // 4, dtype=torch.float32, device=d)
+        return self
+
+    def _prepare_fixed(self, cu, ctx, table, slot_mapping):
+        """prepare() under limits: the plan and the slots are written by the library straight into
+        the pinned host array, which then goes to the device in one copy."""
+        L = self.limits
+        B = len(ctx)
+        T = int(cu[-1]) if B else 0
+        if B != L.B or T != L.T or table.ndim != 2 or table.shape[0] != B or \
+                table.shape[1] > L.max_blocks or (B and int(ctx.max()) > L.max_ctx):
+            raise ValueError("step exceeds the limits the runner was built for")
+        if self._uploaded is not None:
+            self._uploaded.synchronize()                  # the pinned array is free again
+        lib = load()
+        hi = self._h["items"]
+        n = C.c_int32()
+        _check(lib.pa_plan_step(C.byref(self.shape), B, _p32(cu), _p32(ctx),
+                                hi.ctypes.data_as(C.POINTER(WorkItem)), self.n_items_cap,
+                                C.byref(n)), "pa_plan_step")
+        hs = hi.view(WORK_ITEM_DTYPE)
+        if self._n_planned > n.value:
+            hs[n.value:self._n_planned] = 0               # n_q == 0: padding
+        self._n_planned = n.value
+        self._h["cu"][:] = cu
+        self._h["ctx"][:] = ctx
+        ht = self._h["table"]
+        ht[:, :table.shape[1]] = table
+        if table.shape[1] < L.max_blocks:
+            ht[:, table.shape[1]:] = -1
+        if slot_mapping is not None:
+            self._h["slots"][:] = _i32(slot_mapping)
+        elif T > 0:
+            _check(lib.pa_compute_slots(C.byref(self.shape), _p32(table), B, table.shape[1],
+                                        _p32(cu), _p32(ctx), _p32(self._h["slots"])),
+                   "pa_compute_slots")
+        self._meta.copy_(self._h_meta, non_blocking=True)
+        if self._meta.is_cuda:
+            self._uploaded = self.torch.cuda.Event()
+            self._uploaded.record()
         return self
 
     @property

@@ -234,3 +234,26 @@ def test_limits_runner_lays_out_padded_metadata_without_gpu():
         assert r.meta_bytes == 4 * (r.n_items_cap * 8 + 4 + 3 + 18 + 5)
     with pytest.raises(ValueError):
         r.prepare(np.array([0, 1, 2], np.int32), np.array([5, 5], np.int32), np.zeros((2, 1), np.int32))
+
+
+def test_limits_runner_clears_items_of_a_longer_previous_plan_without_gpu():
+    """A plan with fewer items than the one before it: the items past its end read as padding
+    again (the kernel's CTAs past the plan's lists start there)."""
+    pytest.importorskip("torch")
+    shape = bd.Shape.make(8, 2, 64, 16, 1024)
+    lim = bd.StepLimits(B=2, T=2, max_blocks=320, max_ctx=5000)
+    r = bd.StepRunner(shape, device="cpu", limits=lim)
+    cu = np.array([0, 1, 2], np.int32)
+    table = np.arange(640, dtype=np.int32).reshape(2, 320)
+    counts = []
+    for ctx in ([4500, 5000], [100, 200], [5000, 17]):
+        ctx = np.array(ctx, np.int32)
+        r.prepare(cu, ctx, table)
+        items = bd.pa_plan_step(shape, cu, ctx)
+        dev = r.items.numpy().view(bd.WORK_ITEM_DTYPE)
+        assert np.array_equal(dev[:len(items)], items)
+        assert not np.any(dev.view(np.int32).reshape(len(dev), 8)[len(items):])
+        assert np.array_equal(r.slots.numpy(), bd.pa_compute_slots(shape, table, cu, ctx))
+        check_lists(dev, len(dev))
+        counts.append(len(items))
+    assert counts[0] > counts[1] < counts[2]
