@@ -264,10 +264,11 @@ class GpuStep:
         tokens' q / k / v from pinned memory, the captured write and attention graphs, D2H of
         the output, and a wait for it."""
         torch, st = self.torch, self.st
-        self.graph_runner.prepare(st.cu_seqlens_q, st.ctx_lens, st.block_table)
+        # the new tokens' copies go first, so that they run while the host plans the step
         self.q.view(torch.int16).copy_(self.h_q, non_blocking=True)
         self.kn.view(torch.int16).copy_(self.h_kn, non_blocking=True)
         self.vn.view(torch.int16).copy_(self.h_vn, non_blocking=True)
+        self.graph_runner.prepare(st.cu_seqlens_q, st.ctx_lens, st.block_table)
         self.g_write.replay()
         self.g_attend.replay()
         self.h_out.copy_(self.out.view(torch.int16), non_blocking=True)
