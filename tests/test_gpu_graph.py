@@ -121,3 +121,29 @@ def test_limits_are_enforced_on_the_host():
     runner = bd.StepRunner(shape_of(st), limits=lim)
     with pytest.raises(ValueError):
         runner.prepare(st.cu_seqlens_q, st.ctx_lens, st.block_table)    # ctx 50 > 45
+
+
+@pytest.mark.parametrize("name,kv", [("decode", "bf16"), ("mixed", "bf16"), ("prefill", "bf16"),
+                                     ("decode", "fp8")])
+def test_full_size_bench_graphs_equal_direct_launches(name, kv):
+    """The timed configuration of bench.py (its full-size workloads, captured write and
+    attention graphs over the padded plan of a StepLimits runner) gives the bits of direct
+    launches, which the sampled full-size parity tests compare with the oracle."""
+    import bench
+    st = bench.make_workload(name, 0)
+    g = bench.GpuStep(st, torch, bd, kv=kv)
+    g.g_write.replay()
+    g.g_attend.replay()
+    torch.cuda.synchronize()
+    assert g.graph_runner.device_error() == 0
+    got = g.out.view(torch.int16).cpu().numpy()
+    r = bd.StepRunner(g.shape, kv_scales=g.kv_scales).prepare(st.cu_seqlens_q, st.ctx_lens,
+                                                              st.block_table)
+    out = torch.empty_like(g.out)
+    r.run(g.q, g.kn, g.vn, g.kp, g.vp, out)
+    torch.cuda.synchronize()
+    assert r.device_error() == 0
+    assert np.array_equal(got, out.view(torch.int16).cpu().numpy())
+    # the end-to-end path (host metadata, pinned uploads, the same graphs) as well
+    g.step_e2e()
+    assert np.array_equal(g.h_out.numpy(), got)
