@@ -92,7 +92,9 @@ typedef struct pa_shape {
  * through `next`) has no more work, without error. Padding follows every real item. A caller
  * that captures a step in a CUDA graph pads every plan at its end to one fixed item count
  * (pa_plan_max_items for its limits) and rewrites the device buffers in place before each
- * replay: the CTAs past the real plan's lists then start at padding. */
+ * replay: the CTAs past the real plan's lists then start at padding. A plan built by other
+ * means must put every real item on exactly one list: an item on no list is not computed, and
+ * one on two lists is computed twice (to the same values). */
 typedef struct pa_work_item {
     int32_t seq;        /* index into cu_seqlens_q / ctx_lens / block_table rows */
     int32_t q_start;    /* first query row (token index into q and out) */
