@@ -124,11 +124,14 @@ def load_peaks() -> dict:
 
 
 def kernel_source_hash() -> str:
-    """Hash of the attention kernel's code with comments and blank space removed, so that a
-    comment edit does not void the traffic records taken on the same code."""
+    """Hash of the attention kernel's code (its sources and the ABI header it includes) with
+    comments and blank space removed, so that a comment edit does not void the traffic records
+    taken on the same code."""
     h = hashlib.sha256()
-    for f in ("attention.cu", "tmem_ldst.h", "common.h"):
-        src = open(os.path.join(ROOT, "continuous_batching_gb300", "csrc", f)).read()
+    csrc = "continuous_batching_gb300/csrc/"
+    for f in (csrc + "attention.cu", csrc + "tmem_ldst.h", csrc + "common.h",
+              "include/pagedattn.h"):
+        src = open(os.path.join(ROOT, f)).read()
         src = re.sub(r"/\*.*?\*/", " ", src, flags=re.S)
         src = re.sub(r"//[^\n]*", " ", src)
         h.update(" ".join(src.split()).encode())
