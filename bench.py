@@ -1,7 +1,8 @@
 """Benchmark of one flat ragged paged-attention step on GB300 (one JSON line on stdout).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload decode|mixed|longtail|prefix|prefill]
+                    [--workload decode|mixed|longtail|prefix|prefill|long16k]
+                    [--kv bf16|fp8] [--no-mixed] [--no-extras]
 
 A step is the whole hot path over one batch of synthetic input: the KV-write scatter of the
 step's new K/V rows, then paged attention for every query row (plus the fixed-order split
@@ -18,8 +19,13 @@ replay CUDA graphs captured from the same library calls (KV write; attention + c
 no host launch overhead sits inside the timed region; the e2e leg goes through the public
 API call by call, from host buffers, planning included.
 
---impl reference times the CPU oracle (fp64 numpy) on a bounded sample of the same workload
-on the host cores, with the same metric and unit.
+The default run also reports, each under its own key with its own roofline, clocks and
+launch count: decode_16k (32 decode rows at ctx 16,384), prefill_segments (the mixed step's
+four 512-row prefill segments, tensor roofline) and longtail (the long-tail rollout decode).
+
+The CPU baseline (and --impl reference) times the oracle (fp64 numpy, as it stands) on every
+host core: a spawn-started process pool over shared memory, whole passes over the same
+workload for about --cpu-budget seconds, with the same metric and unit.
 
 Under torchrun (N > 1) every rank runs its own decode batch (seed + rank) with no data-path
 collective: the path shards by sequence, so scaling is weak.
@@ -88,7 +94,12 @@ WORKLOADS = {
     "prefill": ("prefill segments: the mixed step's 4 chunked-prefill segments of 512 rows at "
                 "prior offsets {0,512,4096,9000} alone, Hq=32, Hkv=8, D=128, block_size=16, causal, "
                 "T=2048, seed 2"),
+    "long16k": ("16k-context decode: Hq=32, Hkv=8, D=128, block_size=16, 32 decode rows all at ctx "
+                "16384, pool = 32*1024 blocks, permuted tables, bf16 ~N(0,1), seed 5"),
 }
+# reported beside the headline in the default run, each with its own roofline: the 16k-context
+# decode and the prefill segments (the two targets of the path) and the long-tail rollout
+EXTRAS = (("decode_16k", "long16k"), ("prefill_segments", "prefill"), ("longtail", "longtail"))
 # the value of these workloads is tokens/s (ragged steps); the others report KV GB/s
 TOKEN_WORKLOADS = ("mixed", "prefill")
 
@@ -319,7 +330,7 @@ def time_steps(g: GpuStep, torch, steps: int, warmup: int, flush, attn_only=Fals
 
 def rank_seed(name: str, rank: int) -> int:
     """Each rank of a multi-GPU run draws its own batch of the same workload."""
-    base = {"decode": 1, "mixed": 2, "longtail": 3, "prefix": 4}[name]
+    base = {"decode": 1, "mixed": 2, "longtail": 3, "prefix": 4, "long16k": 5}[name]
     return base + rank
 
 
@@ -334,6 +345,66 @@ def combine_ranks(total_ms: float, units: float, dist=None, device="cpu"):
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     dist.all_reduce(u, op=dist.ReduceOp.SUM)
     return float(t.item()), float(u.item())
+
+
+def roofline_for(name: str, st: wl.Step, attn_ms: float, peaks: dict, fp8_kv: bool) -> dict:
+    """Roofline of the attention launches (attention kernel + split combine) of one step:
+    algorithmic bytes (K/V read once; unique bytes for the prefix-shared workload) against
+    the measured copy bandwidth, or, for the prefill segments, causal algorithmic FLOPs
+    against the measured bf16 tensor peak (burst: the kernel is timed by itself)."""
+    traffic = measured_traffic(name + ("_fp8" if fp8_kv else ""))
+    if name == "prefill":
+        achieved = prefill_flops(st) / (attn_ms * 1e-3) / 1e12
+        return {"bound": "tensor", "achieved": round(achieved, 1), "peak": peaks["bf16_tflops"],
+                "unit": "TFLOP/s", "frac": round(achieved / peaks["bf16_tflops"], 4),
+                "traffic": traffic,
+                "kernel": "paged_attention_step (tile routine), causal algorithmic FLOPs "
+                          "4*D*Hq*(n*o + n(n+1)/2)",
+                "peak_src": peaks["src"] + " (burst)"}
+    bytes_step = kv_bytes(st, 1 if fp8_kv else 2)
+    roof_bytes = (unique_kv_bytes(st) // (2 if fp8_kv else 1) if name == "prefix"
+                  else bytes_step)
+    achieved = roof_bytes / (attn_ms * 1e-3) / 1e9
+    roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
+            "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
+            "traffic": traffic,
+            "kernel": "paged_attention_step (attention kernels + split combine)",
+            "peak_src": peaks["src"]}
+    if name == "prefix":
+        roof["bytes"] = "unique K/V bytes (shared prompt blocks counted once)"
+        roof["logical_gbs"] = round(bytes_step / (attn_ms * 1e-3) / 1e9, 1)
+    return roof
+
+
+def measure_extra(name: str, rank: int, torch, bd, args, peaks: dict, flush) -> dict:
+    """One more workload, timed like the headline (graph replays, CUDA events, the same L2
+    rule), with the clocks sampled over its own loaded window."""
+    st = make_workload(name, rank)
+    fp8_kv = args.kv == "fp8"
+    g = GpuStep(st, torch, bd, args.kv)
+    bytes_step = kv_bytes(st, 1 if fp8_kv else 2)
+    needs_flush = bytes_step < 2 * L2_BYTES
+    torch.cuda.synchronize()
+    with ClockSampler(int(os.environ.get("LOCAL_RANK", "0"))) as clk:
+        if not args.no_clocks:
+            load_for(g, torch, 0.6)
+        step_ms, attn_ms = time_steps(g, torch, args.steps, args.warmup,
+                                      flush if needs_flush else None)
+        if not args.no_clocks:
+            load_for(g, torch, 0.6)
+    ms = statistics.mean(step_ms)
+    tokens = name in TOKEN_WORKLOADS
+    out = {"workload": WORKLOADS[name],
+           "value": round(st.T / (ms * 1e-3), 1) if tokens else round(bytes_step / (ms * 1e-3) / 1e9, 2),
+           "unit": "tokens/s" if tokens else UNIT, "ms_per_step": round(ms, 5),
+           "attention_ms": round(statistics.mean(attn_ms), 5),
+           "roofline": roofline_for(name, st, statistics.mean(attn_ms), peaks, fp8_kv),
+           "l2": "flushed by a 256 MiB write between timed steps" if needs_flush else
+                 "inputs larger than L2, no flush",
+           "gpu_launches": g.launches_per_step() * args.steps, "clocks": clk.summary()}
+    del g
+    torch.cuda.empty_cache()
+    return out
 
 
 def load_for(g: GpuStep, torch, seconds: float) -> None:
@@ -412,26 +483,7 @@ def run_ours(args) -> dict:
     h2d, d2h = g.e2e_bytes()
 
     attn_avg = statistics.mean(attn_ms)
-    if name == "prefill":
-        achieved = prefill_flops(st) / (attn_avg * 1e-3) / 1e12
-        roof = {"bound": "tensor", "achieved": round(achieved, 1), "peak": peaks["bf16_tflops"],
-                "unit": "TFLOP/s", "frac": round(achieved / peaks["bf16_tflops"], 4),
-                "traffic": measured_traffic(name + ("_fp8" if fp8_kv else "")),
-                "kernel": "paged_attention_step (tile routine), causal algorithmic FLOPs "
-                          "4*D*Hq*(n*o + n(n+1)/2)",
-                "peak_src": peaks["src"] + " (burst)"}
-    else:
-        roof_bytes = (unique_kv_bytes(st) // (2 if fp8_kv else 1) if name == "prefix"
-                      else bytes_step)
-        achieved = roof_bytes / (attn_avg * 1e-3) / 1e9
-        roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
-                "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
-                "traffic": measured_traffic(name + ("_fp8" if fp8_kv else "")),
-                "kernel": "paged_attention_step (attention kernels + split combine)",
-                "peak_src": peaks["src"]}
-        if name == "prefix":
-            roof["bytes"] = "unique K/V bytes (shared prompt blocks counted once)"
-            roof["logical_gbs"] = round(bytes_step / (attn_avg * 1e-3) / 1e9, 1)
+    roof = roofline_for(name, st, attn_avg, peaks, fp8_kv)
 
     # the mixed ragged step (tokens/s) alongside the decode headline
     mixed = None
@@ -473,6 +525,9 @@ def run_ours(args) -> dict:
     }
     if mixed:
         line["ragged_step"] = mixed
+    if name == "decode" and not args.no_extras:
+        for key, ex in EXTRAS:
+            line[key] = measure_extra(ex, rank, torch, bd, args, peaks, flush)
     if rank == 0 and not args.no_cpu_baseline and not fp8_kv:
         line["cpu_baseline"] = cpu_baseline(st, budget_s=args.cpu_budget, tokens=tokens)
     if world > 1:
@@ -483,43 +538,122 @@ def run_ours(args) -> dict:
 
 # ---------------------------------------------------------------------- CPU oracle arm
 
-def cpu_baseline(st: wl.Step, budget_s: float = 15.0, tokens: bool = False) -> dict:
-    """Times the oracle (fp64 numpy, as it stands) on the workload until about budget_s of CPU
-    work. KV workloads: whole sequences in a seeded order, KV GB/s of the sample. Token
-    workloads: query rows in seeded chunks of 8, tokens/s of the sample."""
+_CPU = {}
+
+
+def _cpu_worker_init(specs: dict, Hq: int) -> None:
+    """Worker of the CPU baseline: attaches to the step's arrays in shared memory (no copy)."""
+    from multiprocessing import shared_memory
+    for name, (shm_name, shape, dtype) in specs.items():
+        shm = shared_memory.SharedMemory(name=shm_name)
+        _CPU[name + "_shm"] = shm
+        _CPU[name] = np.ndarray(shape, np.dtype(dtype), buffer=shm.buf)
+    _CPU["Hq"] = Hq
+
+
+def _cpu_worker_run(rows) -> int:
     import oracle.paged_attention as pa
-    rng = np.random.default_rng(0)
-    if tokens:
-        order = rng.permutation(st.T)
-        groups = [np.sort(order[i:i + 8]) for i in range(0, st.T, 8)]
-    else:
-        groups = [np.arange(st.cu_seqlens_q[s], st.cu_seqlens_q[s + 1])
-                  for s in rng.permutation(st.B)]
-    seq_of = np.searchsorted(st.cu_seqlens_q, np.arange(st.T), side="right") - 1
-    done_bytes = 0
-    done_rows = 0
-    n_groups = 0
-    t0 = time.perf_counter()
-    for r in groups:
-        pa.attention_rows(st.q, st.k_pool, st.v_pool, st.block_table, st.cu_seqlens_q,
-                          st.ctx_lens, st.Hq, r)
-        done_rows += len(r)
-        if not tokens:
-            done_bytes += int(st.ctx_lens[seq_of[r[0]]]) * 2 * st.Hkv * st.D * 2
-        n_groups += 1
-        if time.perf_counter() - t0 > budget_s:
-            break
-    dt = time.perf_counter() - t0
-    where = f"numpy fp64 einsum on one thread (host has {os.cpu_count()} cores)"
-    if tokens:
-        return {"value": round(done_rows / dt, 2), "unit": "tokens/s", "cores": 1,
-                "kind": "oracle",
-                "sample": f"{done_rows} of {st.T} query rows (seeded chunks of 8, all {st.Hq} "
-                          f"heads) in {dt:.1f} s; {where}"}
-    return {"value": round(done_bytes / dt / 1e9, 4), "unit": UNIT, "cores": 1,
-            "kind": "oracle",
-            "sample": f"{n_groups} of {st.B} decode rows (whole sequences, all {st.Hq} heads), "
-                      f"{done_bytes / 1e9:.3f} GB of K/V in {dt:.1f} s; {where}"}
+    c = _CPU
+    pa.attention_rows(c["q"], c["k_pool"], c["v_pool"], c["block_table"], c["cu_seqlens_q"],
+                      c["ctx_lens"], c["Hq"], rows)
+    return len(rows)
+
+
+class OraclePool:
+    """The oracle (fp64 numpy, as it stands) on every host core: a pool of `workers` processes
+    (default os.cpu_count()), started with spawn, shares the step's arrays through shared
+    memory and computes whole query groups (KV workloads: one sequence per task, longest
+    first; token workloads: 8 query rows per task)."""
+
+    def __init__(self, st: wl.Step, tokens: bool = False, workers: int = 0):
+        import multiprocessing as mp
+        from multiprocessing import shared_memory
+        self.st, self.tokens = st, tokens
+        self.n_workers = workers or os.cpu_count() or 1
+        if tokens:
+            self.groups = [np.arange(i, min(i + 8, st.T)) for i in range(0, st.T, 8)]
+        else:
+            order = np.argsort(-st.ctx_lens, kind="stable")
+            self.groups = [np.arange(st.cu_seqlens_q[s], st.cu_seqlens_q[s + 1]) for s in order]
+        seq_of = np.searchsorted(st.cu_seqlens_q, np.arange(st.T), side="right") - 1
+        self.pass_bytes = sum(int(st.ctx_lens[seq_of[r[0]]]) * 2 * st.Hkv * st.D * 2 * len(r)
+                              for r in self.groups if len(r))
+        self.shms, specs = [], {}
+        # one BLAS / OpenMP thread per worker process (the oracle's einsums run in numpy's
+        # own loops; the pool supplies the parallelism)
+        saved = {k: os.environ.get(k) for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS",
+                                                "MKL_NUM_THREADS")}
+        try:
+            for name in ("q", "k_pool", "v_pool", "block_table", "cu_seqlens_q", "ctx_lens"):
+                a = np.ascontiguousarray(getattr(st, name))
+                shm = shared_memory.SharedMemory(create=True, size=max(a.nbytes, 1))
+                np.ndarray(a.shape, a.dtype, buffer=shm.buf)[...] = a
+                self.shms.append(shm)
+                specs[name] = (shm.name, a.shape, a.dtype.str)
+            for k in saved:
+                os.environ[k] = "1"
+            self.pool = mp.get_context("spawn").Pool(
+                self.n_workers, initializer=_cpu_worker_init, initargs=(specs, st.Hq))
+            # every worker started and attached before anything is timed
+            self.pool.map(_cpu_worker_run, [np.zeros(0, np.int64)] * self.n_workers)
+        except BaseException:
+            self.close()
+            raise
+        finally:
+            for k, v in saved.items():
+                if v is None:
+                    os.environ.pop(k, None)
+                else:
+                    os.environ[k] = v
+
+    def run(self, budget_s: float) -> dict:
+        """Full passes over the workload until about budget_s of wall time has gone by (at
+        least one); the value is their K/V bytes (or query rows) over that wall time."""
+        st = self.st
+        passes, rows_done = 0, 0
+        t0 = time.perf_counter()
+        while True:
+            rows_done += sum(self.pool.imap_unordered(_cpu_worker_run, self.groups, chunksize=1))
+            passes += 1
+            if time.perf_counter() - t0 > budget_s:
+                break
+        dt = time.perf_counter() - t0
+        where = (f"numpy fp64 oracle in {self.n_workers} spawned worker processes (host has "
+                 f"{os.cpu_count()} cores), one BLAS/OpenMP thread each")
+        if self.tokens:
+            return {"value": round(rows_done / dt, 2), "unit": "tokens/s", "cores": self.n_workers,
+                    "kind": "oracle", "blas_threads_per_worker": 1,
+                    "sample": f"{passes} full pass(es) over all {st.T} query rows (tasks of 8 rows, "
+                              f"all {st.Hq} heads) in {dt:.1f} s; {where}"}
+        return {"value": round(passes * self.pass_bytes / dt / 1e9, 4), "unit": UNIT,
+                "cores": self.n_workers, "kind": "oracle", "blas_threads_per_worker": 1,
+                "sample": f"{passes} full pass(es) over all {st.B} decode rows (one sequence per "
+                          f"task, all {st.Hq} heads), {passes * self.pass_bytes / 1e9:.3f} GB of K/V "
+                          f"in {dt:.1f} s; {where}"}
+
+    def close(self):
+        pool = getattr(self, "pool", None)
+        if pool is not None:
+            pool.terminate()
+            pool.join()
+            self.pool = None
+        for shm in getattr(self, "shms", []):
+            shm.close()
+            shm.unlink()
+        self.shms = []
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *a):
+        self.close()
+
+
+def cpu_baseline(st: wl.Step, budget_s: float = 10.0, tokens: bool = False,
+                 workers: int = 0) -> dict:
+    """The oracle timed on every host core (OraclePool) for about budget_s of wall time."""
+    with OraclePool(st, tokens, workers) as op:
+        return op.run(budget_s)
 
 
 def run_reference(args) -> dict:
@@ -529,14 +663,15 @@ def run_reference(args) -> dict:
     name = args.workload
     st = make_workload(name, 0)
     tokens = name in TOKEN_WORKLOADS
-    for _ in range(args.warmup):
-        cpu_baseline(st, budget_s=0.5, tokens=tokens)
-    vals = []
-    t0 = time.perf_counter()
     per = max(1.0, min(20.0, 90.0 / max(args.steps, 1)))
-    for _ in range(args.steps):
-        vals.append(cpu_baseline(st, budget_s=per, tokens=tokens))
-    wall = time.perf_counter() - t0
+    vals = []
+    with OraclePool(st, tokens) as op:
+        for _ in range(args.warmup):
+            op.run(0.0)                                  # one pass each
+        t0 = time.perf_counter()
+        for _ in range(args.steps):
+            vals.append(op.run(per))
+        wall = time.perf_counter() - t0
     v = statistics.mean(x["value"] for x in vals)
     base = vals[0]
     base["value"] = round(v, 4)
@@ -560,11 +695,14 @@ def main(argv=None):
     ap.add_argument("--workload", default="decode", choices=sorted(WORKLOADS),
                     help="synthetic workload of the timed step (decode is the headline)")
     ap.add_argument("--no-mixed", action="store_true")
+    ap.add_argument("--no-extras", action="store_true",
+                    help="skip the 16k-decode, prefill-segment and long-tail lines that the "
+                         "default (decode) run reports beside the headline")
     ap.add_argument("--kv", default="bf16", choices=["bf16", "fp8"],
                     help="KV cache type: bf16, or float8_e4m3fn codes with per-tensor scales "
                          "(head_dim 128 workloads)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--cpu-budget", type=float, default=15.0)
+    ap.add_argument("--cpu-budget", type=float, default=10.0)
     ap.add_argument("--no-clocks", action="store_true",
                     help="skip the loaded windows around the timed region that the clock "
                          "samples need (for profiler runs)")

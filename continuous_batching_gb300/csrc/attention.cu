@@ -46,6 +46,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cmath>
 #include <cstring>
 #include <mutex>
@@ -1447,7 +1448,9 @@ __global__ void __launch_bounds__(256)
     const int s = int(w / Hq);
     const int head = int(w % Hq);
     const int64_t tok = __ldg(cu + s);
-    if (__ldg(cu + s + 1) - tok != 1 || tok >= T) return;
+    // metadata the attention kernel rejects (a row outside [0, T)) is skipped here too, so
+    // that no partial or output outside the caller's buffers is touched
+    if (__ldg(cu + s + 1) - tok != 1 || tok < 0 || tok >= T) return;
     const int pos = __ldg(ctx + s) - 1;
     if (pos < 0) return;                      // inconsistent metadata: flagged by the kernel
     const int nsp = pos / kSplit + 1;
@@ -1500,16 +1503,18 @@ __global__ void __launch_bounds__(256)
 
 // ------------------------------------------------------------------------- host side
 
+// The driver's tensor-map encoder, looked up once per process (a function-local static is
+// initialised exactly once even when several host threads call this at the same time).
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    if (!fn) {
+    static const PFN_cuTensorMapEncodeTiled_v12000 fn = []() {
         void* ptr = nullptr;
         cudaDriverEntryPointQueryResult q;
         if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
                                              cudaEnableDefault, &q) == cudaSuccess &&
             q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
-    }
+            return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+        return PFN_cuTensorMapEncodeTiled_v12000(nullptr);
+    }();
     return fn;
 }
 
@@ -1589,19 +1594,29 @@ int32_t make_maps(Maps* m, const void* q, const void* k_pool, const void* v_pool
     return make_map(&m->qn, q, D, s->num_q_heads, T, g, kRows / g);
 }
 
+constexpr int kMaxDevices = 64;
+
+// Raises the kernel's dynamic shared-memory limit once per device. Several host threads (one
+// per GPU, say) may get here at once: the flags are atomic, and the attribute call is
+// idempotent, so two threads that both find a flag clear both set the same value.
+template <int D, bool F8>
+int32_t ensure_smem_attr(int dev) {
+    static std::atomic<bool> raised[kMaxDevices];     // zero-initialised: not raised yet
+    if (dev < 0 || dev >= kMaxDevices) return PA_ERR_INVALID;
+    if (raised[dev].load(std::memory_order_acquire)) return PA_OK;
+    const int32_t st = note_cuda(cudaFuncSetAttribute(
+        paged_attn_kernel<D, F8>, cudaFuncAttributeMaxDynamicSharedMemorySize, Layout<D>::kAlloc));
+    if (st) return st;
+    raised[dev].store(true, std::memory_order_release);
+    return PA_OK;
+}
+
 template <int D, bool F8>
 int32_t launch(const Maps& maps, const Params& prm, int32_t max_ctx, cudaStream_t stream) {
-    static int attr_device = -1;          // device the shared-memory limit was raised on
     int dev = 0;
     int32_t st = note_cuda(cudaGetDevice(&dev));
     if (st) return st;
-    if (attr_device != dev) {
-        st = note_cuda(cudaFuncSetAttribute(paged_attn_kernel<D, F8>,
-                                            cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                            Layout<D>::kAlloc));
-        if (st) return st;
-        attr_device = dev;
-    }
+    if ((st = ensure_smem_attr<D, F8>(dev))) return st;
     const int grid = std::min(prm.n_items, PA_PLAN_CTAS);      // one CTA per list of the plan
     // Both kernels are programmatic dependents of what precedes them on the stream: each
     // launches while its predecessor drains and waits (griddepcontrol.wait) before it reads
@@ -1696,6 +1711,8 @@ extern "C" int32_t paged_attention_step(const void* q, const void* k_pool, const
     if (T == 0 || n_items == 0) return PA_OK;
     if (max_ctx > kSplit && (!workspace || ws_bytes < pa_workspace_bytes(shape, T, max_ctx)))
         return PA_ERR_WORKSPACE;
+    // the partials are stored and loaded as 8- and 16-byte vectors
+    if (max_ctx > kSplit && (reinterpret_cast<uintptr_t>(workspace) & 15)) return PA_ERR_INVALID;
     Maps maps;
     Params prm;
     if ((st = prepare_step(q, k_pool, v_pool, block_table, max_blocks, cu_seqlens_q, ctx_lens, B,
@@ -1726,6 +1743,7 @@ extern "C" int32_t paged_attention_step_fp8(const void* q, const void* k_pool, c
     if (T == 0 || n_items == 0) return PA_OK;
     if (max_ctx > kSplit && (!workspace || ws_bytes < pa_workspace_bytes(shape, T, max_ctx)))
         return PA_ERR_WORKSPACE;
+    if (max_ctx > kSplit && (reinterpret_cast<uintptr_t>(workspace) & 15)) return PA_ERR_INVALID;
     Maps maps;
     Params prm;
     if ((st = prepare_step(q, k_pool, v_pool, block_table, max_blocks, cu_seqlens_q, ctx_lens, B,
@@ -1749,7 +1767,6 @@ namespace {
 
 static __device__ __align__(256) float g_static_scratch[PA_STATIC_SCRATCH_BYTES / sizeof(float)];
 
-constexpr int kMaxDevices = 64;
 float* g_static_scratch_addr[kMaxDevices] = {};   // device address per device, set on first use
 std::mutex g_static_scratch_mu;
 

@@ -91,7 +91,7 @@ class Step:
         return int(self.ctx_lens.astype(np.int64).sum())
 
 
-CONFIG_NAMES = ("tiny", "decode", "mixed", "longtail", "prefix")
+CONFIG_NAMES = ("tiny", "decode", "mixed", "longtail", "prefix", "long16k")
 
 
 def _blocks_for(ctx: np.ndarray, bs: int) -> np.ndarray:
@@ -146,8 +146,10 @@ def make_config(name: str, with_pool: bool = True, seed: Optional[int] = None) -
     prefix   Hq 32, Hkv 8, D 128, bs 16: 16 prompts of 1024 tokens x 8 samples; each sample's
              table starts with its prompt's 64 full blocks (shared by 8 tables) followed by
              its own blocks for a U[1, 3000]-token continuation; 128 decode rows.
+    long16k  Hq 32, Hkv 8, D 128, bs 16: 32 decode rows, every one at ctx 16,384 (the cap of
+             the decode batch's lengths), permuted tables.
     """
-    seeds = {"tiny": 0, "decode": 1, "mixed": 2, "longtail": 3, "prefix": 4}
+    seeds = {"tiny": 0, "decode": 1, "mixed": 2, "longtail": 3, "prefix": 4, "long16k": 5}
     if name not in seeds:
         raise KeyError(f"unknown workload {name!r}; expected one of {CONFIG_NAMES}")
     seed = seeds[name] if seed is None else seed
@@ -177,6 +179,14 @@ def make_config(name: str, with_pool: bool = True, seed: Optional[int] = None) -
         table = _perm_tables(rng, nblk, nb)
         return _finish(name, rng, Hq, Hkv, D, bs, nb, ctx, n_q, table, with_pool, seed,
                        notes={"prefill_offsets": offs.tolist()})
+    if name == "long16k":
+        Hq, Hkv, D, bs, B = 32, 8, 128, 16, 32
+        ctx = np.full(B, 16384, dtype=np.int32)
+        nblk = _blocks_for(ctx, bs)
+        nb = int(nblk.sum())
+        table = _perm_tables(rng, nblk, nb)
+        return _finish(name, rng, Hq, Hkv, D, bs, nb, ctx, np.ones(B, np.int32), table,
+                       with_pool, seed)
     if name == "longtail":
         Hq, Hkv, D, bs, B = 64, 8, 128, 32, 128
         n_long = int(round(0.1 * B))

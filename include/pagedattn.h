@@ -329,10 +329,11 @@ int32_t paged_copy_blocks(const int32_t* pairs, int32_t n_pairs, void* k_pool, v
  * Device inputs: q [T, Hq, D] bf16; k_pool, v_pool [num_blocks, block_size, Hkv, D] bf16;
  * block_table [B, max_blocks] int32; cu_seqlens_q [B+1], ctx_lens [B] int32 (the same values
  * given to pa_plan_step); items [n_items] from pa_plan_step; workspace of ws_bytes >=
- * pa_workspace_bytes(shape, T, max_ctx) with max_ctx >= every ctx_lens[s].
+ * pa_workspace_bytes(shape, T, max_ctx) with max_ctx >= every ctx_lens[s], 16-byte aligned
+ * (partials are stored and read as vectors; it may be NULL when max_ctx <= PA_SPLIT_TOKENS).
  * Device output: out [T, Hq, D] bf16 (rows not covered by items are not written).
- * Host checks: pointers, shape support, workspace size; T == 0 or n_items == 0 launches
- * nothing. */
+ * Host checks: pointers, shape support, workspace size (PA_ERR_WORKSPACE) and alignment
+ * (PA_ERR_INVALID); T == 0 or n_items == 0 launches nothing. */
 int32_t paged_attention_step(const void* q, const void* k_pool, const void* v_pool,
                              const int32_t* block_table, int32_t max_blocks,
                              const int32_t* cu_seqlens_q, const int32_t* ctx_lens,
@@ -387,8 +388,11 @@ int32_t paged_attention_step_fp8(const void* q, const void* k_pool, const void* 
  *   - The first call on each device looks up the array's device address (cudaGetSymbolAddress,
  *     with that device current); make that first call before any stream capture.
  *   - Every call on a device shares the one array, and it keeps whatever the last call left
- *     there; nothing in it needs to start at zero, because every partial the combine reads is
- *     written earlier in the same call. Calls whose kernels overlap on the GPU (different
+ *     there. Nothing in it needs to start at zero for a plan from pa_plan_step (or one that
+ *     meets the list rules of pa_work_item): every partial the combine reads is then written
+ *     earlier in the same call. A plan that leaves out an item of a multi-split decode row
+ *     gives an undefined result for that row, which may fold stale partials of an earlier
+ *     call, another caller's included. Calls whose kernels overlap on the GPU (different
  *     streams, no ordering between them) race on the array: order them on one stream or with
  *     events. */
 #define PA_STATIC_SCRATCH_BYTES (32u << 20)

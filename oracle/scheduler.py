@@ -107,7 +107,7 @@ class SchedulerModel:
                     if not victims:
                         ok = False
                         break
-                    self._preempt(max(victims, key=lambda v: self.seqs[v].stamp))
+                    self._preempt(self._pick_victim(victims))
             if ok:
                 out.append((q, n))
                 done.add(q)
@@ -119,7 +119,7 @@ class SchedulerModel:
             src = None
             if s.leader is not None and s.leader in self.seqs:
                 lead = self.seqs[s.leader]
-                share = (s.prompt_len - 1) // self.bs
+                share = self._shared_blocks(s)
                 if s.leader in self.finished:
                     share = 0
                 elif s.leader not in self.running or lead.num_computed < share * self.bs:
@@ -141,6 +141,14 @@ class SchedulerModel:
             budget -= n
         self._scheduled = out
         return [(q, n, self.seqs[q].num_computed + n) for q, n in out]
+
+    def _pick_victim(self, victims: List[int]) -> int:
+        """S3: the youngest (latest admitted) of the candidates."""
+        return max(victims, key=lambda v: self.seqs[v].stamp)
+
+    def _shared_blocks(self, s: SeqState) -> int:
+        """S6: the leading full blocks before the last prompt token, which is recomputed."""
+        return (s.prompt_len - 1) // self.bs
 
     def _preempt(self, q: int) -> None:
         self.cache.free_seq(q)

@@ -7,6 +7,14 @@ from continuous_batching_gb300 import workloads as wl
 
 MAX_ABS = 1.5e-2      # tolerance on bf16 outputs vs the fp64 oracle (max |diff|)
 MEAN_ABS = 2e-3       # and mean |diff|
+# Scaled to each (row, head): max_d |diff| <= REL * rms_d(oracle row) + REL_FLOOR. The absolute
+# bounds above cannot see a dropped key tile at long context (outputs there are only ~0.01
+# RMS); this one can. The kernel rounds P to bf16 (2^-9 relative), sums l from the fp32 P and
+# rounds the output to bf16 (2^-9 relative), which an fp32 emulation puts at <= 2^-6.4 of the
+# row's RMS; a dropped 128-key tile moves a row by >= 0.08 of its RMS at ctx <= 40960
+# (tests/test_oracle_pins.py checks that on the oracle).
+REL = 2.0 ** -5
+REL_FLOOR = 1e-4
 
 
 def to_dev(a, torch, dtype=None):
@@ -45,10 +53,23 @@ def pool_np(t, torch):
     return t.view(torch.int16).cpu().numpy().view(np.uint16)
 
 
+def rel_error(got: np.ndarray, want: np.ndarray) -> np.ndarray:
+    """Per (row, head): max_d |got - want| / (REL * rms_d(want) + REL_FLOOR); <= 1 passes."""
+    d = np.abs(got - want).max(axis=-1)
+    rms = np.sqrt((want ** 2).mean(axis=-1))
+    return d / (REL * rms + REL_FLOOR)
+
+
 def assert_close(got_bits: np.ndarray, want: np.ndarray, what: str = ""):
+    """bf16 output bits against the fp64 oracle [rows, Hq, D]: the absolute bounds and the
+    per-(row, head) scaled bound. Returns (max|diff|, mean|diff|, max scaled ratio)."""
     got = pa.bf16_to_f64(got_bits)
     assert np.all(np.isfinite(got)), f"{what}: non-finite output"
     d = np.abs(got - want)
     assert d.max() <= MAX_ABS, f"{what}: max|diff| {d.max():.3e}"
     assert d.mean() <= MEAN_ABS, f"{what}: mean|diff| {d.mean():.3e}"
-    return float(d.max()), float(d.mean())
+    r = rel_error(got, want) if d.size else np.zeros(1)
+    worst = np.unravel_index(int(np.argmax(r)), r.shape) if d.size else ()
+    assert r.max() <= 1.0, (f"{what}: (row, head) {worst} off by {r.max():.2f} x "
+                            f"(REL * rms + floor)")
+    return float(d.max()), float(d.mean()), float(r.max())

@@ -24,5 +24,16 @@ def test_every_workload_has_a_description_and_seed():
         if name == "prefill":
             continue
         assert bench.rank_seed(name, 0) == {"decode": 1, "mixed": 2, "longtail": 3,
-                                            "prefix": 4}[name]
+                                            "prefix": 4, "long16k": 5}[name]
     assert set(bench.TOKEN_WORKLOADS) <= set(bench.WORKLOADS)
+
+
+def test_cpu_baseline_pool_matches_the_oracle_work_on_the_tiny_step():
+    """The multi-core CPU baseline runs the oracle in spawned workers over shared memory and
+    counts whole passes: two workers, a zero budget (one pass)."""
+    st = wl.make_config("tiny")
+    r = bench.cpu_baseline(st, budget_s=0.0, workers=2)
+    assert r["cores"] == 2 and r["kind"] == "oracle" and r["value"] > 0
+    assert "1 full pass" in r["sample"]
+    t = bench.cpu_baseline(st, budget_s=0.0, tokens=True, workers=2)
+    assert t["unit"] == "tokens/s" and t["value"] > 0

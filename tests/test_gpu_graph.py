@@ -6,9 +6,10 @@ with n_q == 0 items, table padded with -1) and the graph reads them at replay.""
 import numpy as np
 import pytest
 
+import oracle.paged_attention as pa
 from continuous_batching_gb300 import binding as bd
 from continuous_batching_gb300 import workloads as wl
-from tests.gpu_util import bf16_dev, shape_of
+from tests.gpu_util import assert_close, bf16_dev, pool_np, shape_of
 
 pytestmark = pytest.mark.gpu
 torch = pytest.importorskip("torch")
@@ -71,6 +72,10 @@ def test_captured_decode_step_replays_new_metadata_bitwise():
                       bf16_dev(st.v_new, torch))
         assert runner.device_error() == 0
         assert np.array_equal(got, want)
+        # and the replayed step is the oracle's attention over the pool it wrote
+        ref = pa.attention(st.q, pool_np(kp, torch), pool_np(vp, torch), st.block_table,
+                           st.cu_seqlens_q, st.ctx_lens, st.Hq)
+        assert_close(got.view(np.uint16), ref, f"replay ctx max {int(st.ctx_lens.max())}")
 
 
 def test_captured_mixed_step_equals_direct_launch():
@@ -147,3 +152,28 @@ def test_full_size_bench_graphs_equal_direct_launches(name, kv):
     # the end-to-end path (host metadata, pinned uploads, the same graphs) as well
     g.step_e2e()
     assert np.array_equal(g.h_out.numpy(), got)
+    # the replayed graphs against the oracle on sampled rows (the longest row, both ends of
+    # every prefill segment, a seeded sample)
+    rng = np.random.default_rng(99)
+    rows = set(rng.choice(st.T, size=min(12, st.T), replace=False).tolist())
+    rows.add(int(st.cu_seqlens_q[int(np.argmax(st.ctx_lens)) + 1]) - 1)
+    for s in range(st.B):
+        a, b = int(st.cu_seqlens_q[s]), int(st.cu_seqlens_q[s + 1])
+        if b - a > 1:
+            rows.update([a, b - 1])
+    rows = np.array(sorted(rows))
+    # the oracle reads a compact pool of the blocks those rows' sequences use
+    seq_of = np.searchsorted(st.cu_seqlens_q, rows, side="right") - 1
+    nblk = (st.ctx_lens + st.block_size - 1) // st.block_size
+    used = np.unique(np.concatenate([st.block_table[s, :nblk[s]] for s in np.unique(seq_of)]))
+    remap = np.full(st.num_blocks, -1, np.int32)
+    remap[used] = np.arange(len(used), dtype=np.int32)
+    table = np.where(st.block_table >= 0, remap[np.maximum(st.block_table, 0)], -1)
+    if kv == "fp8":
+        from oracle import fp8
+        kp = fp8.dequantize(g.kp.cpu().numpy()[used], g.kv_scales[0])
+        vp = fp8.dequantize(g.vp.cpu().numpy()[used], g.kv_scales[1])
+    else:
+        kp, vp = pool_np(g.kp, torch)[used], pool_np(g.vp, torch)[used]
+    ref = pa.attention_rows(st.q, kp, vp, table, st.cu_seqlens_q, st.ctx_lens, st.Hq, rows)
+    assert_close(got.view(np.uint16)[rows], ref, f"bench graphs {name} {kv}")

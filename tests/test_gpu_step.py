@@ -257,3 +257,40 @@ def test_host_rejects_bad_arguments_before_launch():
     with pytest.raises(bd.PagedAttnError):
         bd.paged_attention_step(q, kp, kp, runner.table, runner.cu, runner.ctx, 100,
                                 runner.items, runner.ws, out, bad)
+
+
+def test_negative_row_start_is_skipped_without_writing_outside_out():
+    """cu_seqlens_q forged on the device so that a multi-split decode sequence starts at row
+    -1: the attention kernel flags its items (PA_DEVERR_META) and skips them, the split
+    combine skips the row, and nothing lands outside `out` (guard rows on both sides)."""
+    st = wl.make_step(16, 4, 128, 16, [5000, 4500, 700], [1, 1, 1], seed=94)
+    shape = shape_of(st)
+    import tests.gpu_util as gu
+    kp, vp = gu.bf16_dev(st.k_pool, torch), gu.bf16_dev(st.v_pool, torch)
+    q = gu.bf16_dev(st.q, torch)
+    runner = bd.StepRunner(shape).prepare(st.cu_seqlens_q, st.ctx_lens, st.block_table)
+    cu = st.cu_seqlens_q.copy()
+    cu[0], cu[1] = -1, 0                       # sequence 0: one row starting at -1
+    runner.cu = torch.from_numpy(cu).cuda()
+    guard = torch.full((st.T + 2, st.Hq, st.D), 7.0, dtype=torch.bfloat16, device="cuda")
+    out = guard[1:st.T + 1]
+    runner.ws.fill_(float("nan"))
+    runner.attend(q, kp, vp, out)
+    torch.cuda.synchronize()
+    assert runner.device_error() & bd.PA_DEVERR_META
+    g = guard.float().cpu().numpy()
+    assert np.all(g[0] == 7.0) and np.all(g[st.T + 1] == 7.0)
+
+
+def test_host_rejects_a_misaligned_workspace():
+    st = wl.make_step(8, 2, 128, 16, [3000], [1], seed=95)
+    shape = shape_of(st)
+    runner = bd.StepRunner(shape).prepare(st.cu_seqlens_q, st.ctx_lens, st.block_table)
+    import tests.gpu_util as gu
+    q, kp = gu.bf16_dev(st.q, torch), gu.bf16_dev(st.k_pool, torch)
+    out = torch.zeros((st.T, st.Hq, st.D), dtype=torch.bfloat16, device="cuda")
+    ws = torch.empty(runner.ws.numel() + 4, dtype=torch.float32, device="cuda")
+    with pytest.raises(bd.PagedAttnError) as e:
+        bd.paged_attention_step(q, kp, kp, runner.table, runner.cu, runner.ctx, runner.max_ctx,
+                                runner.items, ws[1:], out, shape)
+    assert e.value.status == bd.PA_ERR_INVALID

@@ -236,7 +236,8 @@ def test_page_integer_examples():
 
 
 def test_workload_shapes():
-    want_T = {"tiny": 4, "decode": 64, "mixed": 2096, "longtail": 128, "prefix": 128}
+    want_T = {"tiny": 4, "decode": 64, "mixed": 2096, "longtail": 128, "prefix": 128,
+              "long16k": 32}
     for name in wl.CONFIG_NAMES:
         st = wl.make_config(name, with_pool=False)
         assert st.T == want_T[name]
@@ -315,3 +316,109 @@ def test_planted_mutants_are_killed(monkeypatch, name, fn, check):
             check_brute_force(tiny_mixed(5))
         else:
             check_layout_equivalence()
+
+
+# --------------------------------------------------------- the subset path of the oracle
+
+def _subset_cases():
+    st = wl.make_step(8, 2, 16, 4, [1, 13, 9, 22, 40, 5], [1, 1, 9, 6, 17, 5], seed=31)
+    rng = np.random.default_rng(3)
+    yield st, np.array([17, 3, 0, 25]), "unsorted, several sequences"
+    yield st, rng.permutation(st.T)[:11], "random sparse subset"
+    yield st, np.array([st.T - 1]), "the last row alone"
+    yield st, np.array([5, 5, 2]), "a repeated row"
+    yield st, np.arange(st.T)[::-1].copy(), "every row, reversed"
+
+
+def test_attention_rows_on_subsets_equals_full_attention_and_brute_force():
+    """attention_rows(rows) is the full step's attention at those rows, bit for bit, for any
+    order, gaps, repeats and mix of sequences; and it agrees with the brute-force loop."""
+    for st, rows, what in _subset_cases():
+        slots, kp, vp, full = run_step(st)
+        sub = pa.attention_rows(st.q, kp, vp, st.block_table, st.cu_seqlens_q, st.ctx_lens,
+                                st.Hq, rows)
+        assert np.array_equal(sub, full[rows]), what
+        brute = brute_force_rows(st, kp, vp)
+        assert np.abs(sub - brute[rows]).max() <= 1e-12, what
+
+
+def _attention_rows_slip(q, k_pool, v_pool, block_table, cu_seqlens_q, ctx_lens, Hq, rows,
+                         scale=None):
+    """The subset path with a plausible indexing slip: positions taken by subset index."""
+    rows = np.asarray(rows, dtype=np.int64)
+    D = k_pool.shape[-1]
+    scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
+    seq_of, pos_of = pa.row_positions(cu_seqlens_q, ctx_lens)
+    out = np.empty((len(rows), Hq, D), dtype=np.float64)
+    for s in np.unique(seq_of[rows]):
+        sel = np.nonzero(seq_of[rows] == s)[0]
+        ctx = int(ctx_lens[s])
+        K = pa._as_f64(pa.gather(k_pool, block_table[s], ctx))
+        V = pa._as_f64(pa.gather(v_pool, block_table[s], ctx))
+        out[sel] = pa._attend_sequence(pa._as_f64(q[rows[sel]]), K, V,
+                                       np.minimum(pos_of[sel], ctx - 1), Hq, scale)
+    return out
+
+
+def test_subset_pin_kills_an_indexing_slip(monkeypatch):
+    # control: every row in order, where the slip is invisible, passes
+    st = next(_subset_cases())[0]
+    _, kp, vp, full = run_step(st)
+    every = np.arange(st.T)
+    assert np.array_equal(_attention_rows_slip(st.q, kp, vp, st.block_table, st.cu_seqlens_q,
+                                               st.ctx_lens, st.Hq, every), full)
+    monkeypatch.setattr(pa, "attention_rows", _attention_rows_slip)
+    with pytest.raises(AssertionError):
+        test_attention_rows_on_subsets_equals_full_attention_and_brute_force()
+
+
+# ------------------------------------------- power of the GPU tests' scaled tolerance
+
+def _one_row(ctx, rng, D=128, Hq=32, Hkv=8):
+    q = pa.bf16_to_f64(wl.random_bf16(rng, (Hq, D)))
+    K = pa.bf16_to_f64(wl.random_bf16(rng, (Hkv, ctx, D)))
+    V = pa.bf16_to_f64(wl.random_bf16(rng, (Hkv, ctx, D)))
+    return q, K, V
+
+
+@pytest.mark.parametrize("ctx", [16384, 40960])
+def test_scaled_tolerance_rejects_a_dropped_tile_or_split(ctx):
+    """The per-(row, head) bound REL * rms + floor of the GPU parity tests fails an output that
+    misses one 128-key tile, or one 2048-key split, of a decode row at 16k and 40k context,
+    while the absolute bounds (max 1.5e-2, mean 2e-3) accept it. The mistake is planted in the
+    oracle (keys removed before its softmax), on the CPU."""
+    from tests.gpu_util import MAX_ABS, MEAN_ABS, rel_error
+    rng = np.random.default_rng(ctx)
+    q, K, V = _one_row(ctx, rng, Hq=4, Hkv=1)          # one KV head and its group of 4
+    pos = np.array([ctx - 1])
+    scale = 1.0 / math.sqrt(128)
+    ref = pa._attend_sequence(q[None], K, V, pos, 4, scale)
+    for lo, hi in ((0, 128), (ctx // 2 - 64, ctx // 2 + 64), (ctx - 128, ctx),
+                   (2048, 4096), (ctx - 2048, ctx)):
+        keep = np.r_[0:lo, hi:ctx]
+        bad = pa._attend_sequence(q[None], K[:, keep], V[:, keep], pos - (hi - lo), 4, scale)
+        d = np.abs(bad - ref)
+        if hi - lo == 128:
+            assert d.max() <= MAX_ABS and d.mean() <= MEAN_ABS    # invisible to these
+        assert rel_error(bad, ref).max() > 1.0, (lo, hi)
+
+
+def test_scaled_tolerance_accepts_the_kernel_roundings():
+    """An fp32 restatement of the roundings the kernel makes (P rounded to bf16 before PV, l
+    summed from the fp32 P, the output rounded to bf16) stays inside the scaled bound."""
+    from tests.gpu_util import rel_error
+    rng = np.random.default_rng(5)
+
+    def bf16(x):
+        return pa.bf16_to_f64(wl.f32_to_bf16_bits(np.asarray(x, np.float32)))
+    worst = 0.0
+    for ctx in (1, 100, 2048, 16384):
+        q, K, V = _one_row(ctx, rng, Hq=8, Hkv=2)
+        ref = pa._attend_sequence(q[None], K, V, np.array([ctx - 1]), 8, 1 / math.sqrt(128))
+        got = np.empty_like(ref)
+        for h in range(8):
+            s = K[h // 4] @ q[h] / math.sqrt(128)
+            p32 = np.exp2(((s - s.max()) * math.log2(math.e)).astype(np.float32)).astype(np.float64)
+            got[0, h] = bf16((bf16(p32) @ V[h // 4]) / p32.astype(np.float32).sum(dtype=np.float32))
+        worst = max(worst, rel_error(got, ref).max())
+    assert worst <= 0.5

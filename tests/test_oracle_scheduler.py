@@ -213,3 +213,150 @@ def test_mutant_scheduler_without_decode_priority_is_caught():
     m.commit()                                   # 1 finished its prompt: a decode now
     st = m.step()
     assert st[0][0] == 0                         # the mutant schedules the prefill first
+
+
+# --------------------------------------------------------------- pins that kill mutants
+# The P3 page's Evidence item 5 asks that planted mistakes be killed. Each pin below is a
+# property the page states (Design / engine.py, Admit/evict and Prefix sharing); it passes on
+# the model and fails on a mutant that breaks exactly that property.
+
+def pin_preemption(model_cls):
+    """Admit/evict: on exhaustion the youngest running sequence not yet scheduled is preempted
+    by recompute (its blocks freed, num_computed = 0); the books balance after every step and
+    the pool is fully free at the end, every request having produced all its tokens."""
+    m = model_cls(30, 4, chunk=512, budget=2048)
+    m.add(100, 8, 60)
+    m.step()
+    m.commit()
+    for i in range(6):
+        m.add(i, 24, 40)
+    for _ in range(10000):
+        if m.idle():
+            break
+        running = list(m.running)
+        stamps = {q: m.seqs[q].stamp for q in running}
+        n_before = m.preemptions
+        try:
+            st = m.step()
+            m.cache.check_consistent()
+        except Exception as e:                 # the model itself gave up
+            raise AssertionError(f"step failed: {e!r}")
+        scheduled = {q for q, _, _ in st}
+        gone = [q for q in running if q not in m.running]
+        assert len(gone) == m.preemptions - n_before
+        for v in gone:
+            # the victim was younger than every other sequence it could have been
+            others = [q for q in running if q not in scheduled and q != v and q not in gone]
+            assert all(stamps[v] > stamps[q] for q in others), "not the youngest"
+            assert v not in m.cache.tables, "a preempted sequence keeps its blocks"
+            assert m.seqs[v].num_computed == 0
+        try:
+            m.commit()
+            m.cache.check_consistent()
+        except Exception as e:
+            raise AssertionError(f"commit failed: {e!r}")
+    assert m.idle() and m.preemptions > 0
+    assert m.cache.alloc.num_free == 30
+    assert all(m.seqs[i].generated == 40 for i in range(6)) and m.seqs[100].generated == 60
+
+
+def pin_prefix_sharing(model_cls, P, bs=8):
+    """Prefix sharing: a follower adopts only leading FULL blocks of its leader, shares every
+    full block before its last prompt token, and always recomputes that token: its first
+    step starts at the first unshared position and ends at ctx == P with n >= 1. Its writes
+    land in private blocks and the pool is free at the end."""
+    m = model_cls(64, bs, chunk=16, budget=64)
+    m.add(0, P, 3)
+    for f in (1, 2, 3):
+        m.add(f, P, 3, leader=0)
+    first = {}
+    for _ in range(1000):
+        if m.idle():
+            break
+        try:
+            st = m.step()
+        except Exception as e:
+            raise AssertionError(f"step failed: {e!r}")
+        for q, n, ctx in st:
+            if q in (1, 2, 3) and q not in first:
+                assert 0 in m.cache.tables, "the leader finished before its followers ran"
+                shared = [b for b in m.table(q) if m.cache.alloc.ref[b] > 1]
+                k = len(shared)
+                assert m.table(q)[:k] == m.table(0)[:k], "shared blocks are not the leader's"
+                assert k * bs <= P - 1, "a shared block holds the last prompt token or is partial"
+                assert (k + 1) * bs > P - 1, "a full block before the last token is not shared"
+                assert n >= 1 and ctx - n == k * bs and ctx <= P, (q, n, ctx, k)
+                first[q] = (n, ctx)
+            try:
+                m.slots(q, ctx - n, n)
+            except Exception as e:
+                raise AssertionError(f"write of sequence {q} refused: {e!r}")
+        try:
+            m.commit()
+            m.cache.check_consistent()
+        except Exception as e:
+            raise AssertionError(f"commit failed: {e!r}")
+    assert set(first) == {1, 2, 3}
+    assert all(ctx == P or ctx < P for n, ctx in first.values())
+    assert m.idle() and m.cache.alloc.num_free == 64
+
+
+def pin_youngest_victim(model_cls):
+    """Admit/evict, "preempt the youngest": A, B, C (admitted in that order) decode in lockstep
+    until their next block is missing for all three. The visit serves A first (decodes in
+    admission order); the candidates are then B and C, and C, the youngest, must go back to
+    waiting while A and B both run."""
+    m = model_cls(6, 4, chunk=512, budget=2048)
+    for i in range(3):
+        m.add(i, 4, 10)
+    for _ in range(20):
+        st = m.step()
+        m.commit()
+        if m.preemptions:
+            break
+    assert m.preemptions == 1, m.preemptions
+    assert [q for q, _, _ in st] == [0, 1], st
+    assert list(m.waiting) == [2] and m.running == [0, 1]
+
+
+class _OldestVictim(sc.SchedulerModel):
+    def _pick_victim(self, victims):
+        return min(victims, key=lambda v: self.seqs[v].stamp)
+
+
+class _PreemptKeepsBlocks(sc.SchedulerModel):
+    def _preempt(self, q):
+        self.running.remove(q)
+        s = self.seqs[q]
+        s.num_computed = 0
+        s.stamp = -1
+        self.waiting.appendleft(q)
+        self.preemptions += 1
+
+
+class _SharesPartialBlock(sc.SchedulerModel):
+    def _shared_blocks(self, s):
+        return (s.prompt_len + self.bs - 1) // self.bs
+
+
+class _NoLastTokenRecompute(sc.SchedulerModel):
+    def _shared_blocks(self, s):
+        return s.prompt_len // self.bs
+
+
+def test_pins_pass_on_the_model():
+    pin_youngest_victim(sc.SchedulerModel)
+    pin_preemption(sc.SchedulerModel)
+    for P in (30, 32, 33, 9, 8):
+        pin_prefix_sharing(sc.SchedulerModel, P)
+
+
+@pytest.mark.parametrize("mutant,pin", [
+    (_OldestVictim, lambda c: pin_youngest_victim(c)),
+    (_PreemptKeepsBlocks, lambda c: pin_preemption(c)),
+    (_SharesPartialBlock, lambda c: pin_prefix_sharing(c, 30)),
+    (_NoLastTokenRecompute, lambda c: pin_prefix_sharing(c, 32)),
+])
+def test_scheduler_mutants_are_killed(mutant, pin):
+    with pytest.raises(AssertionError):
+        pin(mutant)

@@ -5,9 +5,10 @@ reserved up front by a serving process, a plug-in that only gets tensors from it
 framework, a loop that cannot take cudaMalloc's implicit synchronisation): it keeps its split
 partials in a fixed array inside the library instead of a caller-provided workspace. This
 test calls it through the C ABI, twice in a row with different steps that both need the
-scratch, and checks each output against paged_attention_step's within the tolerance the other
-GPU tests use. It also checks that a step too large for the fixed array is refused.
-This file is named so that pytest collects it last."""
+scratch, and checks that each output has the bits of paged_attention_step's (the same
+kernels with the same arithmetic; only where the partials live differs), and that the call
+leaves the device's free memory unchanged. It also checks that a step too large for the
+fixed array is refused. This file is named so that pytest collects it last."""
 import ctypes as C
 
 import numpy as np
@@ -59,19 +60,30 @@ def _call_static(lib, st, shape, runner, kp, vp, q, out):
 def test_static_scratch_matches_workspace_entry_point_twice(lib):
     steps = [wl.make_step(32, 8, 128, 16, [3000, 17, 1100, 2100], [1, 1, 77, 33], seed=41),
              wl.make_step(64, 8, 128, 32, [5000, 1025, 40], [1, 100, 1], seed=42)]
-    for st in steps:
+    for i, st in enumerate(steps):
         shape, runner, kp, vp, q = _prepare(st)
         assert bd.pa_workspace_bytes(shape, st.T, runner.max_ctx) <= STATIC_SCRATCH_BYTES
         ref_out = torch.empty((st.T, st.Hq, st.D), dtype=torch.bfloat16, device="cuda")
         runner.attend(q, kp, vp, ref_out)
         out = torch.full((st.T, st.Hq, st.D), float("nan"), dtype=torch.bfloat16, device="cuda")
+        torch.cuda.synchronize()
+        free_before = torch.cuda.mem_get_info()[0]
         assert _call_static(lib, st, shape, runner, kp, vp, q, out) == bd.PA_OK
         torch.cuda.synchronize()
+        if i > 0:
+            # past the first call (which looks the array up on this device), a call takes
+            # no device memory
+            assert torch.cuda.mem_get_info()[0] == free_before
         assert runner.device_error() == 0
-        got = pa.bf16_to_f64(out.view(torch.int16).cpu().numpy().view(np.uint16))
-        want = pa.bf16_to_f64(ref_out.view(torch.int16).cpu().numpy().view(np.uint16))
-        assert np.all(np.isfinite(got))
-        d = np.abs(got - want)
+        got = out.view(torch.int16).cpu().numpy()
+        want = ref_out.view(torch.int16).cpu().numpy()
+        assert np.all(np.isfinite(pa.bf16_to_f64(got.view(np.uint16))))
+        assert np.array_equal(got, want)
+        # and, for the record, both are the oracle's attention within the parity tolerance
+        d = np.abs(pa.bf16_to_f64(got.view(np.uint16)) -
+                   pa.attention(st.q, kp.view(torch.int16).cpu().numpy().view(np.uint16),
+                                vp.view(torch.int16).cpu().numpy().view(np.uint16),
+                                st.block_table, st.cu_seqlens_q, st.ctx_lens, st.Hq))
         assert d.max() <= MAX_ABS and d.mean() <= MEAN_ABS
 
 
