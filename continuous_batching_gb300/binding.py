@@ -138,6 +138,9 @@ def load() -> C.CDLL:
         _sig(lib, "paged_attention_step", C.c_int32,
              [_vp, _vp, _vp, _vp, C.c_int32, _vp, _vp, C.c_int32, C.c_int32, C.c_int32,
               _vp, C.c_int32, _vp, C.c_size_t, _vp, sp, _vp, _vp])
+        _sig(lib, "paged_attention_step_wait_test", C.c_int32,
+             [_vp, _vp, _vp, _vp, C.c_int32, _vp, _vp, C.c_int32, C.c_int32, C.c_int32,
+              _vp, C.c_int32, _vp, C.c_size_t, _vp, sp, _vp, C.c_uint64, _vp])
         _sig(lib, "paged_kv_write_fp8", C.c_int32,
              [_vp, _vp, _vp, C.c_int32, _vp, _vp, C.c_float, C.c_float, sp, _vp, _vp])
         _sig(lib, "paged_attention_step_fp8", C.c_int32,

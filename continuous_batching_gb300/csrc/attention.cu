@@ -122,7 +122,8 @@ enum Bar {
     kKReady = 37,    // + K slot
     kVReady = 41,    // + V slot
     kQReady = 47,    // + Q buffer
-    kNumBars = 49
+    kNever = 49,     // nothing ever arrives here: the wait-timeout test waits on it
+    kNumBars = 50
 };
 constexpr int kHolderOff = 8 * kNumBars;          // TMEM address written by tcgen05.alloc
 constexpr int kAbortOff = kHolderOff + 4;
@@ -149,6 +150,8 @@ struct Params {
     float c;            // log2(e) / sqrt(D) (times the K scale of an fp8 cache): softmax
                         // works in base 2 on raw scores
     float v_scale;      // V scale of an fp8 cache (1 for bf16): out = O * (rcp(l) * v_scale)
+    unsigned long long never_ns;   // nonzero only in the wait-timeout test: the softmax warps
+                                   // first wait this long on kNever, which nothing completes
 };
 
 // ----------------------------------------------------------------- PTX wrappers
@@ -211,15 +214,16 @@ __device__ __forceinline__ unsigned long long global_ns() {
 }
 
 // Waits for the phase of `bar` with the given parity. Gives up when another role has set
-// the CTA's abort word or after kWaitLimitNs; then sets the abort word and returns false.
-__device__ bool wait_bounded(uint32_t bar, uint32_t parity, volatile int* abort_word) {
+// the CTA's abort word or after limit_ns; then sets the abort word and returns false.
+__device__ bool wait_bounded(uint32_t bar, uint32_t parity, volatile int* abort_word,
+                             unsigned long long limit_ns = kWaitLimitNs) {
     if (mbar_try_wait(bar, parity)) return true;
     const unsigned long long t0 = global_ns();
     for (;;) {
         for (int i = 0; i < 32; ++i)
             if (mbar_try_wait(bar, parity)) return true;
         if (*abort_word) return false;
-        if (global_ns() - t0 > kWaitLimitNs) {
+        if (global_ns() - t0 > limit_ns) {
             *abort_word = 1;
             return false;
         }
@@ -278,24 +282,72 @@ __device__ __forceinline__ void tmem_wait_st() {
     asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
-// D[tmem] (+)= A[smem] * B[smem]^T, kind::f16 (bf16 inputs, fp32 accumulator).
-__device__ __forceinline__ void umma_bf16(uint32_t issue, uint32_t d_tmem, uint64_t a_desc,
-                                          uint64_t b_desc, uint32_t idesc, uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t.reg .pred q;\n\tsetp.ne.b32 p, %4, 0;\n\tsetp.ne.b32 q, %5, 0;\n\t"
-        "@q tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate), "r"(issue)
-        : "memory");
+// The MMA groups of one tile, each in one asm block: the issuing warp shares its scheduler
+// with two softmax warps that take most issue slots, so every instruction between two MMAs
+// costs tensor-pipe time. The predicates are set once per group, and a step k only adds its
+// offset / 16 to the low word of a shared-memory descriptor (the start-address field, bits
+// 0-13, never carries: shared addresses stay below 2^18).
+//
+// S group: D[tmem] = sum_k A_k B_k^T with A = Q, B = K (both K-major in shared memory); step k
+// reads 16 columns at byte offset (k / 4) * 16384 + (k % 4) * 32 of both operands.
+#define PA_S_STEP(OFF, PRED)                                                                   \
+    "add.u32 x, al, " #OFF ";\n\tadd.u32 y, bl, " #OFF ";\n\tmov.b64 a, {x, ah};\n\t"            \
+    "mov.b64 b, {y, bh};\n\t@q tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, " PRED ";\n\t"
+template <int D>
+__device__ __forceinline__ void issue_s_group(uint32_t issue, uint32_t d, uint64_t qdesc,
+                                              uint64_t kdesc, uint32_t idesc) {
+    static_assert(D == 64 || D == 128, "head_dim");
+    if constexpr (D == 128) {
+        asm volatile(
+            "{\n\t.reg .pred q, pt, pf;\n\t.reg .b32 al, ah, bl, bh, x, y;\n\t.reg .b64 a, b;\n\t"
+            "setp.ne.b32 q, %4, 0;\n\tsetp.eq.b32 pt, %4, %4;\n\tsetp.ne.b32 pf, %4, %4;\n\t"
+            "mov.b64 {al, ah}, %1;\n\tmov.b64 {bl, bh}, %2;\n\t"
+            "@q tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, pf;\n\t"
+            PA_S_STEP(2, "pt") PA_S_STEP(4, "pt") PA_S_STEP(6, "pt") PA_S_STEP(1024, "pt")
+            PA_S_STEP(1026, "pt") PA_S_STEP(1028, "pt") PA_S_STEP(1030, "pt") "}" ::"r"(d),
+            "l"(qdesc), "l"(kdesc), "r"(idesc), "r"(issue)
+            : "memory");
+    } else {
+        asm volatile(
+            "{\n\t.reg .pred q, pt, pf;\n\t.reg .b32 al, ah, bl, bh, x, y;\n\t.reg .b64 a, b;\n\t"
+            "setp.ne.b32 q, %4, 0;\n\tsetp.eq.b32 pt, %4, %4;\n\tsetp.ne.b32 pf, %4, %4;\n\t"
+            "mov.b64 {al, ah}, %1;\n\tmov.b64 {bl, bh}, %2;\n\t"
+            "@q tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, pf;\n\t"
+            PA_S_STEP(2, "pt") PA_S_STEP(4, "pt") PA_S_STEP(6, "pt") "}" ::"r"(d), "l"(qdesc),
+            "l"(kdesc), "r"(idesc), "r"(issue)
+            : "memory");
+    }
 }
+#undef PA_S_STEP
 
-// D[tmem] (+)= A[tmem] * B[smem]^T, kind::f16; A is 128 lanes (rows) x packed bf16 pairs.
-__device__ __forceinline__ void umma_bf16_tmem_a(uint32_t issue, uint32_t d_tmem,
-                                                 uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
-                                                 uint32_t accumulate) {
+// PV group: D[tmem] (+)= sum_k P_k V_k, P from TMEM (8 packed columns per 16 keys, at p + 8 k),
+// V from shared memory (MN-major) at descriptor offset off[k] (off[0] = 0); the first step
+// accumulates only when acc is set.
+__device__ __forceinline__ void issue_pv_group(uint32_t issue, uint32_t d, uint32_t p_tmem,
+                                               uint64_t vdesc, uint32_t idesc, uint32_t acc,
+                                               const uint32_t (&off)[8]) {
     asm volatile(
-        "{\n\t.reg .pred p;\n\t.reg .pred q;\n\tsetp.ne.b32 p, %4, 0;\n\tsetp.ne.b32 q, %5, 0;\n\t"
-        "@q tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate), "r"(issue)
+        "{\n\t.reg .pred q, pt, p0;\n\t.reg .b32 vl, vh, x, t;\n\t.reg .b64 b;\n\t"
+        "setp.ne.b32 q, %4, 0;\n\tsetp.eq.b32 pt, %4, %4;\n\tsetp.ne.b32 p0, %5, 0;\n\t"
+        "mov.b64 {vl, vh}, %2;\n\t"
+        "@q tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p0;\n\t"
+        "add.u32 t, %1, 8;\n\tadd.u32 x, vl, %7;\n\tmov.b64 b, {x, vh};\n\t"
+        "@q tcgen05.mma.cta_group::1.kind::f16 [%0], [t], b, %3, pt;\n\t"
+        "add.u32 t, %1, 16;\n\tadd.u32 x, vl, %8;\n\tmov.b64 b, {x, vh};\n\t"
+        "@q tcgen05.mma.cta_group::1.kind::f16 [%0], [t], b, %3, pt;\n\t"
+        "add.u32 t, %1, 24;\n\tadd.u32 x, vl, %9;\n\tmov.b64 b, {x, vh};\n\t"
+        "@q tcgen05.mma.cta_group::1.kind::f16 [%0], [t], b, %3, pt;\n\t"
+        "add.u32 t, %1, 32;\n\tadd.u32 x, vl, %10;\n\tmov.b64 b, {x, vh};\n\t"
+        "@q tcgen05.mma.cta_group::1.kind::f16 [%0], [t], b, %3, pt;\n\t"
+        "add.u32 t, %1, 40;\n\tadd.u32 x, vl, %11;\n\tmov.b64 b, {x, vh};\n\t"
+        "@q tcgen05.mma.cta_group::1.kind::f16 [%0], [t], b, %3, pt;\n\t"
+        "add.u32 t, %1, 48;\n\tadd.u32 x, vl, %12;\n\tmov.b64 b, {x, vh};\n\t"
+        "@q tcgen05.mma.cta_group::1.kind::f16 [%0], [t], b, %3, pt;\n\t"
+        "add.u32 t, %1, 56;\n\tadd.u32 x, vl, %13;\n\tmov.b64 b, {x, vh};\n\t"
+        "@q tcgen05.mma.cta_group::1.kind::f16 [%0], [t], b, %3, pt;\n\t"
+        "}" ::"r"(d),
+        "r"(p_tmem), "l"(vdesc), "r"(idesc), "r"(issue), "r"(acc), "r"(off[0]), "r"(off[1]),
+        "r"(off[2]), "r"(off[3]), "r"(off[4]), "r"(off[5]), "r"(off[6]), "r"(off[7])
         : "memory");
 }
 
@@ -999,10 +1051,11 @@ __global__ void __launch_bounds__(kThreadsFor<F8>, 1)
         }
     } else if (warp == 9) {
         // ------------------------------------------------------------ MMA issuer
-        // All 32 lanes run the loop (uniform control flow, no divergence on any branch); lane
-        // 0 alone issues the MMAs, commits and arrivals, through predicates.
-        {
-            const uint32_t leader = lane == 0 ? 1u : 0u;
+        // Lane 0 alone runs the loop: the warp shares its scheduler with two softmax warps,
+        // and every instruction it issues between MMA groups leaves the tensor pipe idle, so
+        // no warp-wide work is spent on it (the other lanes wait at the final barrier).
+        if (lane == 0) {
+            const uint32_t leader = 1u;
             constexpr uint32_t idesc_s = make_idesc(kRows, kTileKeys, false, F8);
             constexpr uint32_t idesc_o = make_idesc(kRows, D, true, F8);
             static_assert(L::kQHalf == L::kKVHalf, "Q and K chunks share the step offsets");
@@ -1015,12 +1068,9 @@ __global__ void __launch_bounds__(kThreadsFor<F8>, 1)
             const uint64_t kd0 = make_sdesc(sb + L::kK, 16, 1024);
             constexpr uint32_t kBufStep = uint32_t(L::kKVTile) >> 4;
             static_assert(L::kQBuf == L::kKVTile, "Q buffers and K/V slots have one size");
+            static_assert(L::kQHalf == 16384, "the S group's step offsets");
             const auto issue_s = [&](uint64_t qdesc, uint64_t kdesc, uint32_t d) {
-#pragma unroll
-                for (int k = 0; k < D / 16; ++k) {
-                    const uint32_t off = uint32_t((k >> 2) * L::kQHalf + (k & 3) * 32) >> 4;
-                    umma_bf16(leader, d, qdesc + off, kdesc + off, idesc_s, k > 0);
-                }
+                issue_s_group<D>(leader, d, qdesc, kdesc, idesc_s);
             };
             // V tile: block b of the tile at b * bs * 128 * chunks bytes, its 64-column halves
             // bs * 128 bytes apart (MN-major B operand: LBO = half stride, SBO = 8-key stride)
@@ -1039,13 +1089,10 @@ __global__ void __launch_bounds__(kThreadsFor<F8>, 1)
                                 uint32_t(key & (p.bs - 1)) * 128) >> 4;
                 }
             }
+            static_assert(kTileKeys / 16 == 8, "eight PV steps per tile");
             const auto issue_pv = [&](uint64_t vdesc, uint32_t p_tmem, uint32_t d, bool acc) {
-#pragma unroll
-                for (int k = 0; k < kTileKeys / 16; ++k) {
-                    // P of keys 16k .. 16k+15 is 8 packed columns of the S buffer
-                    umma_bf16_tmem_a(leader, d, p_tmem + 8 * k, vdesc + v_off[k], idesc_o,
-                                     (acc || k > 0) ? 1u : 0u);
-                }
+                // P of keys 16k .. 16k+15 is 8 packed columns of the S buffer
+                issue_pv_group(leader, d, p_tmem, vdesc, idesc_o, acc ? 1u : 0u, v_off);
             };
             // Two cursors walk the same item sequence: one issues S = Q K^T for the next tile
             // as soon as its K has landed (and its S buffer is free), the other issues O += P V
@@ -1315,7 +1362,10 @@ __global__ void __launch_bounds__(kThreadsFor<F8>, 1)
             reinterpret_cast<const volatile ItemSlot*>(smem + L::kBar + kRingOff);
         int tc = 0, ic = 0, sg = 0;       // tiles, items and splits seen
         bool ok = true;
-        for (;;) {
+        // the wait-timeout test: a wait that nothing completes runs out, and every role leaves
+        // through the same path as after any other wait that ran out
+        if (p.never_ns) ok = wait_bounded(bar(kNever), 0, abort_word, p.never_ns);
+        for (; ok;) {
             if (!(ok = wait_bounded(bar(kItemFull + (ic & 3)), (ic >> 2) & 1, abort_word))) break;
             bool last;
             const Item I = slot_item(ring + (ic & 3), &last);
@@ -1686,6 +1736,7 @@ int32_t prepare_step(const void* q, const void* k_pool, const void* v_pool,
     prm->num_blocks = shape->num_blocks;
     prm->c = float(1.4426950408889634 / std::sqrt(double(D)));
     prm->v_scale = 1.f;
+    prm->never_ns = 0;
     return PA_OK;
 }
 
@@ -1718,6 +1769,33 @@ extern "C" int32_t paged_attention_step(const void* q, const void* k_pool, const
     if ((st = prepare_step(q, k_pool, v_pool, block_table, max_blocks, cu_seqlens_q, ctx_lens, B,
                            T, max_ctx, items, n_items, out, shape, err_flag, &maps, &prm)))
         return st;
+    point_workspace(&prm, static_cast<float*>(workspace), T, shape->num_q_heads, shape->head_dim);
+    if (shape->head_dim == 128) return launch<128, false>(maps, prm, max_ctx, stream);
+    return launch<64, false>(maps, prm, max_ctx, stream);
+}
+
+// The wait-timeout test: paged_attention_step with the softmax role first waiting, for at most
+// never_ns, on a barrier that nothing completes (see pagedattn.h).
+extern "C" int32_t paged_attention_step_wait_test(
+    const void* q, const void* k_pool, const void* v_pool, const int32_t* block_table,
+    int32_t max_blocks, const int32_t* cu_seqlens_q, const int32_t* ctx_lens, int32_t B,
+    int32_t T, int32_t max_ctx, const pa_work_item* items, int32_t n_items, void* workspace,
+    size_t ws_bytes, void* out, const pa_shape* shape, int32_t* err_flag,
+    uint64_t never_ns, pa_stream_t stream) {
+    int32_t st = check_shape(shape);
+    if (st) return st;
+    if (B < 0 || T < 0 || n_items < 0 || max_ctx < 0 || max_blocks < 0) return PA_ERR_INVALID;
+    if (never_ns == 0 || never_ns > kWaitLimitNs) return PA_ERR_INVALID;
+    if (T == 0 || n_items == 0) return PA_OK;
+    if (max_ctx > kSplit && (!workspace || ws_bytes < pa_workspace_bytes(shape, T, max_ctx)))
+        return PA_ERR_WORKSPACE;
+    if (max_ctx > kSplit && (reinterpret_cast<uintptr_t>(workspace) & 15)) return PA_ERR_INVALID;
+    Maps maps;
+    Params prm;
+    if ((st = prepare_step(q, k_pool, v_pool, block_table, max_blocks, cu_seqlens_q, ctx_lens, B,
+                           T, max_ctx, items, n_items, out, shape, err_flag, &maps, &prm)))
+        return st;
+    prm.never_ns = never_ns;
     point_workspace(&prm, static_cast<float*>(workspace), T, shape->num_q_heads, shape->head_dim);
     if (shape->head_dim == 128) return launch<128, false>(maps, prm, max_ctx, stream);
     return launch<64, false>(maps, prm, max_ctx, stream);

@@ -342,6 +342,23 @@ int32_t paged_attention_step(const void* q, const void* k_pool, const void* v_po
                              void* workspace, size_t ws_bytes, void* out,
                              const pa_shape* shape, int32_t* err_flag, pa_stream_t stream);
 
+/* Test of the bounded-wait error path (no counterpart on the pages: a diagnostic of this
+ * library). The same call as paged_attention_step, except that the softmax role of every CTA
+ * first waits, for at most never_ns nanoseconds (1 .. 10^9), on a barrier that nothing ever
+ * completes. That wait runs out, the CTA's roles leave their loops exactly as after any other
+ * wait that runs out (each drains its own copies and MMAs, with its usual bounded waits, and
+ * TMEM is freed), PA_DEVERR_TIMEOUT is ORed into *err_flag, and the kernel returns; the
+ * outputs of the step are then undefined, but the device stays usable for the next call. It
+ * faults nothing and hangs nothing. PA_ERR_INVALID for never_ns outside that range. */
+int32_t paged_attention_step_wait_test(const void* q, const void* k_pool, const void* v_pool,
+                                       const int32_t* block_table, int32_t max_blocks,
+                                       const int32_t* cu_seqlens_q, const int32_t* ctx_lens,
+                                       int32_t B, int32_t T, int32_t max_ctx,
+                                       const pa_work_item* items, int32_t n_items,
+                                       void* workspace, size_t ws_bytes, void* out,
+                                       const pa_shape* shape, int32_t* err_flag,
+                                       uint64_t never_ns, pa_stream_t stream);
+
 /* ------------------------------------------------------------------ FP8 KV cache
  * K and V stored as float8_e4m3fn codes (1 byte each) with one scale per tensor ("P3: native
  * paged-KV continuous-batching sampler", Review, kv_dtype item: dequantised on read; unscaled

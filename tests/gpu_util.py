@@ -60,6 +60,11 @@ def rel_error(got: np.ndarray, want: np.ndarray) -> np.ndarray:
     return d / (REL * rms + REL_FLOOR)
 
 
+# (what, max|diff|, mean|diff|, max scaled ratio) of every comparison in this process; the
+# test session writes them to the file PA_PARITY_STATS names, if set
+STATS = []
+
+
 def assert_close(got_bits: np.ndarray, want: np.ndarray, what: str = ""):
     """bf16 output bits against the fp64 oracle [rows, Hq, D]: the absolute bounds and the
     per-(row, head) scaled bound. Returns (max|diff|, mean|diff|, max scaled ratio)."""
@@ -69,6 +74,8 @@ def assert_close(got_bits: np.ndarray, want: np.ndarray, what: str = ""):
     assert d.max() <= MAX_ABS, f"{what}: max|diff| {d.max():.3e}"
     assert d.mean() <= MEAN_ABS, f"{what}: mean|diff| {d.mean():.3e}"
     r = rel_error(got, want) if d.size else np.zeros(1)
+    if d.size:
+        STATS.append((what, float(d.max()), float(d.mean()), float(r.max())))
     worst = np.unravel_index(int(np.argmax(r)), r.shape) if d.size else ()
     assert r.max() <= 1.0, (f"{what}: (row, head) {worst} off by {r.max():.2f} x "
                             f"(REL * rms + floor)")

@@ -1,6 +1,8 @@
 """GPU parity of the hot path through the C ABI: KV write bit-exact against the oracle, bf16
 attention within max|diff| <= 1.5e-2 and mean|diff| <= 2e-3 of the fp64 oracle, on small
 cases in full and on the five named workloads at full size (sampled rows)."""
+import ctypes as C
+
 import numpy as np
 import pytest
 
@@ -294,3 +296,56 @@ def test_host_rejects_a_misaligned_workspace():
         bd.paged_attention_step(q, kp, kp, runner.table, runner.cu, runner.ctx, runner.max_ctx,
                                 runner.items, ws[1:], out, shape)
     assert e.value.status == bd.PA_ERR_INVALID
+
+
+def test_a_wait_that_runs_out_sets_the_timeout_bit_and_the_device_stays_usable():
+    """The bounded-wait error path, made to run without faulting anything: the test entry
+    point has the softmax role wait 2 ms on a barrier nothing completes. The call returns, the
+    error word carries PA_DEVERR_TIMEOUT, and the next ordinary step on the same buffers is
+    the oracle's, with a clean error word."""
+    for st in (wl.make_config("tiny"), wl.make_step(32, 8, 128, 16, [3000, 40, 700], [1, 1, 64],
+                                                    seed=96)):
+        shape = shape_of(st)
+        import tests.gpu_util as gu
+        kp, vp = gu.bf16_dev(st.k_pool, torch), gu.bf16_dev(st.v_pool, torch)
+        q = gu.bf16_dev(st.q, torch)
+        runner = bd.StepRunner(shape).prepare(st.cu_seqlens_q, st.ctx_lens, st.block_table)
+        runner.write(gu.bf16_dev(st.k_new, torch), gu.bf16_dev(st.v_new, torch), kp, vp)
+        out = torch.zeros((st.T, st.Hq, st.D), dtype=torch.bfloat16, device="cuda")
+        ws = runner.ws
+        lib = bd.load()
+        stream = torch.cuda.current_stream().cuda_stream
+        rc = lib.paged_attention_step_wait_test(
+            q.data_ptr(), kp.data_ptr(), vp.data_ptr(), runner.table.data_ptr(),
+            int(runner.table.shape[1]), runner.cu.data_ptr(), runner.ctx.data_ptr(), st.B, st.T,
+            runner.max_ctx, runner.items.data_ptr(), int(runner.items.numel() // 8),
+            ws.data_ptr() if ws is not None and ws.numel() else None,
+            0 if ws is None else ws.numel() * 4, out.data_ptr(), C.byref(shape),
+            runner.err.data_ptr(), 2_000_000, stream)
+        assert rc == bd.PA_OK
+        torch.cuda.synchronize()
+        assert runner.device_error() & bd.PA_DEVERR_TIMEOUT
+        runner.err.zero_()
+        runner.attend(q, kp, vp, out)
+        torch.cuda.synchronize()
+        assert runner.device_error() == 0
+        ref = pa.attention(st.q, pool_np(kp, torch), pool_np(vp, torch), st.block_table,
+                           st.cu_seqlens_q, st.ctx_lens, st.Hq)
+        assert_close(out.view(torch.int16).cpu().numpy().view(np.uint16), ref, "after a timeout")
+
+
+def test_wait_test_rejects_limits_outside_its_range():
+    st = wl.make_config("tiny")
+    shape = shape_of(st)
+    runner = bd.StepRunner(shape).prepare(st.cu_seqlens_q, st.ctx_lens, st.block_table)
+    import tests.gpu_util as gu
+    q = gu.bf16_dev(st.q, torch)
+    out = torch.zeros((st.T, st.Hq, st.D), dtype=torch.bfloat16, device="cuda")
+    lib = bd.load()
+    for never in (0, 2_000_000_000):
+        rc = lib.paged_attention_step_wait_test(
+            q.data_ptr(), q.data_ptr(), q.data_ptr(), runner.table.data_ptr(),
+            int(runner.table.shape[1]), runner.cu.data_ptr(), runner.ctx.data_ptr(), st.B, st.T,
+            runner.max_ctx, runner.items.data_ptr(), int(runner.items.numel() // 8), None, 0,
+            out.data_ptr(), C.byref(shape), None, never, None)
+        assert rc == bd.PA_ERR_INVALID
