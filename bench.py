@@ -258,10 +258,14 @@ class GpuStep:
                                                  self.out, attend=False)
         self.g_attend = self.graph_runner.capture(self.q, self.kn, self.vn, self.kp, self.vp,
                                                   self.out, write=False)
-        # pinned host copies for the end-to-end measurement
+        # pinned host copies for the end-to-end measurement, and the public pipeline that runs
+        # steps from them (two buffer sets, so that one step's host work and copies overlap the
+        # kernels of the step before it)
         pin = lambda a: torch.from_numpy(a.view(np.int16).copy()).pin_memory()
         self.h_q, self.h_kn, self.h_vn = pin(st.q), pin(st.k_new), pin(st.v_new)
-        self.h_out = torch.empty((st.T, st.Hq, st.D), dtype=torch.int16).pin_memory()
+        self.h_out = [torch.empty((st.T, st.Hq, st.D), dtype=torch.int16).pin_memory()
+                      for _ in range(2)]
+        self.pipe = bd.StepPipeline(self.shape, lim, self.kp, self.vp, kv_scales=self.kv_scales)
 
     def launches_per_step(self) -> int:
         """kv_write_kernel, paged_attn_kernel, and the split combine when a context spans more
@@ -272,25 +276,31 @@ class GpuStep:
     def step(self):
         self.runner.run(self.q, self.kn, self.vn, self.kp, self.vp, self.out)
 
-    def step_e2e(self):
-        """Public API from host buffers, as a serving loop runs it: plan + slots on the host and
-        one pinned upload of the step's metadata (StepRunner with StepLimits), H2D of the new
-        tokens' q / k / v from pinned memory, the captured write and attention graphs, D2H of
-        the output, and a wait for it."""
-        torch, st = self.torch, self.st
-        # the new tokens' copies go first, so that they run while the host plans the step
-        self.q.view(torch.int16).copy_(self.h_q, non_blocking=True)
-        self.kn.view(torch.int16).copy_(self.h_kn, non_blocking=True)
-        self.vn.view(torch.int16).copy_(self.h_vn, non_blocking=True)
-        self.graph_runner.prepare(st.cu_seqlens_q, st.ctx_lens, st.block_table)
-        self.g_write.replay()
-        self.g_attend.replay()
-        self.h_out.copy_(self.out.view(torch.int16), non_blocking=True)
-        torch.cuda.current_stream().synchronize()
+    def submit_e2e(self, i: int):
+        """Step i through the public pipeline from host buffers: plan and slots on the host, one
+        pinned metadata upload, pinned H2D of the new tokens' q / k / v, the captured KV write
+        and attention, D2H of the output. Returns the event after which its output is on the
+        host."""
+        st = self.st
+        return self.pipe.submit(st.cu_seqlens_q, st.ctx_lens, st.block_table, self.h_q,
+                                self.h_kn, self.h_vn, self.h_out[i % 2])
+
+    def run_e2e(self, n: int) -> float:
+        """n steps end to end, each step's output read back before its host buffer is reused;
+        returns seconds per step (wall clock from the first submission to the last output)."""
+        pending = []
+        t0 = time.perf_counter()
+        for i in range(n):
+            pending.append(self.submit_e2e(i))
+            if len(pending) > 1:
+                pending.pop(0).synchronize()          # the previous step's output is on the host
+        while pending:
+            pending.pop(0).synchronize()
+        return (time.perf_counter() - t0) / n
 
     def e2e_bytes(self):
         st = self.st
-        h2d = st.q.nbytes + st.k_new.nbytes + st.v_new.nbytes + self.graph_runner.meta_bytes
+        h2d = st.q.nbytes + st.k_new.nbytes + st.v_new.nbytes + self.pipe.meta_bytes
         return h2d, st.T * st.Hq * st.D * 2
 
 
@@ -472,14 +482,9 @@ def run_ours(args) -> dict:
     ms_per_step = total_ms / args.steps
     value = all_units / (ms_per_step * 1e-3) * scale
 
-    # end to end through the public API with host buffers
-    for _ in range(2):
-        g.step_e2e()
-    t1 = time.perf_counter()
-    n_e2e = max(3, args.steps // 2)
-    for _ in range(n_e2e):
-        g.step_e2e()
-    e2e_s = (time.perf_counter() - t1) / n_e2e
+    # end to end through the public API with host buffers (StepPipeline)
+    g.run_e2e(4)
+    e2e_s = g.run_e2e(max(8, args.steps))
     h2d, d2h = g.e2e_bytes()
 
     attn_avg = statistics.mean(attn_ms)

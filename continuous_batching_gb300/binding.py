@@ -141,6 +141,16 @@ def load() -> C.CDLL:
         _sig(lib, "paged_attention_step_wait_test", C.c_int32,
              [_vp, _vp, _vp, _vp, C.c_int32, _vp, _vp, C.c_int32, C.c_int32, C.c_int32,
               _vp, C.c_int32, _vp, C.c_size_t, _vp, sp, _vp, C.c_uint64, _vp])
+        pp = C.c_void_p                  # pa_pipeline*
+        _sig(lib, "pa_pipeline_create", C.c_int32,
+             [sp, C.c_int32, C.c_int32, C.c_int32, C.c_int32, _vp, _vp, C.c_int32, C.c_float,
+              C.c_float, C.POINTER(pp)])
+        _sig(lib, "pa_pipeline_destroy", C.c_int32, [pp])
+        _sig(lib, "pa_pipeline_meta_bytes", C.c_int64, [pp])
+        _sig(lib, "pa_pipeline_submit", C.c_int32,
+             [pp, _i32p, _i32p, _i32p, C.c_int32, _vp, _vp, _vp, _vp, _i32p])
+        _sig(lib, "pa_pipeline_wait", C.c_int32, [pp, C.c_int32])
+        _sig(lib, "pa_pipeline_device_error", C.c_int32, [pp, _i32p])
         _sig(lib, "paged_kv_write_fp8", C.c_int32,
              [_vp, _vp, _vp, C.c_int32, _vp, _vp, C.c_float, C.c_float, sp, _vp, _vp])
         _sig(lib, "paged_attention_step_fp8", C.c_int32,
@@ -651,3 +661,64 @@ class StepRunner:
 
     def device_error(self) -> int:
         return int(self.err.item())
+
+
+class StepPipeline:
+    """A stream of steps under fixed limits, run end to end from host buffers by the library's
+    native pipeline (pa_pipeline_* in pagedattn.h): per step one call plans the step into
+    pinned metadata and queues the uploads, the captured KV write + attention and the read of
+    the output, so that one step's host work and copies overlap the kernels of the step before
+    it. k_pool / v_pool are the device pools every step writes and reads (bf16, or uint8 codes
+    with kv_scales)."""
+
+    class Pending:
+        """A submitted step; synchronize() returns once its output is in its host buffer."""
+
+        def __init__(self, pipe, slot):
+            self.pipe, self.slot = pipe, slot
+
+        def synchronize(self):
+            _check(self.pipe._lib.pa_pipeline_wait(self.pipe._h, self.slot), "pa_pipeline_wait")
+
+    def __init__(self, shape: Shape, limits: StepLimits, k_pool, v_pool,
+                 kv_scales: Optional[tuple] = None):
+        self._lib = load()
+        self.shape, self.limits = shape, limits
+        self._pools = (k_pool, v_pool)                # kept alive as long as the pipeline
+        L = limits
+        fp8 = kv_scales is not None
+        ks, vs = (float(kv_scales[0]), float(kv_scales[1])) if fp8 else (1.0, 1.0)
+        h = C.c_void_p()
+        _check(self._lib.pa_pipeline_create(C.byref(shape), L.B, L.T, L.max_blocks, L.max_ctx,
+                                            _dev(k_pool), _dev(v_pool), 1 if fp8 else 0, ks, vs,
+                                            C.byref(h)), "pa_pipeline_create")
+        self._h = h
+
+    def close(self):
+        if getattr(self, "_h", None):
+            self._lib.pa_pipeline_destroy(self._h)
+            self._h = None
+
+    __del__ = close
+
+    @property
+    def meta_bytes(self) -> int:
+        return int(self._lib.pa_pipeline_meta_bytes(self._h))
+
+    def submit(self, cu_seqlens_q, ctx_lens, block_table, h_q, h_k_new, h_v_new, h_out):
+        """Queues one step; h_* are host tensors (pinned for asynchronous copies): q and out
+        [T, Hq, D], k_new and v_new [T, Hkv, D], bf16 (or int16 bit patterns). Returns a
+        Pending whose synchronize() returns once h_out holds the step's output."""
+        cu, ctx, table = _i32(cu_seqlens_q), _i32(ctx_lens), _i32(block_table)
+        slot = C.c_int32()
+        _check(self._lib.pa_pipeline_submit(self._h, _p32(cu), _p32(ctx), _p32(table),
+                                            int(table.shape[1]), h_q.data_ptr(),
+                                            h_k_new.data_ptr(), h_v_new.data_ptr(),
+                                            h_out.data_ptr(), C.byref(slot)),
+               "pa_pipeline_submit")
+        return StepPipeline.Pending(self, int(slot.value))
+
+    def device_error(self) -> int:
+        e = C.c_int32()
+        _check(self._lib.pa_pipeline_device_error(self._h, C.byref(e)), "pa_pipeline_device_error")
+        return int(e.value)

@@ -26,7 +26,7 @@ HEADERS = [os.path.join(ROOT, "include", "pagedattn.h")]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-O3",
          "--expt-relaxed-constexpr", "-I", os.path.join(ROOT, "include")]
-SOURCES = ["host.cpp", "sched.cpp", "kv_write.cu", "attention.cu"]
+SOURCES = ["host.cpp", "sched.cpp", "pipeline.cpp", "kv_write.cu", "attention.cu"]
 
 
 def nvcc() -> str:

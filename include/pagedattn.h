@@ -359,6 +359,51 @@ int32_t paged_attention_step_wait_test(const void* q, const void* k_pool, const 
                                        const pa_shape* shape, int32_t* err_flag,
                                        uint64_t never_ns, pa_stream_t stream);
 
+/* ------------------------------------------------------------------ step pipeline
+ * A stream of steps under fixed limits, run end to end from host buffers (no counterpart on
+ * the pages: the serving loop around "P3: native paged-KV continuous-batching sampler",
+ * Design / engine.py, one flat ragged step per engine step). Two slots take alternate steps;
+ * each owns device metadata, q / k_new / v_new / out buffers, a workspace, pinned host
+ * metadata, and a CUDA graph of its KV write (paged_kv_write, or paged_kv_write_fp8) and
+ * attention (paged_attention_step, or its fp8 form) captured once at creation. A submission
+ * plans the step on the host (pa_plan_step, pa_compute_slots into the slot's pinned
+ * metadata), then queues the uploads of the metadata and of the caller's q / k_new / v_new
+ * on one stream, the graph on a second (after the uploads, and after the previous step's
+ * kernels), and the read of the output into the caller's buffer on a third. One step's host
+ * work and copies so overlap the kernels of the step before it; the kernels run in
+ * submission order. Not thread-safe; one pipeline per device and host thread. */
+typedef struct pa_pipeline pa_pipeline;
+
+/* Creates a pipeline for steps of exactly B sequences and T query rows, tables of at most
+ * max_blocks columns and contexts up to max_ctx, over device pools k_pool / v_pool (bf16, or
+ * float8_e4m3fn codes with fp8 != 0 and the per-tensor scales k_scale, v_scale). Allocates its
+ * buffers (cudaMalloc, cudaMallocHost) and captures its graphs on the current device; the
+ * caller keeps the pools alive until pa_pipeline_destroy. *out owns the pipeline. */
+int32_t pa_pipeline_create(const pa_shape* shape, int32_t B, int32_t T, int32_t max_blocks,
+                           int32_t max_ctx, void* k_pool, void* v_pool, int32_t fp8,
+                           float k_scale, float v_scale, pa_pipeline** out);
+/* Waits for the pipeline's outstanding steps and frees everything it allocated (NULL ignored). */
+int32_t pa_pipeline_destroy(pa_pipeline* p);
+/* Bytes of metadata a submission uploads (the plan padded to pa_plan_max_items, cu_seqlens_q,
+ * ctx_lens, the table at max_blocks columns and the slots), or -1 for NULL. */
+int64_t pa_pipeline_meta_bytes(const pa_pipeline* p);
+/* Queues one step. Host inputs: cu_seqlens_q [B+1] (cu[B] == T), ctx_lens [B] (each <=
+ * max_ctx), block_table [B * table_cols] row-major (table_cols <= max_blocks); h_q [T, Hq, D],
+ * h_k_new / h_v_new [T, Hkv, D] bf16 and h_out [T, Hq, D] bf16, host memory (pinned memory
+ * makes the copies asynchronous). Validates everything before queueing anything (PA_ERR_*
+ * as pa_plan_step and pa_compute_slots). *slot receives the slot (0 or 1) the step went to.
+ * The caller leaves the step's host buffers alone until pa_pipeline_wait(p, slot) returns, and
+ * waits for a slot before submitting two more steps (a submission into a busy slot first
+ * waits for that slot's previous step). */
+int32_t pa_pipeline_submit(pa_pipeline* p, const int32_t* cu_seqlens_q, const int32_t* ctx_lens,
+                           const int32_t* block_table, int32_t table_cols, const void* h_q,
+                           const void* h_k_new, const void* h_v_new, void* h_out,
+                           int32_t* slot);
+/* Blocks until the step last submitted into slot has its output in its h_out. */
+int32_t pa_pipeline_wait(pa_pipeline* p, int32_t slot);
+/* Waits for outstanding steps, then ORs the device error words of both slots into *err. */
+int32_t pa_pipeline_device_error(pa_pipeline* p, int32_t* err);
+
 /* ------------------------------------------------------------------ FP8 KV cache
  * K and V stored as float8_e4m3fn codes (1 byte each) with one scale per tensor ("P3: native
  * paged-KV continuous-batching sampler", Review, kv_dtype item: dequantised on read; unscaled

@@ -149,9 +149,14 @@ def test_full_size_bench_graphs_equal_direct_launches(name, kv):
     torch.cuda.synchronize()
     assert r.device_error() == 0
     assert np.array_equal(got, out.view(torch.int16).cpu().numpy())
-    # the end-to-end path (host metadata, pinned uploads, the same graphs) as well
-    g.step_e2e()
-    assert np.array_equal(g.h_out.numpy(), got)
+    # the end-to-end pipeline (host metadata, pinned uploads, its own captured graphs), three
+    # steps in a row so that both of its buffer sets serve
+    evs = [g.submit_e2e(i) for i in range(3)]
+    for ev in evs:
+        ev.synchronize()
+    assert g.pipe.device_error() == 0
+    for h in g.h_out:
+        assert np.array_equal(h.numpy(), got)
     # the replayed graphs against the oracle on sampled rows (the longest row, both ends of
     # every prefill segment, a seeded sample)
     rng = np.random.default_rng(99)
@@ -177,3 +182,29 @@ def test_full_size_bench_graphs_equal_direct_launches(name, kv):
         kp, vp = pool_np(g.kp, torch)[used], pool_np(g.vp, torch)[used]
     ref = pa.attention_rows(st.q, kp, vp, table, st.cu_seqlens_q, st.ctx_lens, st.Hq, rows)
     assert_close(got.view(np.uint16)[rows], ref, f"bench graphs {name} {kv}")
+
+
+def test_pipeline_of_different_steps_equals_direct_launches():
+    """StepPipeline (two buffer sets, host work and copies of one step overlapping the kernels of
+    the previous one) gives every step of a stream the bits of direct launches, and the oracle's
+    attention."""
+    step1, step2 = _steps(seed=31)
+    kp, vp = bf16_dev(step2.k_pool, torch), bf16_dev(step2.v_pool, torch)
+    lim = bd.StepLimits(B=step2.B, T=step2.T, max_blocks=step2.block_table.shape[1], max_ctx=8192)
+    pipe = bd.StepPipeline(shape_of(step2), lim, kp, vp)
+    pin = lambda a: torch.from_numpy(a.view(np.int16).copy()).pin_memory()
+    stream = [step1, step2, step1, step2, step2]
+    host = [(pin(st.q), pin(st.k_new), pin(st.v_new),
+             torch.empty((st.T, st.Hq, st.D), dtype=torch.int16).pin_memory()) for st in stream]
+    events = [pipe.submit(st.cu_seqlens_q, st.ctx_lens, st.block_table, *h)
+              for st, h in zip(stream, host)]
+    for ev in events:
+        ev.synchronize()
+    assert pipe.device_error() == 0
+    for st, h in zip(stream, host):
+        want = _eager(st, kp, vp, bf16_dev(st.q, torch), bf16_dev(st.k_new, torch),
+                      bf16_dev(st.v_new, torch))
+        assert np.array_equal(h[3].numpy(), want)
+    ref = pa.attention(step2.q, pool_np(kp, torch), pool_np(vp, torch), step2.block_table,
+                       step2.cu_seqlens_q, step2.ctx_lens, step2.Hq)
+    assert_close(host[-1][3].numpy().view(np.uint16), ref, "pipeline")
