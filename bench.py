@@ -98,8 +98,10 @@ WORKLOADS = {
                 "16384, pool = 32*1024 blocks, permuted tables, bf16 ~N(0,1), seed 5"),
 }
 # reported beside the headline in the default run, each with its own roofline: the 16k-context
-# decode and the prefill segments (the two targets of the path) and the long-tail rollout
-EXTRAS = (("decode_16k", "long16k"), ("prefill_segments", "prefill"), ("longtail", "longtail"))
+# decode and the prefill segments (the two targets of the path), the long-tail rollout and the
+# prefix-shared decode
+EXTRAS = (("decode_16k", "long16k"), ("prefill_segments", "prefill"), ("longtail", "longtail"),
+          ("prefix_shared", "prefix"))
 # the value of these workloads is tokens/s (ragged steps); the others report KV GB/s
 TOKEN_WORKLOADS = ("mixed", "prefill")
 

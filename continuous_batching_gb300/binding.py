@@ -60,10 +60,13 @@ class Shape(C.Structure):
 class WorkItem(C.Structure):
     _fields_ = [("seq", C.c_int32), ("q_start", C.c_int32), ("n_q", C.c_int32),
                 ("kv_head", C.c_int32), ("split", C.c_int32), ("n_tiles", C.c_int32),
-                ("n_splits", C.c_int32), ("next", C.c_int32)]
+                ("n_splits", C.c_int32), ("next", C.c_int32), ("kind", C.c_int32),
+                ("tile0", C.c_int32)]
 
 
 WORK_ITEM_DTYPE = np.dtype([(n, np.int32) for n, _ in WorkItem._fields_])
+ITEM_INTS = len(WorkItem._fields_)          # int32 words per pa_work_item
+PA_ITEM_PLAIN, PA_ITEM_GROUP, PA_ITEM_RESUME = 0, 1, 2
 
 _lib = None
 _lock = threading.Lock()
@@ -129,6 +132,10 @@ def load() -> C.CDLL:
         _sig(lib, "pa_plan_max_items", C.c_int64, [sp, C.c_int32, C.c_int32, C.c_int32])
         _sig(lib, "pa_plan_step", C.c_int32,
              [sp, C.c_int32, _i32p, _i32p, C.POINTER(WorkItem), C.c_int32, _i32p])
+        _sig(lib, "pa_plan_max_items_shared", C.c_int64, [sp, C.c_int32, C.c_int32, C.c_int32])
+        _sig(lib, "pa_plan_step_shared", C.c_int32,
+             [sp, C.c_int32, _i32p, _i32p, _i32p, C.c_int32, C.POINTER(WorkItem), C.c_int32,
+              _i32p])
         _sig(lib, "pa_workspace_bytes", C.c_size_t, [sp, C.c_int32, C.c_int32])
         _sig(lib, "pa_upload_block_table", C.c_int32,
              [sp, _i32p, _vp, C.c_int32, C.c_int32, _vp])
@@ -406,6 +413,24 @@ def pa_plan_step(shape: Shape, cu_seqlens_q: np.ndarray, ctx_lens: np.ndarray) -
     return arr
 
 
+def pa_plan_step_shared(shape: Shape, cu_seqlens_q: np.ndarray, ctx_lens: np.ndarray,
+                        block_table: np.ndarray) -> np.ndarray:
+    """Work items with prefix sharing (GROUP / RESUME items for decode rows whose tables share
+    leading key tiles), as a numpy structured array (dtype WORK_ITEM_DTYPE)."""
+    lib = load()
+    cu, ctx, bt = _i32(cu_seqlens_q), _i32(ctx_lens), _i32(block_table)
+    B = len(ctx)
+    T = int(cu[-1]) if B else 0
+    max_ctx = int(ctx.max()) if B else 0
+    cap = int(lib.pa_plan_max_items_shared(C.byref(shape), B, T, max_ctx))
+    buf = (WorkItem * max(cap, 1))()
+    n = C.c_int32()
+    mb = bt.shape[1] if bt.ndim == 2 else 0
+    _check(lib.pa_plan_step_shared(C.byref(shape), B, _p32(cu), _p32(ctx), _p32(bt), mb, buf, cap,
+                                   C.byref(n)), "pa_plan_step_shared")
+    return np.frombuffer(buf, dtype=WORK_ITEM_DTYPE, count=max(cap, 1))[:n.value].copy()
+
+
 def pa_workspace_bytes(shape: Shape, T: int, max_ctx: int) -> int:
     return int(load().pa_workspace_bytes(C.byref(shape), int(T), int(max_ctx)))
 
@@ -440,7 +465,7 @@ def paged_attention_step(q, k_pool, v_pool, block_table, cu_seqlens_q, ctx_lens,
     """items: a device int32 tensor holding the pa_work_item records from pa_plan_step."""
     B = int(ctx_lens.shape[0])
     T = int(q.shape[0])
-    n_items = int(items.numel() // 8)
+    n_items = int(items.numel() // ITEM_INTS)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _check(load().paged_attention_step(
         _dev(q), _dev(k_pool), _dev(v_pool), _dev(block_table), int(block_table.shape[1]),
@@ -466,7 +491,7 @@ def paged_attention_step_fp8(q, k_pool, v_pool, block_table, cu_seqlens_q, ctx_l
     """paged_attention_step over uint8 float8_e4m3fn pools with per-tensor scales."""
     B = int(ctx_lens.shape[0])
     T = int(q.shape[0])
-    n_items = int(items.numel() // 8)
+    n_items = int(items.numel() // ITEM_INTS)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _check(load().paged_attention_step_fp8(
         _dev(q), _dev(k_pool), _dev(v_pool), _dev(block_table), int(block_table.shape[1]),
@@ -514,9 +539,9 @@ class StepRunner:
         if limits is not None:
             L = limits
             d = self.device
-            cap = int(load().pa_plan_max_items(C.byref(shape), L.B, L.T, L.max_ctx))
+            cap = int(load().pa_plan_max_items_shared(C.byref(shape), L.B, L.T, L.max_ctx))
             self.n_items_cap = max(cap, 1)
-            parts = (("items", self.n_items_cap * 8), ("cu", L.B + 1), ("ctx", L.B),
+            parts = (("items", self.n_items_cap * ITEM_INTS), ("cu", L.B + 1), ("ctx", L.B),
                      ("table", L.B * L.max_blocks), ("slots", L.T))
             total = sum(n for _, n in parts)
             self._meta = torch.empty(max(total, 1), dtype=torch.int32, device=d)
@@ -548,7 +573,7 @@ class StepRunner:
         cu, ctx = _i32(cu_seqlens_q), _i32(ctx_lens)
         if self.limits is not None:
             return self._prepare_fixed(cu, ctx, _i32(block_table), slot_mapping)
-        items = pa_plan_step(self.shape, cu, ctx)
+        items = pa_plan_step_shared(self.shape, cu, ctx, block_table)
         if slot_mapping is None:
             slot_mapping = pa_compute_slots(self.shape, block_table, cu, ctx)
         d = self.device
@@ -578,9 +603,9 @@ class StepRunner:
         lib = load()
         hi = self._h["items"]
         n = C.c_int32()
-        _check(lib.pa_plan_step(C.byref(self.shape), B, _p32(cu), _p32(ctx),
-                                hi.ctypes.data_as(C.POINTER(WorkItem)), self.n_items_cap,
-                                C.byref(n)), "pa_plan_step")
+        _check(lib.pa_plan_step_shared(C.byref(self.shape), B, _p32(cu), _p32(ctx), _p32(table),
+                                       table.shape[1], hi.ctypes.data_as(C.POINTER(WorkItem)),
+                                       self.n_items_cap, C.byref(n)), "pa_plan_step_shared")
         hs = hi.view(WORK_ITEM_DTYPE)
         if self._n_planned > n.value:
             hs[n.value:self._n_planned] = 0               # n_q == 0: padding

@@ -123,7 +123,9 @@ enum Bar {
     kVReady = 41,    // + V slot
     kQReady = 47,    // + Q buffer
     kNever = 49,     // nothing ever arrives here: the wait-timeout test waits on it
-    kNumBars = 50
+    kSaved = 50,     // softmax (256 arrivals) -> softmax: a GROUP item's rows have saved their
+                     //   state, which the RESUME items after it on the list restore
+    kNumBars = 51
 };
 constexpr int kHolderOff = 8 * kNumBars;          // TMEM address written by tcgen05.alloc
 constexpr int kAbortOff = kHolderOff + 4;
@@ -509,13 +511,14 @@ __device__ __forceinline__ void st_shared_zero16(uint32_t addr) {
 struct Item {
     bool good;
     int seq, ctx, q_start, n_q, kvh, split, n_splits, pos0, k_begin, n_tiles, rows_valid;
+    int kind, tile0;    // PA_ITEM_*; GROUP / RESUME: the shared tiles [0, tile0) of split 0
 };
 
 // What the producer publishes in an item slot (64 bytes); `last` marks the end of the CTA's
 // item list.
 struct ItemSlot {
     int seq, ctx, q_start, n_q, kvh, split, n_splits, pos0, k_begin, n_tiles, rows_valid, last,
-        pad[4];
+        kind, tile0, pad[2];
 };
 static_assert(sizeof(ItemSlot) == 64, "item slot size");
 
@@ -533,16 +536,52 @@ __device__ __forceinline__ Item slot_item(const volatile ItemSlot* sl, bool* las
     I.k_begin = sl->k_begin;
     I.n_tiles = sl->n_tiles;
     I.rows_valid = sl->rows_valid;
+    I.kind = sl->kind;
+    I.tile0 = sl->tile0;
     *last = sl->last != 0;
     return I;
 }
 
-__device__ __forceinline__ Item load_item(const Params& p, int idx) {
+// Called by all 32 lanes of the producer warp (a GROUP item's members are checked one per
+// lane).
+__device__ __forceinline__ Item load_item(const Params& p, int idx, int lane) {
     const pa_work_item it = p.items[idx];
     Item I;
+    const bool shared = it.kind == PA_ITEM_GROUP || it.kind == PA_ITEM_RESUME;
     bool good = it.seq >= 0 && it.seq < p.B && it.kv_head >= 0 && it.kv_head < p.Hkv &&
                 it.n_q >= 1 && it.n_q * p.g <= kRows && it.split >= 0 && it.q_start >= 0 &&
-                it.q_start + it.n_q <= p.T;
+                it.q_start + it.n_q <= p.T &&
+                (it.kind == PA_ITEM_PLAIN ||
+                 (shared && it.split == 0 && it.n_splits <= 1 && it.tile0 >= 1 &&
+                  it.tile0 < kSplitTiles && p.ws_acc != nullptr));
+    I.kind = good ? it.kind : PA_ITEM_PLAIN;
+    I.tile0 = good && shared ? it.tile0 : 0;
+    if (good && it.kind == PA_ITEM_GROUP) {
+        // the decode rows of sequences seq .. seq + n_q - 1 at tokens q_start .. , each with
+        // keys past the shared tiles; the shared tiles are read through seq's table
+        good = it.seq + it.n_q <= p.B;
+        bool mine = true;
+        if (good && lane < it.n_q) {
+            const int s = it.seq + lane;
+            const int c0 = p.cu[s], c1 = p.cu[s + 1], cx = p.ctx[s];
+            mine = c1 - c0 == 1 && c0 == it.q_start + lane && cx > it.tile0 * kTileKeys &&
+                   (int64_t(cx) + p.bs - 1) / p.bs <= p.max_blocks;
+        }
+        good = __all_sync(0xffffffffu, good && mine);
+        I.good = good;
+        I.seq = it.seq;
+        I.ctx = it.tile0 * kTileKeys;        // every tile of the item is a whole tile of keys
+        I.q_start = it.q_start;
+        I.n_q = it.n_q;
+        I.kvh = it.kv_head;
+        I.split = 0;
+        I.n_splits = 1;
+        I.pos0 = it.tile0 * kTileKeys - 1;   // no key of the item lies past any row
+        I.k_begin = 0;
+        I.n_tiles = good ? it.tile0 : 0;
+        I.rows_valid = good ? it.n_q * p.g : 0;
+        return I;
+    }
     const int seq = good ? it.seq : 0;
     const int ctx_s = good ? p.ctx[seq] : 0;
     const int cu0 = good ? p.cu[seq] : 0;
@@ -551,13 +590,15 @@ __device__ __forceinline__ Item load_item(const Params& p, int idx) {
            (int64_t(ctx_s) + p.bs - 1) / p.bs <= p.max_blocks;
     const int pos0 = ctx_s - cu1 + it.q_start;              // position of the item's first row
     const int p_max = pos0 + it.n_q - 1;
-    const int k_begin = it.split * kSplit;
+    // a RESUME item continues its row's split 0 at key tile tile0
+    const int k_begin = I.kind == PA_ITEM_RESUME ? I.tile0 * kTileKeys : it.split * kSplit;
     good = good && k_begin <= p_max && (p_max < kSplit || p_max / kSplit < p.max_splits);
     // a decode row's splits are separate items (folded by the combine kernel); a prefill
     // tile's item starts at split 0 and covers every split its last row reaches
     const int ns = max(it.n_splits, 1);
-    good = good && (cu1 - cu0 == 1 ? ns == 1 : it.split == 0 && ns == p_max / kSplit + 1);
-    const int k_end = min(k_begin + ns * kSplit, p_max + 1);
+    good = good && (cu1 - cu0 == 1 ? ns == 1 : it.split == 0 && ns == p_max / kSplit + 1) &&
+           (I.kind != PA_ITEM_RESUME || cu1 - cu0 == 1);
+    const int k_end = min(it.split * kSplit + ns * kSplit, p_max + 1);
     I.good = good;
     I.seq = seq;
     I.ctx = ctx_s;
@@ -794,6 +835,67 @@ __device__ __forceinline__ void store_half(const Params& p, const uint32_t* o, i
     }
 }
 
+// End of a GROUP item: each valid row's state (accumulator O, already in registers as for
+// store_half, reference maximum m and sum l) goes to the row's split-0 slot of the workspace,
+// exactly as a split partial would, for the RESUME item that continues the row.
+template <int D>
+__device__ __forceinline__ void save_half(const Params& p, const uint32_t* o, int r0, int rs,
+                                          int q4, int rows_valid, int q_start, int kvh,
+                                          const Rows2& R) {
+#pragma unroll
+    for (int sr = 0; sr < 2; ++sr) {
+        const int row = r0 + rs + 8 * sr;
+        if (row >= rows_valid) continue;
+        const int tok = q_start + row / p.g;
+        const int64_t slot = int64_t(tok) * p.max_splits * p.Hq + kvh * p.g + row % p.g;
+        float* acc = p.ws_acc + slot * D;
+#pragma unroll
+        for (int cc = 0; cc < D / 8; ++cc)
+            *reinterpret_cast<float2*>(acc + 8 * cc + 2 * q4) =
+                make_float2(__uint_as_float(o[4 * cc + 2 * sr]),
+                            __uint_as_float(o[4 * cc + 2 * sr + 1]));
+        if (q4 == 0)
+            *reinterpret_cast<float2*>(p.ws_ml + slot * 2) = make_float2(R.m[sr], R.l[sr]);
+    }
+}
+
+// Start of a RESUME item: the rows' state saved by their GROUP item is restored, (m, l) into R
+// and the accumulator into the item's O buffer (TMEM address tm_o, lane offset included), so
+// that the row continues its split exactly where it would have been without the sharing.
+template <int D>
+__device__ __forceinline__ void restore_half(const Params& p, uint32_t tm_o, int r0, int rs,
+                                             int q4, int rows_valid, int q_start, int kvh,
+                                             int pos0, Rows2& R) {
+    uint32_t o[D / 2];
+#pragma unroll
+    for (int sr = 0; sr < 2; ++sr) {
+        const int row = r0 + rs + 8 * sr;
+        const bool valid = row < rows_valid;
+        R.pos[sr] = valid ? pos0 + row / p.g : -1;
+        R.m[sr] = -INFINITY;
+        R.l[sr] = 0.f;
+        const int64_t slot = valid ? int64_t(q_start + row / p.g) * p.max_splits * p.Hq +
+                                         kvh * p.g + row % p.g
+                                   : 0;
+        if (valid) {
+            const float2 ml = *reinterpret_cast<const float2*>(p.ws_ml + slot * 2);
+            R.m[sr] = ml.x;
+            R.l[sr] = ml.y;
+        }
+        const float* acc = p.ws_acc + slot * D;
+#pragma unroll
+        for (int cc = 0; cc < D / 8; ++cc) {
+            const float2 v = valid ? *reinterpret_cast<const float2*>(acc + 8 * cc + 2 * q4)
+                                   : make_float2(0.f, 0.f);
+            o[4 * cc + 2 * sr] = __float_as_uint(v.x);
+            o[4 * cc + 2 * sr + 1] = __float_as_uint(v.y);
+        }
+    }
+    if constexpr (D == 128) tmem_st_16x256b_x16(tm_o, o);
+    else tmem_st_16x256b_x8(tm_o, o);
+    tmem_wait_st();
+}
+
 // Running result of a prefill tile's splits 0 .. j-1, per row: reference maximum and sum
 // (its accumulator stays in TMEM).
 struct Fold2 {
@@ -920,7 +1022,8 @@ __global__ void __launch_bounds__(kThreadsFor<F8>, 1)
     if (threadIdx.x == 0) {
         for (int b = 0; b < kNumBars; ++b)
             mbar_init(bars + 8 * b,
-                      (b == kPFull || b == kPFull + 1 || b == kOFree || b == kOFree + 1) ? 256
+                      (b == kPFull || b == kPFull + 1 || b == kOFree || b == kOFree + 1 ||
+                       b == kSaved) ? 256
                       : (b >= kItemEmpty && b < kItemEmpty + 4)       ? 2 + 256 + 64 + (F8 ? 128 : 0)
                       : (b >= kKReady && b < kQReady)                 ? 64
                       : b >= kQReady                                  ? 32
@@ -973,7 +1076,7 @@ __global__ void __launch_bounds__(kThreadsFor<F8>, 1)
                 } else {
                     idx = nxt > 0 ? nxt : -1;
                 }
-                I = load_item(p, cur);
+                I = load_item(p, cur, lane);
                 if (I.good) {
                     have = true;
                     break;
@@ -999,6 +1102,8 @@ __global__ void __launch_bounds__(kThreadsFor<F8>, 1)
                     sl->k_begin = I.k_begin;
                     sl->n_tiles = I.n_tiles;
                     sl->rows_valid = I.rows_valid;
+                    sl->kind = I.kind;
+                    sl->tile0 = I.tile0;
                     sl->last = have ? 0 : 1;
                     mbar_arrive(bar(kItemFull + slot));
                 }
@@ -1145,7 +1250,10 @@ __global__ void __launch_bounds__(kThreadsFor<F8>, 1)
                 // O += P V for the oldest tile whose P is ready (P published implies that V
                 // has landed; the first tile of a split starts its O buffer once the epilogue
                 // has released it)
-                const bool cont = (cv.jt & (kSplitTiles - 1)) != 0;
+                // (a RESUME item's first tile continues its split: it accumulates onto the
+                // restored O)
+                const int jt0 = cv.I.kind == PA_ITEM_RESUME ? cv.I.tile0 : 0;
+                const bool cont = ((jt0 + cv.jt) & (kSplitTiles - 1)) != 0;
                 if (cv.have && cv.tc < cs.tc &&
                     mbar_test_wait(bar(kPFull + (cv.tc & 1)), (cv.tc >> 1) & 1) &&
                     (cont || cv.sg < 2 ||
@@ -1361,6 +1469,7 @@ __global__ void __launch_bounds__(kThreadsFor<F8>, 1)
         const volatile ItemSlot* ring =
             reinterpret_cast<const volatile ItemSlot*>(smem + L::kBar + kRingOff);
         int tc = 0, ic = 0, sg = 0;       // tiles, items and splits seen
+        int ng = 0;                       // GROUP items whose state has been saved
         bool ok = true;
         // the wait-timeout test: a wait that nothing completes runs out, and every role leaves
         // through the same path as after any other wait that ran out
@@ -1374,12 +1483,26 @@ __global__ void __launch_bounds__(kThreadsFor<F8>, 1)
             const bool on = r0 < I.rows_valid;    // warp-uniform: the warp holds a valid row
             Rows2 R;
             Fold2 F;
+            // a RESUME item starts inside split 0, at tile tile0
+            const int jt0 = I.kind == PA_ITEM_RESUME ? I.tile0 : 0;
             for (int jt = 0; jt < I.n_tiles; ++jt, ++tc) {
                 // every split starts afresh, exactly as an item of that split alone would
-                const int jin = jt & (kSplitTiles - 1);
+                const int jin = (jt0 + jt) & (kSplitTiles - 1);
                 if (jin == 0) rows_init(R, r0, rs, I.rows_valid, I.pos0, p.g);
                 const int ob = sg & 1;
                 const uint32_t tm_o = tmem + kTmemO + ob * 128 + lanes;
+                if (jt == 0 && jt0 > 0) {
+                    // the state its GROUP item saved (that item is earlier on this CTA's list;
+                    // its O buffer was released by these warps' own epilogue two splits ago)
+                    if (ng == 0) {
+                        if (tid == 0 && p.err) atomicOr(p.err, PA_DEVERR_META);
+                    } else if (!(ok = wait_bounded(bar(kSaved), (ng - 1) & 1, abort_word))) {
+                        break;
+                    }
+                    if (on)
+                        restore_half<D>(p, tm_o, r0, rs, q4, I.rows_valid, I.q_start, I.kvh,
+                                        I.pos0, R);
+                }
                 if (!(ok = wait_bounded(bar(kSFull + (tc & (SK - 1))), (tc >> kLog2SK) & 1,
                                         abort_word)))
                     break;
@@ -1414,7 +1537,7 @@ __global__ void __launch_bounds__(kThreadsFor<F8>, 1)
                 mbar_arrive(bar(kPFull + (tc & 1)));            // all 256 softmax threads arrive
                 if (jin != kSplitTiles - 1 && jt != I.n_tiles - 1) continue;
                 // ------------------------------------------------------ end of a split
-                const int js = jt / kSplitTiles;       // split of the item (0 for a decode's)
+                const int js = (jt0 + jt) / kSplitTiles;   // split of the item (0 for a decode's)
                 ++sg;
                 if (I.n_splits > 1 && js == 0) {
                     // split 0's O stays where it is as the running result: nothing to wait for
@@ -1447,7 +1570,18 @@ __global__ void __launch_bounds__(kThreadsFor<F8>, 1)
                     tmem_wait_ld();
                     tc_fence_before();
                     mbar_arrive(bar(kOFree + ob));       // O is in registers: its buffer is free
-                    store_half<D>(p, o, r0, rs, q4, I.rows_valid, I.q_start, I.kvh, I.split, R);
+                    if (I.kind == PA_ITEM_GROUP)
+                        save_half<D>(p, o, r0, rs, q4, I.rows_valid, I.q_start, I.kvh, R);
+                    else
+                        store_half<D>(p, o, r0, rs, q4, I.rows_valid, I.q_start, I.kvh, I.split,
+                                      R);
+                }
+                if (I.kind == PA_ITEM_GROUP) {
+                    // the saved state is published to the RESUME items (other threads of these
+                    // warps restore it)
+                    __threadfence_block();
+                    mbar_arrive(bar(kSaved));
+                    ++ng;
                 }
             }
             if (!ok) break;

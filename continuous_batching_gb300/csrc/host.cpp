@@ -73,7 +73,7 @@ struct pa_allocator {
 
 extern "C" {
 
-int32_t pa_abi_version(void) { return 2; }
+int32_t pa_abi_version(void) { return 3; }
 
 const char* pa_status_string(int32_t st) {
     switch (st) {
@@ -411,76 +411,87 @@ int64_t pa_plan_max_items(const pa_shape* shape, int32_t B, int32_t T, int32_t m
     return tiles * shape->num_kv_heads * std::max<int64_t>(splits, 1);
 }
 
-int32_t pa_plan_step(const pa_shape* shape, int32_t B, const int32_t* cu, const int32_t* ctx,
-                     pa_work_item* items, int32_t max_items, int32_t* n_items) {
-    int32_t st = check_shape(shape);
-    if (st) return st;
-    st = check_step_meta(B, cu, ctx);
-    if (st) return st;
-    if (!n_items || max_items < 0 || (max_items > 0 && !items)) return PA_ERR_INVALID;
-    const int32_t g = shape->num_q_heads / shape->num_kv_heads;
-    const int32_t rpt = PA_ROWS / g;
-    std::vector<pa_work_item> out;
-    out.reserve(size_t(std::min<int64_t>(max_items, 1 << 16)));
-    for (int32_t s = 0; s < B; ++s) {
-        const int32_t n = cu[s + 1] - cu[s];
-        for (int32_t t0 = 0; t0 < n; t0 += rpt) {
-            const int32_t nt = std::min(rpt, n - t0);
-            const int64_t p_max = int64_t(ctx[s]) - n + t0 + nt - 1;
-            const int32_t nsplit = int32_t(p_max / PA_SPLIT_TOKENS + 1);
-            // a decode row's splits go to separate items; a prefill tile keeps all of its
-            // splits in one item and folds them in the kernel
-            const int32_t per_item = n > 1 ? nsplit : 1;
-            for (int32_t h = 0; h < shape->num_kv_heads; ++h)
-                for (int32_t sp = 0; sp < nsplit; sp += per_item) {
-                    if (int64_t(out.size()) >= max_items) return PA_ERR_INVALID;
-                    const int64_t k0 = int64_t(sp) * PA_SPLIT_TOKENS;
-                    const int64_t k1 =
-                        std::min<int64_t>(k0 + int64_t(per_item) * PA_SPLIT_TOKENS, p_max + 1);
-                    pa_work_item it{};
-                    it.seq = s;
-                    it.q_start = cu[s] + t0;
-                    it.n_q = nt;
-                    it.kv_head = h;
-                    it.split = sp;
-                    it.n_tiles = int32_t((k1 - k0 + PA_TILE_KEYS - 1) / PA_TILE_KEYS);
-                    it.n_splits = per_item;
-                    out.push_back(it);
-                }
+namespace {
+
+// A unit of the deal: items [first, first + count) of the generated items, which go to one
+// list, consecutively, in this order (one item, or a group's GROUP item and its RESUMEs).
+struct Unit {
+    int32_t first, count;
+    int64_t cost;       // sum over its items of n_tiles + 1
+};
+
+// The PLAIN items of query-row tile [t0, t0 + nt) of sequence s, KV heads all, splits from
+// sp_first on: a decode row's splits go to separate items; a prefill tile keeps all of its
+// splits in one item and folds them in the kernel.
+void plain_items(const pa_shape* shape, int32_t s, int32_t q0, int32_t n, int32_t t0, int32_t nt,
+                 const int32_t* ctx, int32_t sp_first, std::vector<pa_work_item>& out,
+                 std::vector<Unit>& units) {
+    const int64_t p_max = int64_t(ctx[s]) - n + t0 + nt - 1;
+    const int32_t nsplit = int32_t(p_max / PA_SPLIT_TOKENS + 1);
+    const int32_t per_item = n > 1 ? nsplit : 1;
+    for (int32_t h = 0; h < shape->num_kv_heads; ++h)
+        for (int32_t sp = sp_first; sp < nsplit; sp += per_item) {
+            const int64_t k0 = int64_t(sp) * PA_SPLIT_TOKENS;
+            const int64_t k1 = std::min<int64_t>(k0 + int64_t(per_item) * PA_SPLIT_TOKENS, p_max + 1);
+            pa_work_item it{};
+            it.seq = s;
+            it.q_start = q0 + t0;
+            it.n_q = nt;
+            it.kv_head = h;
+            it.split = sp;
+            it.n_tiles = int32_t((k1 - k0 + PA_TILE_KEYS - 1) / PA_TILE_KEYS);
+            it.n_splits = per_item;
+            it.kind = PA_ITEM_PLAIN;
+            units.push_back({int32_t(out.size()), 1, int64_t(it.n_tiles) + 1});
+            out.push_back(it);
         }
-    }
+}
+
+// Deals the units longest processing time first: each unit, by decreasing cost (ties in
+// generation order), joins the list (one per CTA) with the least cost so far, the lower list on
+// a tie; its items take consecutive places in that list. The output holds the first item of
+// every list (list c at index c), then the second item of every list that has one, in list
+// order, and so on, with `next` linking each list. The kernel runs min(output items,
+// PA_PLAN_CTAS) CTAs, CTA c from index c: when units make fewer lists G than that, padding
+// items (n_q == 0) take indices G .. PA_PLAN_CTAS - 1, so that the CTAs past the lists find
+// no work.
+int32_t deal(const std::vector<pa_work_item>& out, const std::vector<Unit>& units,
+             pa_work_item* items, int32_t max_items, int32_t* n_items) {
     const int32_t n = int32_t(out.size());
-    // by decreasing n_tiles, ties in generation order (a stable counting sort)
-    int32_t max_tiles = 0;
-    for (const pa_work_item& it : out) max_tiles = std::max(max_tiles, it.n_tiles);
-    std::vector<int32_t> by_cost(static_cast<size_t>(n));
-    if (max_tiles <= 4 * n + 4096) {
-        std::vector<int32_t> first(size_t(max_tiles) + 2, 0);
-        for (const pa_work_item& it : out) ++first[size_t(max_tiles - it.n_tiles) + 1];
+    const int32_t nu = int32_t(units.size());
+    const int32_t G = std::min<int32_t>(nu, PA_PLAN_CTAS);
+    const int32_t pad = G < std::min<int32_t>(n, PA_PLAN_CTAS) ? PA_PLAN_CTAS - G : 0;
+    if (int64_t(n) + pad > max_items) return PA_ERR_INVALID;
+    // by decreasing cost, ties in generation order (a stable counting sort when it is small)
+    int64_t max_cost = 0;
+    for (const Unit& u : units) max_cost = std::max(max_cost, u.cost);
+    std::vector<int32_t> by_cost(static_cast<size_t>(nu));
+    if (max_cost <= 4 * int64_t(nu) + 4096) {
+        std::vector<int32_t> first(size_t(max_cost) + 2, 0);
+        for (const Unit& u : units) ++first[size_t(max_cost - u.cost) + 1];
         for (size_t k = 1; k < first.size(); ++k) first[k] += first[k - 1];
-        for (int32_t i = 0; i < n; ++i)
-            by_cost[size_t(first[size_t(max_tiles - out[size_t(i)].n_tiles)]++)] = i;
+        for (int32_t i = 0; i < nu; ++i)
+            by_cost[size_t(first[size_t(max_cost - units[size_t(i)].cost)]++)] = i;
     } else {
-        for (int32_t i = 0; i < n; ++i) by_cost[size_t(i)] = i;
+        for (int32_t i = 0; i < nu; ++i) by_cost[size_t(i)] = i;
         std::stable_sort(by_cost.begin(), by_cost.end(), [&](int32_t x, int32_t y) {
-            return out[size_t(x)].n_tiles > out[size_t(y)].n_tiles;
+            return units[size_t(x)].cost > units[size_t(y)].cost;
         });
     }
-    // Longest processing time first: each item, longest first, joins the list (one per CTA)
-    // with the least cost so far, the lower list on a tie. A binary min-heap of keys
-    // cost * 256 + list (G <= 256), so that equal costs order by list.
+    // a binary min-heap of keys cost * 256 + list (G <= 256), so that equal costs order by list
     static_assert(PA_PLAN_CTAS <= 256, "list index must fit the heap key's low byte");
-    const int32_t G = std::min<int32_t>(n, PA_PLAN_CTAS);
     std::vector<uint64_t> heap(static_cast<size_t>(G));
     for (int32_t c = 0; c < G; ++c) heap[size_t(c)] = uint64_t(c);   // ascending: a heap
     std::vector<int32_t> owner(static_cast<size_t>(n)), rank(static_cast<size_t>(n));
     std::vector<int32_t> len(static_cast<size_t>(G), 0);
-    for (int32_t j = 0; j < n; ++j) {
-        const int32_t i = by_cost[size_t(j)];
+    for (int32_t j = 0; j < nu && G > 0; ++j) {
+        const Unit& u = units[size_t(by_cost[size_t(j)])];
         const int32_t c = int32_t(heap[0] & 255u);
-        owner[size_t(i)] = c;
-        rank[size_t(i)] = len[size_t(c)]++;
-        uint64_t key = heap[0] + (uint64_t(out[size_t(i)].n_tiles) + 1) * 256u;
+        for (int32_t k = 0; k < u.count; ++k) {
+            owner[size_t(u.first + k)] = c;
+            rank[size_t(u.first + k)] = len[size_t(c)]++;
+        }
+        uint64_t key = heap[0] + uint64_t(u.cost) * 256u;
         size_t k = 0;                                                // sift the root down
         for (;;) {
             size_t m = 2 * k + 1;
@@ -492,8 +503,8 @@ int32_t pa_plan_step(const pa_shape* shape, int32_t B, const int32_t* cu, const 
         }
         heap[k] = key;
     }
-    // Stored position by position: the k-th item of every list that has one, lists in order,
-    // for k = 0, 1, ...; so list c starts at index c and a successor has a higher index.
+    // stored position by position: so list c starts at index c and a successor has a higher
+    // index
     std::vector<int32_t> off(size_t(G) + 1, 0);
     int32_t longest = 0;
     for (int32_t c = 0; c < G; ++c) {
@@ -504,17 +515,138 @@ int32_t pa_plan_step(const pa_shape* shape, int32_t B, const int32_t* cu, const 
     for (int32_t i = 0; i < n; ++i)
         member[size_t(off[size_t(owner[size_t(i)])] + rank[size_t(i)])] = i;
     int32_t pos = 0;
-    for (int32_t k = 0; k < longest; ++k)
+    for (int32_t k = 0; k < longest; ++k) {
         for (int32_t c = 0; c < G; ++c)
             if (k < len[size_t(c)]) at[size_t(member[size_t(off[size_t(c)] + k)])] = pos++;
+        if (k == 0) {
+            for (int32_t j = 0; j < pad; ++j) items[pos + j] = pa_work_item{};   // n_q == 0
+            pos += pad;
+        }
+    }
     for (int32_t i = 0; i < n; ++i) {
         const int32_t c = owner[size_t(i)], k = rank[size_t(i)];
         pa_work_item it = out[size_t(i)];
         it.next = k + 1 < len[size_t(c)] ? at[size_t(member[size_t(off[size_t(c)] + k + 1)])] : -1;
         items[at[size_t(i)]] = it;
     }
-    *n_items = n;
+    *n_items = n + pad;
     return PA_OK;
+}
+
+int32_t plan(const pa_shape* shape, int32_t B, const int32_t* cu, const int32_t* ctx,
+             const int32_t* table, int32_t max_blocks, pa_work_item* items, int32_t max_items,
+             int32_t* n_items) {
+    int32_t st = check_shape(shape);
+    if (st) return st;
+    st = check_step_meta(B, cu, ctx);
+    if (st) return st;
+    if (!n_items || max_items < 0 || (max_items > 0 && !items)) return PA_ERR_INVALID;
+    const int32_t g = shape->num_q_heads / shape->num_kv_heads;
+    const int32_t rpt = PA_ROWS / g;
+    const int32_t bs = shape->block_size;
+    if (table) {
+        if (max_blocks < 0) return PA_ERR_INVALID;
+        for (int32_t s = 0; s < B; ++s)
+            if ((int64_t(ctx[s]) + bs - 1) / bs > max_blocks) return PA_ERR_BOUNDS;
+    }
+    std::vector<pa_work_item> out;
+    std::vector<Unit> units;
+    out.reserve(size_t(std::min<int64_t>(max_items, 1 << 16)));
+    const auto decode = [&](int32_t s) { return cu[s + 1] - cu[s] == 1; };
+    // the leading key tiles of split 0 that a row at ctx has keys past (the rest of its split
+    // 0 is left for a RESUME item)
+    const auto tile_cap = [&](int32_t s) {
+        return std::min<int32_t>(PA_SPLIT_TOKENS / PA_TILE_KEYS - 1, (ctx[s] - 1) / PA_TILE_KEYS);
+    };
+    const int32_t blocks_per_tile = PA_TILE_KEYS / bs;
+    const auto common = [&](int32_t a, int32_t b, int32_t bound) {
+        const int32_t* ra = table + int64_t(a) * max_blocks;
+        const int32_t* rb = table + int64_t(b) * max_blocks;
+        int32_t t = 0;
+        while (t < bound &&
+               std::memcmp(ra + int64_t(t) * blocks_per_tile, rb + int64_t(t) * blocks_per_tile,
+                           size_t(blocks_per_tile) * 4) == 0)
+            ++t;
+        return t;
+    };
+    for (int32_t s = 0; s < B;) {
+        // a run of decode rows that share at least two leading tiles with its first row
+        int32_t e = s + 1, shared = 0;
+        if (table && decode(s)) {
+            shared = tile_cap(s);
+            while (e < B && decode(e) && (e - s + 1) * g <= PA_ROWS) {
+                const int32_t c = common(s, e, std::min(shared, tile_cap(e)));
+                if (c < 2) break;
+                shared = c;
+                ++e;
+            }
+        }
+        if (e - s < 2 || shared < 2) {
+            const int32_t n = cu[s + 1] - cu[s];
+            for (int32_t t0 = 0; t0 < n; t0 += rpt)
+                plain_items(shape, s, cu[s], n, t0, std::min(rpt, n - t0), ctx, 0, out, units);
+            ++s;
+            continue;
+        }
+        for (int32_t h = 0; h < shape->num_kv_heads; ++h) {
+            Unit u{int32_t(out.size()), 0, 0};
+            pa_work_item it{};
+            it.seq = s;
+            it.q_start = cu[s];
+            it.n_q = e - s;
+            it.kv_head = h;
+            it.split = 0;
+            it.n_tiles = shared;
+            it.n_splits = 1;
+            it.kind = PA_ITEM_GROUP;
+            it.tile0 = shared;
+            out.push_back(it);
+            u.cost += int64_t(it.n_tiles) + 1;
+            for (int32_t m = s; m < e; ++m) {
+                pa_work_item r{};
+                r.seq = m;
+                r.q_start = cu[m];
+                r.n_q = 1;
+                r.kv_head = h;
+                r.split = 0;
+                r.n_tiles = (std::min(ctx[m], PA_SPLIT_TOKENS) + PA_TILE_KEYS - 1) / PA_TILE_KEYS -
+                            shared;
+                r.n_splits = 1;
+                r.kind = PA_ITEM_RESUME;
+                r.tile0 = shared;
+                out.push_back(r);
+                u.cost += int64_t(r.n_tiles) + 1;
+            }
+            u.count = int32_t(out.size()) - u.first;
+            units.push_back(u);
+        }
+        for (int32_t m = s; m < e; ++m) plain_items(shape, m, cu[m], 1, 0, 1, ctx, 1, out, units);
+        s = e;
+    }
+    if (int64_t(out.size()) > max_items) return PA_ERR_INVALID;
+    return deal(out, units, items, max_items, n_items);
+}
+
+}  // namespace
+
+int32_t pa_plan_step(const pa_shape* shape, int32_t B, const int32_t* cu, const int32_t* ctx,
+                     pa_work_item* items, int32_t max_items, int32_t* n_items) {
+    return plan(shape, B, cu, ctx, nullptr, 0, items, max_items, n_items);
+}
+
+int64_t pa_plan_max_items_shared(const pa_shape* shape, int32_t B, int32_t T, int32_t max_ctx) {
+    const int64_t n = pa_plan_max_items(shape, B, T, max_ctx);
+    if (n <= 0) return n;
+    // at most one GROUP item per KV head for every two sequences, and the padding that keeps
+    // the CTAs past a plan's lists idle
+    return n + int64_t(B / 2) * shape->num_kv_heads + PA_PLAN_CTAS;
+}
+
+int32_t pa_plan_step_shared(const pa_shape* shape, int32_t B, const int32_t* cu,
+                            const int32_t* ctx, const int32_t* block_table, int32_t max_blocks,
+                            pa_work_item* items, int32_t max_items, int32_t* n_items) {
+    if (!block_table && B > 0) return PA_ERR_INVALID;
+    return plan(shape, B, cu, ctx, block_table, max_blocks, items, max_items, n_items);
 }
 
 size_t pa_workspace_bytes(const pa_shape* shape, int32_t T, int32_t max_ctx) {

@@ -9,7 +9,7 @@
 // read-back, so that one step's planning and copies overlap the kernels of the step before
 // it; the kernels themselves run in submission order on one stream, since every step writes
 // and reads the same pools. What is run per step is exactly paged_kv_write (or its fp8 form)
-// followed by paged_attention_step over a plan from pa_plan_step ("P3: native paged-KV
+// followed by paged_attention_step over a plan from pa_plan_step_shared ("P3: native paged-KV
 // continuous-batching sampler", Design / engine.py: one flat ragged step per engine step).
 #include <cmath>
 #include <cstdint>
@@ -105,8 +105,9 @@ extern "C" int32_t pa_pipeline_create(const pa_shape* shape, int32_t B, int32_t 
     if (fp8 && (!(k_scale > 0.f) || !(v_scale > 0.f) || !(k_scale < INFINITY) ||
                 !(v_scale < INFINITY)))
         return PA_ERR_INVALID;
-    const int64_t cap = pa_plan_max_items(shape, B, T, max_ctx);
-    if (cap <= 0 || cap > INT32_MAX / 8) return PA_ERR_INVALID;
+    const int64_t cap = pa_plan_max_items_shared(shape, B, T, max_ctx);
+    constexpr int64_t kItemInts = sizeof(pa_work_item) / 4;
+    if (cap <= 0 || cap > INT32_MAX / kItemInts) return PA_ERR_INVALID;
     auto* p = new pa_pipeline();
     p->shape = *shape;
     p->B = B;
@@ -120,7 +121,7 @@ extern "C" int32_t pa_pipeline_create(const pa_shape* shape, int32_t B, int32_t 
     p->k_pool = k_pool;
     p->v_pool = v_pool;
     p->o_items = 0;
-    p->o_cu = size_t(cap) * 8;
+    p->o_cu = size_t(cap) * size_t(kItemInts);
     p->o_ctx = p->o_cu + size_t(B) + 1;
     p->o_table = p->o_ctx + size_t(B);
     p->o_slots = p->o_table + size_t(B) * size_t(max_blocks);
@@ -233,7 +234,9 @@ extern "C" int32_t pa_pipeline_submit(pa_pipeline* p, const int32_t* cu_seqlens_
     std::memcpy(h + p->o_ctx, ctx_lens, size_t(p->B) * 4);
     auto* items = reinterpret_cast<pa_work_item*>(h + p->o_items);
     int32_t n = 0;
-    if ((st = pa_plan_step(&p->shape, p->B, cu_seqlens_q, ctx_lens, items, p->cap, &n))) return st;
+    if ((st = pa_plan_step_shared(&p->shape, p->B, cu_seqlens_q, ctx_lens, tab, p->max_blocks, items,
+                                  p->cap, &n)))
+        return st;
     if (n < s.n_planned) std::memset(items + n, 0, size_t(s.n_planned - n) * sizeof(pa_work_item));
     s.n_planned = n;
     // uploads, kernels, read-back

@@ -106,7 +106,23 @@ typedef struct pa_work_item {
     int32_t next;       /* index of the next item of this item's list; <= 0 ends the list. A
                          * successor has a higher index (an item that breaks this, or points
                          * past n_items, ends its list and raises PA_DEVERR_META) */
+    int32_t kind;       /* PA_ITEM_PLAIN, PA_ITEM_GROUP or PA_ITEM_RESUME (see below) */
+    int32_t tile0;      /* GROUP / RESUME: the shared key tiles [0, tile0) of split 0 */
 } pa_work_item;
+
+/* Item kinds. A PLAIN item is as described above. Prefix sharing (pa_plan_step_shared) adds
+ * two: a GROUP item holds the decode rows of n_q consecutive sequences seq .. seq + n_q - 1
+ * (one query row each, at tokens q_start .. q_start + n_q - 1) whose block tables agree on the
+ * blocks of key tiles [0, tile0); it reads those shared tiles once, through seq's table, for
+ * all of its rows, and saves each row's softmax state (accumulator, maximum, sum) to the row's
+ * split-0 workspace slot. A RESUME item, later on the same list, continues one of those rows
+ * over its own keys [tile0 * PA_TILE_KEYS, end of split 0) from the saved state. Every row runs
+ * the same instruction sequence as without sharing (a tensor-core output element depends only
+ * on its own row of A and column of B, and the state carried across is exact), so the output
+ * bits are those of PLAIN items. */
+#define PA_ITEM_PLAIN 0
+#define PA_ITEM_GROUP 1
+#define PA_ITEM_RESUME 2
 
 /* ---------------------------------------------------------------- library ---------- */
 
@@ -279,6 +295,24 @@ int64_t pa_plan_max_items(const pa_shape* shape, int32_t B, int32_t T, int32_t m
 int32_t pa_plan_step(const pa_shape* shape, int32_t B, const int32_t* cu_seqlens_q,
                      const int32_t* ctx_lens, pa_work_item* items, int32_t max_items,
                      int32_t* n_items);
+
+/* pa_plan_step with prefix sharing (same output for steps without it): runs of consecutive
+ * decode sequences (one query row each, at most 128 / group of them) whose block tables
+ * [B, max_blocks] agree on the blocks of at least two leading key tiles become GROUP and
+ * RESUME items (see pa_work_item) for every KV head, their splits past 0 PLAIN items. A
+ * group's items (GROUP, then its RESUMEs) are dealt to one list as a unit; the balance rule is
+ * otherwise that of pa_plan_step. Since a group's items share one list, such a plan can have
+ * fewer lists than min(items, PA_PLAN_CTAS); its padding items (n_q == 0) then take indices
+ * lists .. PA_PLAN_CTAS - 1, before the lists' second items, and *n_items counts them. A plan
+ * with such items needs the workspace even when no
+ * context exceeds PA_SPLIT_TOKENS (pa_workspace_bytes(shape, T, max_ctx) bytes; without one
+ * its GROUP and RESUME items are flagged PA_DEVERR_META and skipped). At most
+ * pa_plan_max_items_shared items. */
+int64_t pa_plan_max_items_shared(const pa_shape* shape, int32_t B, int32_t T, int32_t max_ctx);
+int32_t pa_plan_step_shared(const pa_shape* shape, int32_t B, const int32_t* cu_seqlens_q,
+                            const int32_t* ctx_lens, const int32_t* block_table,
+                            int32_t max_blocks, pa_work_item* items, int32_t max_items,
+                            int32_t* n_items);
 
 /* Bytes of fp32 workspace paged_attention_step needs for T query rows and contexts up to
  * max_ctx: split partials (acc[D], m, l) for every (row, split, q head). Sized by limits, not

@@ -38,7 +38,7 @@ def test_every_declared_symbol_is_exported(built_library):
 
 
 def test_abi_version_and_status_strings():
-    assert bd.pa_abi_version() == 2
+    assert bd.pa_abi_version() == 3
     assert bd.status_string(bd.PA_ERR_OOM) == "PA_ERR_OOM"
     assert bd.status_string(999) == "PA_ERR_UNKNOWN"
 
@@ -231,7 +231,7 @@ def test_limits_runner_lays_out_padded_metadata_without_gpu():
         want[:, :tab.shape[1]] = tab
         assert np.array_equal(r.table.numpy(), want)
         assert np.array_equal(r.slots.numpy(), bd.pa_compute_slots(shape, tab, cu, ctx))
-        assert r.meta_bytes == 4 * (r.n_items_cap * 8 + 4 + 3 + 18 + 5)
+        assert r.meta_bytes == 4 * (r.n_items_cap * bd.ITEM_INTS + 4 + 3 + 18 + 5)
     with pytest.raises(ValueError):
         r.prepare(np.array([0, 1, 2], np.int32), np.array([5, 5], np.int32), np.zeros((2, 1), np.int32))
 
@@ -252,8 +252,91 @@ def test_limits_runner_clears_items_of_a_longer_previous_plan_without_gpu():
         items = bd.pa_plan_step(shape, cu, ctx)
         dev = r.items.numpy().view(bd.WORK_ITEM_DTYPE)
         assert np.array_equal(dev[:len(items)], items)
-        assert not np.any(dev.view(np.int32).reshape(len(dev), 8)[len(items):])
+        assert not np.any(dev.view(np.int32).reshape(len(dev), bd.ITEM_INTS)[len(items):])
         assert np.array_equal(r.slots.numpy(), bd.pa_compute_slots(shape, table, cu, ctx))
         check_lists(dev, len(dev))
         counts.append(len(items))
     assert counts[0] > counts[1] < counts[2]
+
+
+# ------------------------------------------------------------ prefix sharing in the plan
+
+def _tiles_covered(items, st):
+    """(token, kv head) -> list of key tiles the items give it (GROUP items: tiles [0, tile0)
+    of split 0 for each member row; RESUME: [tile0, end of split 0); PLAIN: its splits)."""
+    seq_of, pos_of = pa.row_positions(st.cu_seqlens_q, st.ctx_lens)
+    cov = {}
+    T_SPLIT = bd.PA_SPLIT_TOKENS // bd.PA_TILE_KEYS
+    for it in items:
+        rows = range(it["q_start"], it["q_start"] + it["n_q"])
+        for t in rows:
+            last_tile = int(pos_of[t]) // bd.PA_TILE_KEYS
+            if it["kind"] == bd.PA_ITEM_GROUP:
+                tiles = range(0, int(it["tile0"]))
+            elif it["kind"] == bd.PA_ITEM_RESUME:
+                tiles = range(int(it["tile0"]), min(T_SPLIT - 1, last_tile) + 1)
+            else:
+                lo = int(it["split"]) * T_SPLIT
+                hi = (int(it["split"]) + max(int(it["n_splits"]), 1)) * T_SPLIT
+                tiles = range(lo, min(hi - 1, last_tile) + 1)
+            cov.setdefault((t, int(it["kv_head"])), []).extend(tiles)
+    return cov, pos_of
+
+
+@pytest.mark.parametrize("name", wl.CONFIG_NAMES)
+def test_shared_plan_covers_every_key_tile_once(name):
+    st = wl.make_config(name, with_pool=False)
+    shape = bd.Shape.make(st.Hq, st.Hkv, st.D, st.block_size, st.num_blocks)
+    items = bd.pa_plan_step_shared(shape, st.cu_seqlens_q, st.ctx_lens, st.block_table)
+    cov, pos_of = _tiles_covered(items, st)
+    for t in range(st.T):
+        for h in range(st.Hkv):
+            want = list(range(int(pos_of[t]) // bd.PA_TILE_KEYS + 1))
+            assert sorted(cov[(t, h)]) == want, (t, h)
+    groups = items[items["kind"] == bd.PA_ITEM_GROUP]
+    if name == "prefix":
+        # 16 prompts x 8 samples sharing 64 blocks of 16 tokens: one group of 8 rows per
+        # prompt and KV head over the 8 shared tiles
+        assert len(groups) == 16 * st.Hkv
+        assert np.all(groups["n_q"] == 8) and np.all(groups["tile0"] == 8)
+        assert np.sum(items["kind"] == bd.PA_ITEM_RESUME) == 128 * st.Hkv
+    else:
+        # no block is shared: the plan is pa_plan_step's
+        assert len(groups) == 0
+        assert np.array_equal(items, bd.pa_plan_step(shape, st.cu_seqlens_q, st.ctx_lens))
+    # every real item on exactly one list; a group's RESUME items follow it on its list
+    lists = walk(items, len(items))
+    real = np.flatnonzero(items["n_q"] != 0).tolist()
+    assert sorted(i for L in lists for i in L) == real
+    where = {i: (c, k) for c, L in enumerate(lists) for k, i in enumerate(L)}
+    for gi in np.flatnonzero(items["kind"] == bd.PA_ITEM_GROUP):
+        g_it = items[gi]
+        c, k = where[int(gi)]
+        members = range(int(g_it["seq"]), int(g_it["seq"]) + int(g_it["n_q"]))
+        nxt = lists[c][k + 1:k + 1 + len(members)]
+        assert [int(items[j]["seq"]) for j in nxt] == list(members)
+        assert all(items[j]["kind"] == bd.PA_ITEM_RESUME and items[j]["kv_head"] == g_it["kv_head"]
+                   and items[j]["tile0"] == g_it["tile0"] for j in nxt)
+
+
+def test_shared_plan_needs_two_whole_shared_tiles():
+    """Decode rows whose tables agree on one 128-key tile only, or on blocks that do not fill a
+    tile, stay PLAIN; rows that agree on two tiles form a group whose tile0 is the tiles all
+    of them share."""
+    shape = bd.Shape.make(32, 8, 128, 16, 4096)
+    ctx = np.array([900, 900, 900], np.int32)
+    cu = np.arange(4, dtype=np.int32)
+    table = np.arange(3 * 64, dtype=np.int32).reshape(3, 64)
+    table[1, :8] = table[0, :8]                                   # one tile in common
+    items = bd.pa_plan_step_shared(shape, cu, ctx, table)
+    assert np.all(items["kind"] == bd.PA_ITEM_PLAIN)
+    table[1, :20] = table[0, :20]                                 # 2.5 tiles in common
+    table[2, :40] = table[0, :40]                                 # 5 tiles
+    items = bd.pa_plan_step_shared(shape, cu, ctx, table)
+    groups = items[items["kind"] == bd.PA_ITEM_GROUP]
+    assert len(groups) == 8 and np.all(groups["n_q"] == 3) and np.all(groups["tile0"] == 2)
+    # 8 lists (one group per KV head) for 32 items: CTAs 8 .. 151 start at padding
+    lists = walk(items, len(items))
+    assert len(items) == 32 + bd.PA_PLAN_CTAS - 8
+    assert all(L for L in lists[:8]) and not any(lists[8:])
+    assert sorted(i for L in lists for i in L) == np.flatnonzero(items["n_q"] != 0).tolist()

@@ -318,7 +318,7 @@ def test_a_wait_that_runs_out_sets_the_timeout_bit_and_the_device_stays_usable()
         rc = lib.paged_attention_step_wait_test(
             q.data_ptr(), kp.data_ptr(), vp.data_ptr(), runner.table.data_ptr(),
             int(runner.table.shape[1]), runner.cu.data_ptr(), runner.ctx.data_ptr(), st.B, st.T,
-            runner.max_ctx, runner.items.data_ptr(), int(runner.items.numel() // 8),
+            runner.max_ctx, runner.items.data_ptr(), int(runner.items.numel() // bd.ITEM_INTS),
             ws.data_ptr() if ws is not None and ws.numel() else None,
             0 if ws is None else ws.numel() * 4, out.data_ptr(), C.byref(shape),
             runner.err.data_ptr(), 2_000_000, stream)
@@ -346,6 +346,6 @@ def test_wait_test_rejects_limits_outside_its_range():
         rc = lib.paged_attention_step_wait_test(
             q.data_ptr(), q.data_ptr(), q.data_ptr(), runner.table.data_ptr(),
             int(runner.table.shape[1]), runner.cu.data_ptr(), runner.ctx.data_ptr(), st.B, st.T,
-            runner.max_ctx, runner.items.data_ptr(), int(runner.items.numel() // 8), None, 0,
+            runner.max_ctx, runner.items.data_ptr(), int(runner.items.numel() // bd.ITEM_INTS), None, 0,
             out.data_ptr(), C.byref(shape), None, never, None)
         assert rc == bd.PA_ERR_INVALID

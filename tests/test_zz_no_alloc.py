@@ -53,7 +53,7 @@ def _call_static(lib, st, shape, runner, kp, vp, q, out):
     return lib.paged_attention_step_static_scratch(
         q.data_ptr(), kp.data_ptr(), vp.data_ptr(), runner.table.data_ptr(),
         int(runner.table.shape[1]), runner.cu.data_ptr(), runner.ctx.data_ptr(), st.B, st.T,
-        runner.max_ctx, runner.items.data_ptr(), int(runner.items.numel() // 8),
+        runner.max_ctx, runner.items.data_ptr(), int(runner.items.numel() // bd.ITEM_INTS),
         out.data_ptr(), C.byref(shape), runner.err.data_ptr(), stream)
 
 
