@@ -349,3 +349,31 @@ def test_wait_test_rejects_limits_outside_its_range():
             runner.max_ctx, runner.items.data_ptr(), int(runner.items.numel() // bd.ITEM_INTS), None, 0,
             out.data_ptr(), C.byref(shape), None, never, None)
         assert rc == bd.PA_ERR_INVALID
+
+
+def test_no_wait_runs_out_silently():
+    """Every wait of a step answers long before its one-second limit. The drains at a CTA's end
+    give up at that limit without an error bit (the copies and MMAs they wait for are the CTA's
+    own), so a barrier that can never complete there (a wrong arrival count, say) would leave
+    the outputs right and every launch a second long: timed here, it cannot hide."""
+    cases = [wl.make_config("tiny"),
+             wl.make_step(32, 8, 128, 16, [3000, 40, 9000, 5000], [1, 1, 512, 1], seed=97),
+             wl.make_step(16, 4, 64, 16, [700, 2600], [64, 1], seed=98)]
+    for st in cases:
+        shape = shape_of(st)
+        import tests.gpu_util as gu
+        kp, vp = gu.bf16_dev(st.k_pool, torch), gu.bf16_dev(st.v_pool, torch)
+        q = gu.bf16_dev(st.q, torch)
+        runner = bd.StepRunner(shape).prepare(st.cu_seqlens_q, st.ctx_lens, st.block_table)
+        runner.write(gu.bf16_dev(st.k_new, torch), gu.bf16_dev(st.v_new, torch), kp, vp)
+        out = torch.zeros((st.T, st.Hq, st.D), dtype=torch.bfloat16, device="cuda")
+        runner.attend(q, kp, vp, out)
+        torch.cuda.synchronize()
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+        ev[0].record()
+        for _ in range(5):
+            runner.attend(q, kp, vp, out)
+        ev[1].record()
+        torch.cuda.synchronize()
+        assert runner.device_error() == 0
+        assert ev[0].elapsed_time(ev[1]) / 5 < 50.0, (st.name, ev[0].elapsed_time(ev[1]) / 5)
