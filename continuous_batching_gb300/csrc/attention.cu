@@ -511,7 +511,9 @@ __device__ __forceinline__ void st_shared_zero16(uint32_t addr) {
 struct Item {
     bool good;
     int seq, ctx, q_start, n_q, kvh, split, n_splits, pos0, k_begin, n_tiles, rows_valid;
-    int kind, tile0;    // PA_ITEM_*; GROUP / RESUME: the shared tiles [0, tile0) of split 0
+    int kind;           // PA_ITEM_*
+    int tile0;          // the item's first key tile within its split: a RESUME item's tile0
+                        // (it continues split 0 there), 0 for every other item
 };
 
 // What the producer publishes in an item slot (64 bytes); `last` marks the end of the CTA's
@@ -544,6 +546,23 @@ __device__ __forceinline__ Item slot_item(const volatile ItemSlot* sl, bool* las
 
 // Called by all 32 lanes of the producer warp (a GROUP item's members are checked one per
 // lane).
+// A GROUP item covers the decode rows of sequences seq .. seq + n_q - 1 at tokens q_start .. ,
+// each with keys past the shared tiles (which are read through seq's table). Lane i checks
+// member i; the warp agrees. Out of line, as it runs for GROUP items only.
+__device__ __noinline__ bool group_members_ok(const int32_t* cu, const int32_t* ctx, int B,
+                                              int bs, int max_blocks, int seq, int n_q,
+                                              int q_start, int tile0, int lane) {
+    bool good = seq + n_q <= B;
+    bool mine = true;
+    if (good && lane < n_q) {
+        const int s = seq + lane;
+        const int c0 = cu[s], c1 = cu[s + 1], cx = ctx[s];
+        mine = c1 - c0 == 1 && c0 == q_start + lane && cx > tile0 * kTileKeys &&
+               (int64_t(cx) + bs - 1) / bs <= max_blocks;
+    }
+    return __all_sync(0xffffffffu, good && mine);
+}
+
 __device__ __forceinline__ Item load_item(const Params& p, int idx, int lane) {
     const pa_work_item it = p.items[idx];
     Item I;
@@ -555,19 +574,10 @@ __device__ __forceinline__ Item load_item(const Params& p, int idx, int lane) {
                  (shared && it.split == 0 && it.n_splits <= 1 && it.tile0 >= 1 &&
                   it.tile0 < kSplitTiles && p.ws_acc != nullptr));
     I.kind = good ? it.kind : PA_ITEM_PLAIN;
-    I.tile0 = good && shared ? it.tile0 : 0;
+    I.tile0 = good && it.kind == PA_ITEM_RESUME ? it.tile0 : 0;
     if (good && it.kind == PA_ITEM_GROUP) {
-        // the decode rows of sequences seq .. seq + n_q - 1 at tokens q_start .. , each with
-        // keys past the shared tiles; the shared tiles are read through seq's table
-        good = it.seq + it.n_q <= p.B;
-        bool mine = true;
-        if (good && lane < it.n_q) {
-            const int s = it.seq + lane;
-            const int c0 = p.cu[s], c1 = p.cu[s + 1], cx = p.ctx[s];
-            mine = c1 - c0 == 1 && c0 == it.q_start + lane && cx > it.tile0 * kTileKeys &&
-                   (int64_t(cx) + p.bs - 1) / p.bs <= p.max_blocks;
-        }
-        good = __all_sync(0xffffffffu, good && mine);
+        good = group_members_ok(p.cu, p.ctx, p.B, p.bs, p.max_blocks, it.seq, it.n_q,
+                                it.q_start, it.tile0, lane);
         I.good = good;
         I.seq = it.seq;
         I.ctx = it.tile0 * kTileKeys;        // every tile of the item is a whole tile of keys
@@ -799,10 +809,12 @@ __device__ __forceinline__ void rescale_half(uint32_t tm_o, const float alpha[2]
 // finished here (out = bf16(O * (rcp(l) * v_scale))); a row spanning several splits stores this split's
 // partial (acc = O, m, l) for the fixed-order combine. Rows are those of a tile whose first
 // row is token q_start at position pos0 (rows_valid rows, g heads per token).
+// A GROUP item (save) stores every valid row as the partial of split 0, whatever the row's
+// own position: the state its RESUME item restores and continues.
 template <int D>
 __device__ __forceinline__ void store_half(const Params& p, const uint32_t* o, int r0, int rs,
                                            int q4, int rows_valid, int q_start, int kvh,
-                                           int split, const Rows2& R) {
+                                           int split, const Rows2& R, bool save) {
 #pragma unroll
     for (int sr = 0; sr < 2; ++sr) {
         const int row = r0 + rs + 8 * sr;
@@ -812,7 +824,7 @@ __device__ __forceinline__ void store_half(const Params& p, const uint32_t* o, i
         if (split >= nsp) continue;              // the row has no keys in this split
         const int tok = q_start + row / p.g;
         const int head = kvh * p.g + row % p.g;
-        if (nsp == 1) {
+        if (nsp == 1 && !save) {
             const float inv = __fmul_rn(__frcp_rn(R.l[sr]), p.v_scale);
             __nv_bfloat16* dst = p.out + (int64_t(tok) * p.Hq + head) * D;
 #pragma unroll
@@ -835,54 +847,34 @@ __device__ __forceinline__ void store_half(const Params& p, const uint32_t* o, i
     }
 }
 
-// End of a GROUP item: each valid row's state (accumulator O, already in registers as for
-// store_half, reference maximum m and sum l) goes to the row's split-0 slot of the workspace,
-// exactly as a split partial would, for the RESUME item that continues the row.
+// Start of a RESUME item: the rows' state saved by their GROUP item is restored, (m, l) into the
+// returned rows and the accumulator into the item's O buffer (TMEM address tm_o, lane offset
+// included), so that the row continues its split exactly where it would have been without the
+// sharing. Out of line: it runs once per RESUME item, and inlined it would sit in the body of
+// the persistent loop that every other item runs.
 template <int D>
-__device__ __forceinline__ void save_half(const Params& p, const uint32_t* o, int r0, int rs,
-                                          int q4, int rows_valid, int q_start, int kvh,
-                                          const Rows2& R) {
-#pragma unroll
-    for (int sr = 0; sr < 2; ++sr) {
-        const int row = r0 + rs + 8 * sr;
-        if (row >= rows_valid) continue;
-        const int tok = q_start + row / p.g;
-        const int64_t slot = int64_t(tok) * p.max_splits * p.Hq + kvh * p.g + row % p.g;
-        float* acc = p.ws_acc + slot * D;
-#pragma unroll
-        for (int cc = 0; cc < D / 8; ++cc)
-            *reinterpret_cast<float2*>(acc + 8 * cc + 2 * q4) =
-                make_float2(__uint_as_float(o[4 * cc + 2 * sr]),
-                            __uint_as_float(o[4 * cc + 2 * sr + 1]));
-        if (q4 == 0)
-            *reinterpret_cast<float2*>(p.ws_ml + slot * 2) = make_float2(R.m[sr], R.l[sr]);
-    }
-}
-
-// Start of a RESUME item: the rows' state saved by their GROUP item is restored, (m, l) into R
-// and the accumulator into the item's O buffer (TMEM address tm_o, lane offset included), so
-// that the row continues its split exactly where it would have been without the sharing.
-template <int D>
-__device__ __forceinline__ void restore_half(const Params& p, uint32_t tm_o, int r0, int rs,
-                                             int q4, int rows_valid, int q_start, int kvh,
-                                             int pos0, Rows2& R) {
+__device__ __noinline__ Rows2 restore_half(const float* ws_acc, const float* ws_ml, int g,
+                                           int max_splits, int Hq, uint32_t tm_o, int r0, int rs,
+                                           int q4, int rows_valid, int q_start, int kvh,
+                                           int pos0) {
+    Rows2 R;
     uint32_t o[D / 2];
 #pragma unroll
     for (int sr = 0; sr < 2; ++sr) {
         const int row = r0 + rs + 8 * sr;
         const bool valid = row < rows_valid;
-        R.pos[sr] = valid ? pos0 + row / p.g : -1;
+        R.pos[sr] = valid ? pos0 + row / g : -1;
         R.m[sr] = -INFINITY;
         R.l[sr] = 0.f;
-        const int64_t slot = valid ? int64_t(q_start + row / p.g) * p.max_splits * p.Hq +
-                                         kvh * p.g + row % p.g
+        const int64_t slot = valid ? int64_t(q_start + row / g) * max_splits * Hq + kvh * g +
+                                         row % g
                                    : 0;
         if (valid) {
-            const float2 ml = *reinterpret_cast<const float2*>(p.ws_ml + slot * 2);
+            const float2 ml = *reinterpret_cast<const float2*>(ws_ml + slot * 2);
             R.m[sr] = ml.x;
             R.l[sr] = ml.y;
         }
-        const float* acc = p.ws_acc + slot * D;
+        const float* acc = ws_acc + slot * D;
 #pragma unroll
         for (int cc = 0; cc < D / 8; ++cc) {
             const float2 v = valid ? *reinterpret_cast<const float2*>(acc + 8 * cc + 2 * q4)
@@ -894,6 +886,7 @@ __device__ __forceinline__ void restore_half(const Params& p, uint32_t tm_o, int
     if constexpr (D == 128) tmem_st_16x256b_x16(tm_o, o);
     else tmem_st_16x256b_x8(tm_o, o);
     tmem_wait_st();
+    return R;
 }
 
 // Running result of a prefill tile's splits 0 .. j-1, per row: reference maximum and sum
@@ -1252,8 +1245,7 @@ __global__ void __launch_bounds__(kThreadsFor<F8>, 1)
                 // has released it)
                 // (a RESUME item's first tile continues its split: it accumulates onto the
                 // restored O)
-                const int jt0 = cv.I.kind == PA_ITEM_RESUME ? cv.I.tile0 : 0;
-                const bool cont = ((jt0 + cv.jt) & (kSplitTiles - 1)) != 0;
+                const bool cont = ((cv.I.tile0 + cv.jt) & (kSplitTiles - 1)) != 0;
                 if (cv.have && cv.tc < cs.tc &&
                     mbar_test_wait(bar(kPFull + (cv.tc & 1)), (cv.tc >> 1) & 1) &&
                     (cont || cv.sg < 2 ||
@@ -1483,26 +1475,27 @@ __global__ void __launch_bounds__(kThreadsFor<F8>, 1)
             const bool on = r0 < I.rows_valid;    // warp-uniform: the warp holds a valid row
             Rows2 R;
             Fold2 F;
-            // a RESUME item starts inside split 0, at tile tile0
-            const int jt0 = I.kind == PA_ITEM_RESUME ? I.tile0 : 0;
+            // a RESUME item starts inside split 0, at tile tile0 (0 for every other item)
+            const int jt0 = I.tile0;
+            if (jt0 > 0) {
+                // the state its GROUP item saved (that item is earlier on this CTA's list; its
+                // O buffer was released by these warps' own epilogue two splits ago)
+                if (ng == 0) {
+                    if (tid == 0 && p.err) atomicOr(p.err, PA_DEVERR_META);
+                } else if (!(ok = wait_bounded(bar(kSaved), (ng - 1) & 1, abort_word))) {
+                    break;
+                }
+                if (on)
+                    R = restore_half<D>(p.ws_acc, p.ws_ml, p.g, p.max_splits, p.Hq,
+                                        tmem + kTmemO + (sg & 1) * 128 + lanes, r0, rs, q4,
+                                        I.rows_valid, I.q_start, I.kvh, I.pos0);
+            }
             for (int jt = 0; jt < I.n_tiles; ++jt, ++tc) {
                 // every split starts afresh, exactly as an item of that split alone would
                 const int jin = (jt0 + jt) & (kSplitTiles - 1);
                 if (jin == 0) rows_init(R, r0, rs, I.rows_valid, I.pos0, p.g);
                 const int ob = sg & 1;
                 const uint32_t tm_o = tmem + kTmemO + ob * 128 + lanes;
-                if (jt == 0 && jt0 > 0) {
-                    // the state its GROUP item saved (that item is earlier on this CTA's list;
-                    // its O buffer was released by these warps' own epilogue two splits ago)
-                    if (ng == 0) {
-                        if (tid == 0 && p.err) atomicOr(p.err, PA_DEVERR_META);
-                    } else if (!(ok = wait_bounded(bar(kSaved), (ng - 1) & 1, abort_word))) {
-                        break;
-                    }
-                    if (on)
-                        restore_half<D>(p, tm_o, r0, rs, q4, I.rows_valid, I.q_start, I.kvh,
-                                        I.pos0, R);
-                }
                 if (!(ok = wait_bounded(bar(kSFull + (tc & (SK - 1))), (tc >> kLog2SK) & 1,
                                         abort_word)))
                     break;
@@ -1570,11 +1563,8 @@ __global__ void __launch_bounds__(kThreadsFor<F8>, 1)
                     tmem_wait_ld();
                     tc_fence_before();
                     mbar_arrive(bar(kOFree + ob));       // O is in registers: its buffer is free
-                    if (I.kind == PA_ITEM_GROUP)
-                        save_half<D>(p, o, r0, rs, q4, I.rows_valid, I.q_start, I.kvh, R);
-                    else
-                        store_half<D>(p, o, r0, rs, q4, I.rows_valid, I.q_start, I.kvh, I.split,
-                                      R);
+                    store_half<D>(p, o, r0, rs, q4, I.rows_valid, I.q_start, I.kvh, I.split, R,
+                                  I.kind == PA_ITEM_GROUP);
                 }
                 if (I.kind == PA_ITEM_GROUP) {
                     // the saved state is published to the RESUME items (other threads of these
