@@ -199,12 +199,23 @@ def make_config(name: str, with_pool: bool = True, seed: Optional[int] = None) -
         return _finish(name, rng, Hq, Hkv, D, bs, nb, ctx, np.ones(B, np.int32), table,
                        with_pool, seed, notes={"long_positions": long_pos.tolist()})
     # prefix
-    Hq, Hkv, D, bs = 32, 8, 128, 16
-    P, G, prompt = 16, 8, 1024
-    shared_per = prompt // bs
-    cont = rng.integers(1, 3000, size=P * G, endpoint=True).astype(np.int32)
-    ctx = (prompt + cont).astype(np.int32)
-    own = _blocks_for(cont, bs)
+    return make_prefix_step(32, 8, 128, 16, prompts=16, samples=8, prompt_tokens=1024,
+                            cont_max=3000, seed=seed, with_pool=with_pool, rng=rng)
+
+
+def make_prefix_step(Hq: int, Hkv: int, D: int, block_size: int, prompts: int, samples: int,
+                     prompt_tokens: int, cont_max: int, seed: int, with_pool: bool = True,
+                     rng: Optional[np.random.Generator] = None, name: str = "prefix") -> Step:
+    """Decode rows of `prompts` x `samples` sequences: each sample's table starts with its
+    prompt's prompt_tokens // block_size full blocks (shared by the prompt's `samples` tables)
+    followed by its own blocks for a U[1, cont_max]-token continuation (ctx = prompt_tokens +
+    continuation); one decode row each, blocks a seeded permutation of the pool."""
+    rng = np.random.default_rng(seed) if rng is None else rng
+    bs, P, G = block_size, prompts, samples
+    shared_per = prompt_tokens // bs
+    cont = rng.integers(1, cont_max, size=P * G, endpoint=True).astype(np.int32)
+    ctx = (prompt_tokens + cont).astype(np.int32)
+    own = _blocks_for(ctx, bs) - shared_per
     nb = int(P * shared_per + own.sum())
     perm = rng.permutation(nb).astype(np.int32)
     mb = int(shared_per + own.max())
@@ -218,9 +229,9 @@ def make_config(name: str, with_pool: bool = True, seed: Optional[int] = None) -
             table[i, :shared_per] = shared
             table[i, shared_per:shared_per + n] = perm[off:off + n]
             off += n
-    return _finish("prefix", rng, Hq, Hkv, D, bs, nb, ctx, np.ones(P * G, np.int32), table,
+    return _finish(name, rng, Hq, Hkv, D, bs, nb, ctx, np.ones(P * G, np.int32), table,
                    with_pool, seed, shared_blocks=P * shared_per,
-                   notes={"prompts": P, "samples": G, "prompt_tokens": prompt})
+                   notes={"prompts": P, "samples": G, "prompt_tokens": prompt_tokens})
 
 
 def make_step(Hq: int, Hkv: int, D: int, block_size: int, ctx_lens, n_q, seed: int,

@@ -80,3 +80,21 @@ def assert_close(got_bits: np.ndarray, want: np.ndarray, what: str = ""):
     assert r.max() <= 1.0, (f"{what}: (row, head) {worst} off by {r.max():.2f} x "
                             f"(REL * rms + floor)")
     return float(d.max()), float(d.mean()), float(r.max())
+
+
+def attend_with_plan(st, kp, vp, items, torch):
+    """Attention of step st over pools kp / vp (already written) with a given plan."""
+    shape = bd.Shape.make(st.Hq, st.Hkv, st.D, st.block_size, st.num_blocks)
+    dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
+    q = dev(st.q.view(np.int16)).view(torch.bfloat16)
+    out = torch.full((st.T, st.Hq, st.D), float("nan"), dtype=torch.bfloat16, device="cuda")
+    max_ctx = int(st.ctx_lens.max())
+    ws = torch.empty((bd.pa_workspace_bytes(shape, st.T, max_ctx) + 3) // 4, dtype=torch.float32,
+                     device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    bd.paged_attention_step(q, kp, vp, dev(st.block_table), dev(st.cu_seqlens_q),
+                            dev(st.ctx_lens), max_ctx,
+                            dev(items.view(np.int32).reshape(-1)), ws, out, shape, err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    return out.view(torch.int16).cpu().numpy()

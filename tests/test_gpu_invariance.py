@@ -8,7 +8,7 @@ import pytest
 
 from continuous_batching_gb300 import binding as bd
 from continuous_batching_gb300 import workloads as wl
-from tests.gpu_util import pool_np, run_step
+from tests.gpu_util import attend_with_plan, pool_np, run_step
 
 pytestmark = pytest.mark.gpu
 torch = pytest.importorskip("torch")
@@ -132,24 +132,6 @@ def test_repeat_runs_are_bitwise_deterministic():
     assert np.array_equal(a, b) and np.array_equal(b, c)
 
 
-def _attend_with_plan(st, kp, vp, items, torch):
-    """Attention of step st over pools kp / vp (already written) with a given plan."""
-    shape = bd.Shape.make(st.Hq, st.Hkv, st.D, st.block_size, st.num_blocks)
-    dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
-    q = dev(st.q.view(np.int16)).view(torch.bfloat16)
-    out = torch.full((st.T, st.Hq, st.D), float("nan"), dtype=torch.bfloat16, device="cuda")
-    max_ctx = int(st.ctx_lens.max())
-    ws = torch.empty((bd.pa_workspace_bytes(shape, st.T, max_ctx) + 3) // 4, dtype=torch.float32,
-                     device="cuda")
-    err = torch.zeros(1, dtype=torch.int32, device="cuda")
-    bd.paged_attention_step(q, kp, vp, dev(st.block_table), dev(st.cu_seqlens_q),
-                            dev(st.ctx_lens), max_ctx,
-                            dev(items.view(np.int32).reshape(-1)), ws, out, shape, err)
-    torch.cuda.synchronize()
-    assert int(err.item()) == 0
-    return out.view(torch.int16).cpu().numpy()
-
-
 def test_prefix_groups_give_the_bits_of_plain_items():
     """Samples that share a prompt's blocks, planned with GROUP / RESUME items (the shared tiles
     read once for all of them, each row's softmax state carried across) and with PLAIN items
@@ -162,8 +144,8 @@ def test_prefix_groups_give_the_bits_of_plain_items():
     shared = bd.pa_plan_step_shared(shape, sub.cu_seqlens_q, sub.ctx_lens, sub.block_table)
     assert np.sum(shared["kind"] == bd.PA_ITEM_GROUP) == 4 * sub.Hkv
     plain = bd.pa_plan_step(shape, sub.cu_seqlens_q, sub.ctx_lens)
-    got_shared = _attend_with_plan(sub, kp, vp, shared, torch)
-    got_plain = _attend_with_plan(sub, kp, vp, plain, torch)
+    got_shared = attend_with_plan(sub, kp, vp, shared, torch)
+    got_plain = attend_with_plan(sub, kp, vp, plain, torch)
     assert np.array_equal(got_shared, got_plain)
     assert np.array_equal(out.view(np.int16), got_plain)
     # a sample alone (no group at all) and a group of two
@@ -171,5 +153,5 @@ def test_prefix_groups_give_the_bits_of_plain_items():
         one, rows = wl.subset(sub, idx)
         items = bd.pa_plan_step_shared(shape, one.cu_seqlens_q, one.ctx_lens, one.block_table)
         assert np.sum(items["kind"] == bd.PA_ITEM_GROUP) == (sub.Hkv if len(idx) == 2 else 0)
-        alone = _attend_with_plan(one, kp, vp, items, torch)
+        alone = attend_with_plan(one, kp, vp, items, torch)
         assert np.array_equal(alone, got_plain[np.concatenate(rows)])
