@@ -9,7 +9,7 @@ import pytest
 import oracle.paged_attention as pa
 from continuous_batching_gb300 import binding as bd
 from continuous_batching_gb300 import workloads as wl
-from tests.gpu_util import assert_close, bf16_dev, pool_np, shape_of
+from tests.gpu_util import assert_close, attend_with_plan, bf16_dev, pool_np, shape_of
 
 pytestmark = pytest.mark.gpu
 torch = pytest.importorskip("torch")
@@ -208,3 +208,41 @@ def test_pipeline_of_different_steps_equals_direct_launches():
     ref = pa.attention(step2.q, pool_np(kp, torch), pool_np(vp, torch), step2.block_table,
                        step2.cu_seqlens_q, step2.ctx_lens, step2.Hq)
     assert_close(host[-1][3].numpy().view(np.uint16), ref, "pipeline")
+
+
+def test_pipeline_runs_prefix_shared_steps():
+    """Two consecutive decode steps of samples that share their prompts' blocks, through
+    StepPipeline (which plans with GROUP / RESUME items): each step's output has the bits of the
+    same step planned with plain items only, and the second matches the oracle."""
+    full = wl.make_prefix_step(32, 8, 128, 16, prompts=3, samples=6, prompt_tokens=768,
+                               cont_max=2600, seed=41)
+    rng = np.random.default_rng(42)
+    step1, _ = wl.subset(full, range(full.B), name="step1")
+    step1.ctx_lens = (full.ctx_lens - 1).astype(np.int32)
+    step1.q = wl.random_bf16(rng, step1.q.shape)
+    step1.k_new = wl.random_bf16(rng, step1.k_new.shape)
+    step1.v_new = wl.random_bf16(rng, step1.v_new.shape)
+    shape = shape_of(full)
+    for st in (step1, full):
+        items = bd.pa_plan_step_shared(shape, st.cu_seqlens_q, st.ctx_lens, st.block_table)
+        assert np.sum(items["kind"] == bd.PA_ITEM_GROUP) == 3 * full.Hkv
+    kp, vp = bf16_dev(full.k_pool, torch), bf16_dev(full.v_pool, torch)
+    lim = bd.StepLimits(B=full.B, T=full.T, max_blocks=full.block_table.shape[1],
+                        max_ctx=int(full.ctx_lens.max()))
+    pipe = bd.StepPipeline(shape, lim, kp, vp)
+    pin = lambda a: torch.from_numpy(a.view(np.int16).copy()).pin_memory()
+    host = [(pin(st.q), pin(st.k_new), pin(st.v_new),
+             torch.empty((st.T, st.Hq, st.D), dtype=torch.int16).pin_memory())
+            for st in (step1, full)]
+    events = [pipe.submit(st.cu_seqlens_q, st.ctx_lens, st.block_table, *h)
+              for st, h in zip((step1, full), host)]
+    for ev in events:
+        ev.synchronize()
+    assert pipe.device_error() == 0
+    # the second step's write lands past the first step's keys, so the final pools serve both
+    for st, h in zip((step1, full), host):
+        plain = bd.pa_plan_step(shape, st.cu_seqlens_q, st.ctx_lens)
+        assert np.array_equal(h[3].numpy(), attend_with_plan(st, kp, vp, plain, torch)), st.name
+    ref = pa.attention(full.q, pool_np(kp, torch), pool_np(vp, torch), full.block_table,
+                       full.cu_seqlens_q, full.ctx_lens, full.Hq)
+    assert_close(host[-1][3].numpy().view(np.uint16), ref, "pipeline, prefix-shared")
