@@ -15,13 +15,17 @@ Inputs are resident in HBM before timing. The decode K/V pools (0.84 GB) exceed 
 so no flush runs between timed steps; a workload whose K/V fit in L2 twice over (prefill
 segments) is flushed by a 256 MiB write between timed steps. Timing: CUDA events on the
 launching stream around each step, W untimed warm-up steps, max over ranks. The timed steps
-replay CUDA graphs captured from the same library calls (KV write; attention + combine), so
-no host launch overhead sits inside the timed region; the e2e leg goes through the public
-API call by call, from host buffers, planning included.
+replay CUDA graphs captured from the same library calls, so no host launch overhead sits
+inside the timed region: the step is one graph (the KV write, then attention + combine as its
+programmatic dependents, as the library's pipeline runs a step); the attention kernels alone
+(the roofline) are timed in a second pass, their graph between the events and the write's
+outside. The e2e leg runs steps through the public pipeline from host buffers, planning
+included.
 
 The default run also reports, each under its own key with its own roofline, clocks and
 launch count: decode_16k (32 decode rows at ctx 16,384), prefill_segments (the mixed step's
-four 512-row prefill segments, tensor roofline) and longtail (the long-tail rollout decode).
+four 512-row prefill segments, tensor roofline), longtail (the long-tail rollout decode) and
+prefix_shared (samples sharing their prompts' blocks; roofline on the unique K/V bytes).
 
 The CPU baseline (and --impl reference) times the oracle (fp64 numpy, as it stands) on every
 host core: a spawn-started process pool over shared memory, whole passes over the same
@@ -260,6 +264,10 @@ class GpuStep:
                                                  self.out, attend=False)
         self.g_attend = self.graph_runner.capture(self.q, self.kn, self.vn, self.kp, self.vp,
                                                   self.out, write=False)
+        # and the whole step in one graph, as the library's pipeline runs it: the attention is
+        # launched as a programmatic dependent of the KV write, so its start overlaps the write
+        self.g_step = self.graph_runner.capture(self.q, self.kn, self.vn, self.kp, self.vp,
+                                                self.out)
         # pinned host copies for the end-to-end measurement, and the public pipeline that runs
         # steps from them (two buffer sets, so that one step's host work and copies overlap the
         # kernels of the step before it)
@@ -312,31 +320,40 @@ def hold_gpu(torch, seconds: float) -> None:
 
 
 def time_steps(g: GpuStep, torch, steps: int, warmup: int, flush, attn_only=False):
-    """Per-step CUDA events (L2 flushed before each step when `flush` is given, outside the
-    events) around replays
-    of the captured step graphs. Returns (per-step ms list, per-attention-call ms list)."""
+    """Per-step CUDA events around replays of the captured graphs, L2 flushed before each step
+    when `flush` is given (outside the events). First the whole step as one graph (the KV write,
+    then the attention as its programmatic dependent, as the library's pipeline runs a step),
+    then the attention kernels alone: the write graph outside the events, the attention graph
+    between them. Returns (per-step ms list, per-attention-call ms list)."""
     s = torch.cuda.current_stream()
     for _ in range(warmup):
+        g.g_step.replay()
         g.g_write.replay()
         g.g_attend.replay()
     torch.cuda.synchronize()
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
-           torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(2 * steps)]
     # hold the GPU (outside every timed interval) while the host queues all timed steps, so
     # that no interval includes the GPU waiting for the host to enqueue the next graph
-    hold_gpu(torch, 1e-3 + 3e-4 * steps)
+    hold_gpu(torch, 1e-3 + 6e-4 * steps)
     for i in range(steps):
         if flush is not None:
             flush.zero_()
-        a, b, c = ev[i]
+        a, c = ev[i]
         a.record(s)
+        g.g_step.replay()
+        c.record(s)
+    for i in range(steps):
+        if flush is not None:
+            flush.zero_()
         g.g_write.replay()
+        b, c = ev[steps + i]
         b.record(s)
         g.g_attend.replay()
         c.record(s)
     torch.cuda.synchronize()
-    step_ms = [a.elapsed_time(c) for a, b, c in ev]
-    attn_ms = [b.elapsed_time(c) for a, b, c in ev]
+    step_ms = [a.elapsed_time(c) for a, c in ev[:steps]]
+    attn_ms = [b.elapsed_time(c) for b, c in ev[steps:]]
     return step_ms, attn_ms
 
 
