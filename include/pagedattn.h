@@ -299,7 +299,9 @@ int32_t pa_plan_step(const pa_shape* shape, int32_t B, const int32_t* cu_seqlens
 /* pa_plan_step with prefix sharing (same output for steps without it): runs of consecutive
  * decode sequences (one query row each, at most 128 / group of them) whose block tables
  * [B, max_blocks] agree on the blocks of at least two leading key tiles become GROUP and
- * RESUME items (see pa_work_item) for every KV head, their splits past 0 PLAIN items. A
+ * RESUME items (see pa_work_item) for every KV head, their splits past 0 PLAIN items. The
+ * shared tiles are whole tiles of split 0 below every member's last key (at most
+ * PA_SPLIT_TOKENS / PA_TILE_KEYS - 1 of them), so that each RESUME item has keys of its own. A
  * group's items (GROUP, then its RESUMEs) are dealt to one list as a unit; the balance rule is
  * otherwise that of pa_plan_step. Since a group's items share one list, such a plan can have
  * fewer lists than min(items, PA_PLAN_CTAS); its padding items (n_q == 0) then take indices
@@ -400,10 +402,11 @@ int32_t paged_attention_step_wait_test(const void* q, const void* k_pool, const 
  * each owns device metadata, q / k_new / v_new / out buffers, a workspace, pinned host
  * metadata, and a CUDA graph of its KV write (paged_kv_write, or paged_kv_write_fp8) and
  * attention (paged_attention_step, or its fp8 form) captured once at creation. A submission
- * plans the step on the host (pa_plan_step, pa_compute_slots into the slot's pinned
- * metadata), then queues the uploads of the metadata and of the caller's q / k_new / v_new
- * on one stream, the graph on a second (after the uploads, and after the previous step's
- * kernels), and the read of the output into the caller's buffer on a third. One step's host
+ * plans the step on the host (pa_plan_step_shared, so that samples sharing a prompt's blocks
+ * read them once, and pa_compute_slots, into the slot's pinned metadata), then queues the
+ * uploads of the metadata and of the caller's q / k_new / v_new on one stream, the graph on a
+ * second (after the uploads, and after the previous step's kernels), and the read of the
+ * output into the caller's buffer on a third. One step's host
  * work and copies so overlap the kernels of the step before it; the kernels run in
  * submission order. Not thread-safe; one pipeline per device and host thread. */
 typedef struct pa_pipeline pa_pipeline;
@@ -418,8 +421,8 @@ int32_t pa_pipeline_create(const pa_shape* shape, int32_t B, int32_t T, int32_t 
                            float k_scale, float v_scale, pa_pipeline** out);
 /* Waits for the pipeline's outstanding steps and frees everything it allocated (NULL ignored). */
 int32_t pa_pipeline_destroy(pa_pipeline* p);
-/* Bytes of metadata a submission uploads (the plan padded to pa_plan_max_items, cu_seqlens_q,
- * ctx_lens, the table at max_blocks columns and the slots), or -1 for NULL. */
+/* Bytes of metadata a submission uploads (the plan padded to pa_plan_max_items_shared,
+ * cu_seqlens_q, ctx_lens, the table at max_blocks columns and the slots), or -1 for NULL. */
 int64_t pa_pipeline_meta_bytes(const pa_pipeline* p);
 /* Queues one step. Host inputs: cu_seqlens_q [B+1] (cu[B] == T), ctx_lens [B] (each <=
  * max_ctx), block_table [B * table_cols] row-major (table_cols <= max_blocks); h_q [T, Hq, D],
