@@ -51,6 +51,11 @@ def _stale(target: str, sources: list) -> bool:
     return any(os.path.getmtime(s) > t for s in sources)
 
 
+# what the last build() in this process did: the translation units it compiled (the others were
+# up to date) and whether it linked the library
+LAST_BUILD = {}
+
+
 def build(force: bool = False, verbose: bool = False) -> str:
     os.makedirs(BUILD, exist_ok=True)
     cc = nvcc()
@@ -76,10 +81,14 @@ def build(force: bool = False, verbose: bool = False) -> str:
 
     with ThreadPoolExecutor(max_workers=max(1, len(jobs))) as ex:
         list(ex.map(run, jobs))
-    if force or jobs or _stale(LIB, objs):
+    linked = bool(force or jobs or _stale(LIB, objs))
+    if linked:
         tmp = LIB + ".tmp"
         run([cc] + ARCH + ["-shared", "-o", tmp] + objs)
         os.replace(tmp, LIB)
+    LAST_BUILD.clear()
+    LAST_BUILD.update(compiled=[os.path.basename(j[-3]) for j in jobs], linked=linked,
+                      arch=" ".join(ARCH), library=LIB)
     return LIB
 
 
