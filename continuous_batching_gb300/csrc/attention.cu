@@ -209,6 +209,34 @@ __device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 
+__device__ __forceinline__ void prefetch_l2(const void* a) {
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(a));
+}
+
+// Warms L2 with the step metadata a CTA reads first, before the grid dependency wait: its first
+// work item, and, dealt out over the grid's CTAs and a warp's lanes, the 128-byte lines of
+// cu_seqlens_q, ctx_lens and the block table (up to 8 lines a lane). The dependent reads
+// after the wait (item, then the sequence's metadata, then its table window) then hit L2. A
+// prefetch loads nothing into registers: a preceding kernel's writes to these arrays are still
+// what the reads after the wait see.
+__device__ __forceinline__ void prefetch_step_meta(const pa_work_item* items, int n_items,
+                                                   const int32_t* cu, const int32_t* ctx,
+                                                   const int32_t* table, int B, int max_blocks,
+                                                   int lane) {
+    const int c = int(blockIdx.x);
+    if (lane == 0 && items && c < n_items) prefetch_l2(items + c);
+    if (!cu || !ctx || !table || B <= 0 || max_blocks <= 0) return;
+    const int64_t l_cu = (int64_t(B) + 1 + 31) / 32, l_ctx = (int64_t(B) + 31) / 32;
+    const int64_t l_tab = (int64_t(B) * max_blocks + 31) / 32;
+    const int64_t total = l_cu + l_ctx + l_tab;
+    const int64_t stride = int64_t(gridDim.x) * 32;
+    int64_t l = int64_t(c) * 32 + lane;
+    for (int k = 0; k < 8 && l < total; ++k, l += stride)
+        prefetch_l2(l < l_cu ? cu + l * 32
+                    : l < l_cu + l_ctx ? ctx + (l - l_cu) * 32
+                                       : table + (l - l_cu - l_ctx) * 32);
+}
+
 __device__ __forceinline__ unsigned long long global_ns() {
     unsigned long long t;
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
@@ -1012,6 +1040,9 @@ __global__ void __launch_bounds__(kThreadsFor<F8>, 1)
     const int lane = threadIdx.x & 31;
     const auto bar = [&](int b) { return bars + 8 * b; };
 
+    if (warp == 8)
+        prefetch_step_meta(p.items, p.n_items, p.cu, p.ctx, p.block_table, p.B, p.max_blocks,
+                           lane);
     if (threadIdx.x == 0) {
         for (int b = 0; b < kNumBars; ++b)
             mbar_init(bars + 8 * b,
