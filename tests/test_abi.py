@@ -340,3 +340,62 @@ def test_shared_plan_needs_two_whole_shared_tiles():
     assert len(items) == 32 + bd.PA_PLAN_CTAS - 8
     assert all(L for L in lists[:8]) and not any(lists[8:])
     assert sorted(i for L in lists for i in L) == np.flatnonzero(items["n_q"] != 0).tolist()
+
+
+def _check_shared_plan(shape, cu, ctx, table):
+    """Plans with sharing, checks that every (row, KV head) gets each of its key tiles exactly
+    once and that the plan's lists hold every real item once; returns the items."""
+    from types import SimpleNamespace
+    items = bd.pa_plan_step_shared(shape, cu, ctx, table)
+    st = SimpleNamespace(cu_seqlens_q=cu, ctx_lens=ctx, T=int(cu[-1]), Hkv=shape.num_kv_heads)
+    cov, pos_of = _tiles_covered(items, st)
+    for t in range(st.T):
+        for h in range(st.Hkv):
+            assert sorted(cov[(t, h)]) == list(range(int(pos_of[t]) // bd.PA_TILE_KEYS + 1))
+    lists = walk(items, len(items))
+    assert sorted(i for L in lists for i in L) == np.flatnonzero(items["n_q"] != 0).tolist()
+    return items
+
+
+def test_shared_plan_groups_stop_at_the_row_limit_and_at_other_rows():
+    """At g = 16 a tile holds 8 decode rows: 20 sequences sharing a prompt form groups of 8, 8
+    and 4. A prefill row between samples of one prompt ends the run, and a later run of the
+    same prompt forms a group of its own."""
+    shape = bd.Shape.make(16, 1, 128, 16, 1 << 14)
+    rng = np.random.default_rng(7)
+    B = 20
+    ctx = (512 + rng.integers(1, 700, size=B)).astype(np.int32)
+    cu = np.arange(B + 1, dtype=np.int32)
+    table = (np.arange(B * 96, dtype=np.int32).reshape(B, 96) + 64)
+    table[:, :32] = np.arange(32)                                 # 512 tokens = 4 tiles shared
+    items = _check_shared_plan(shape, cu, ctx, table)
+    groups = items[items["kind"] == bd.PA_ITEM_GROUP]
+    assert sorted(groups["n_q"].tolist()) == [4, 8, 8] and np.all(groups["tile0"] == 4)
+    # sequence 5 becomes a 10-row prefill chunk between the samples
+    n_q = np.ones(B, np.int32)
+    n_q[5] = 10
+    cu2 = np.concatenate([[0], np.cumsum(n_q)]).astype(np.int32)
+    items = _check_shared_plan(shape, cu2, ctx, table)
+    groups = items[items["kind"] == bd.PA_ITEM_GROUP]
+    assert sorted((int(g["seq"]), int(g["n_q"])) for g in groups) == [(0, 5), (6, 8), (14, 6)]
+    assert not np.any((items["kind"] != bd.PA_ITEM_PLAIN) & (items["seq"] == 5))
+
+
+def test_shared_plan_tiles_stop_at_split_0_and_at_every_members_last_key():
+    """A 4096-token shared prompt: the group takes the first 15 tiles (split 0 keeps one for
+    each RESUME item), later splits are PLAIN items. A sample whose context ends 600 tokens in
+    limits the group to the 4 whole tiles below its last key."""
+    shape = bd.Shape.make(32, 8, 128, 16, 1 << 14)
+    ctx = np.array([5000, 4500, 4200], np.int32)
+    cu = np.arange(4, dtype=np.int32)
+    table = np.arange(3 * 320, dtype=np.int32).reshape(3, 320) + 256
+    table[:, :256] = np.arange(256)                              # 4096 tokens shared
+    items = _check_shared_plan(shape, cu, ctx, table)
+    groups = items[items["kind"] == bd.PA_ITEM_GROUP]
+    assert len(groups) == 8 and np.all(groups["tile0"] == 15) and np.all(groups["n_q"] == 3)
+    res = items[items["kind"] == bd.PA_ITEM_RESUME]
+    assert len(res) == 24 and np.all(res["n_tiles"] == 1)
+    ctx[1] = 600
+    items = _check_shared_plan(shape, cu, ctx, table)
+    groups = items[items["kind"] == bd.PA_ITEM_GROUP]
+    assert len(groups) == 8 and np.all(groups["tile0"] == 4)
