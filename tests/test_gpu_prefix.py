@@ -2,10 +2,10 @@
 RESUME items (each shared tile read once for the whole group, every row's softmax state carried
 from the GROUP item to its RESUME item) give the bits of the same step planned with plain items
 only, and stay within the tolerance of the fp64 oracle. Cases cover head_dim 64 and 128, block
-sizes 16 to 64, one, four and eight q heads per KV head, groups up to the 128-row limit (and a
-prompt with more samples than one group holds), prompts that are not a whole number of blocks,
-rows past the first split (their later splits are plain items, folded by the combine), and an
-fp8 cache."""
+sizes 16 to 64, one, four, eight and sixteen q heads per KV head, groups up to the 128-row
+limit (and a prompt with more samples than one group holds), prompts that are not a whole
+number of blocks, rows past the first split (their later splits are plain items, folded by the
+combine), and an fp8 cache."""
 import numpy as np
 import pytest
 
@@ -39,6 +39,7 @@ CASES = [
     (16, 4, 64, 32, 2, 40, 256, 1500, 202),     # 40 samples: groups of 32 (the row limit) + 8
     (8, 8, 128, 64, 2, 3, 1920, 3000, 203),     # g = 1, 15 shared tiles (the most split 0 holds)
     (16, 2, 64, 16, 4, 2, 300, 700, 204),       # g = 8; 18 whole blocks = 2 whole tiles shared
+    (16, 1, 128, 16, 2, 10, 512, 900, 206),     # g = 16: a group of 8 fills a tile's 128 rows
 ]
 
 
